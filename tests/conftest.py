@@ -1,0 +1,23 @@
+"""Shared pytest configuration.
+
+``gpu`` marks tests that need a CUDA device (a GB300, sm_103a); the CPU suite
+runs with ``-m "not gpu"``.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a)")
+    config.addinivalue_line("markers", "slow: full-size GPU parity cases")
+
+
+@pytest.fixture(scope="session")
+def golden_dir():
+    return os.path.join(ROOT, "tests", "golden")
