@@ -1,0 +1,385 @@
+"""Benchmark of the owner-side Muon step on GB300 (prints one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--e2e-steps E] [--no-cpu-baseline]
+
+A step is one dmuon_step over every matrix of the workload (momentum,
+Nesterov input, normalisation, 5 quintic Newton-Schulz iterations, update),
+with W, G and M resident in HBM.  Metric: algorithmic TFLOP/s, counting per
+matrix 5*(3 m^2 n + m^3) flops (symmetric products as one triangle), plus
+matrices/s.  Inputs (83.8 GB of fp32 W/G/M for the Llama-3-8B set) are far
+larger than the 129 MB L2, so no flush is needed between steps.
+
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample
+of the same workload, on this machine's host cores.
+
+Multi-GPU (torchrun): every rank runs the whole workload as an independent
+replica (the matrices of a step are independent units; there is no exchange
+step on one owner), so scaling is weak; timing is max over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--workload", default="llama3_8b")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                return json.load(f), "measured"
+        except Exception:
+            pass
+    return None, "fallback"
+
+
+def tensor_peak():
+    pk, src = measured_peaks()
+    if pk:
+        for key in ("bf16_tflops_sustained", "bf16_tflops"):
+            if key in pk and pk[key]:
+                return float(pk[key]), "of measured (%s)" % key
+    return FALLBACK_BF16_TFLOPS_SUSTAINED, "of fallback (sustained bf16, 1.7 PFLOP/s)"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_median": statistics.median(
+                    [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()] or [0.0])}
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_sample(workload):
+    """Bounded CPU sample of a workload: layer-0 q, k, v of the Llama set,
+    else the first matrices up to a similar flop budget."""
+    from newton_schulz_nesterov_gb300 import workloads
+    w = workloads.get(workload)
+    if workload == "llama3_8b":
+        return [0, 1, 2], "layer-0 q (4096x4096), k, v (1024x4096): 3 of 224 matrices"
+    budget, idx, tot = 2.5e12, [], 0
+    for i, (r, c) in enumerate(w.shapes):
+        m, n = min(r, c), max(r, c)
+        f = 5 * (4 * m * m * n + 2 * m ** 3)
+        if idx and tot + f > budget:
+            break
+        idx.append(i)
+        tot += f
+    return idx, "first %d of %d matrices" % (len(idx), len(w.shapes))
+
+
+def time_oracle(workload, indices, reps=1):
+    import numpy as np
+    import oracle
+    from newton_schulz_nesterov_gb300 import workloads, flops
+    w = workloads.get(workload)
+    data = []
+    for i in indices:
+        data.append((workloads.weight(w, i).numpy(), workloads.grad(w, i, 0).numpy(),
+                     workloads.momentum(w, i).numpy()))
+    shapes = [w.shapes[i] for i in indices]
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        for W, G, M in data:
+            oracle.muon_step(W, G, M, lr=float(np.float32(0.02)), mu=float(np.float32(0.95)))
+        times.append(time.perf_counter() - t0)
+    return times, flops.algorithmic_flops(shapes), len(indices)
+
+
+def cpu_threads():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    idx, desc = oracle_sample(args.workload)
+    for _ in range(args.warmup):
+        time_oracle(args.workload, idx, 1)
+    times, fl, nm = time_oracle(args.workload, idx, args.steps)
+    tot = sum(times)
+    value = fl * len(times) / tot / 1e12
+    cores = cpu_threads()
+    line = {
+        "impl": "reference", "metric": "muon_step_tflops", "value": value,
+        "unit": "TFLOP/s (algorithmic)", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "matrices_per_s": nm * len(times) / tot,
+        "config": {"workload": args.workload, "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s (algorithmic)", "cores": cores,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s (algorithmic)", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import newton_schulz_nesterov_gb300 as dm
+    from newton_schulz_nesterov_gb300 import _build, workloads, flops
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    _build.build()
+    w = workloads.get(args.workload)
+    n = len(w.shapes)
+    shapes = list(w.shapes)
+    lr, mu = 0.02, 0.95
+
+    Ws = [workloads.weight(w, i, dev) for i in range(n)]
+    Ms = [workloads.momentum(w, i, dev) for i in range(n)]
+    h = dm.Handle(local_rank)
+    for step in range(w.warm_steps):
+        Gw = [workloads.grad(w, i, step, dev) for i in range(n)]
+        h.step(Ws, Gw, Ms, lr=lr, mu=mu)
+        del Gw
+    Gs = [workloads.grad(w, i, w.warm_steps, dev) for i in range(n)]
+    torch.cuda.synchronize()
+    resident = sum(3 * 4 * r * c for r, c in shapes)
+
+    stream = torch.cuda.current_stream()
+    wp = [t.data_ptr() for t in Ws]
+    gp = [t.data_ptr() for t in Gs]
+    mp = [t.data_ptr() for t in Ms]
+
+    def one_step():
+        dm.dmuon_step_ptrs(h.h, wp, gp, mp, shapes, lr, mu, 5, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        one_step()
+    rc, _ = h.status()
+    if rc != 0:
+        raise RuntimeError("warm-up status %d" % rc)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- timed region (device time with CUDA events on the launch stream)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    dm.dmuon_profile_read(h.h)
+    dm.dmuon_profile_enable(h.h, True)
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = dm.dmuon_launch_count(h.h)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = dm.dmuon_launch_count(h.h) - launches0
+    dm.dmuon_profile_enable(h.h, False)
+    prof = dm.dmuon_profile_read(h.h)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    rc, _ = h.status()
+    if rc != 0:
+        raise RuntimeError("timed status %d" % rc)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    sec = ms / 1e3
+    fl = flops.algorithmic_flops(shapes)
+    value = fl * args.steps * world / sec / 1e12
+
+    # ---- dominant kernel roofline (B*X apply phase; tensor-bound)
+    peak, peak_src = tensor_peak()
+    apply_ms, apply_n = prof["apply"]
+    roofline = None
+    if apply_n:
+        per_launch_flops = flops.apply_flops(shapes, 1)
+        achieved = per_launch_flops / (apply_ms / apply_n / 1e3) / 1e12
+        roofline = {"kernel": "ns_gemm_kernel<Apply> (B*X + a*X)", "bound": "tensor",
+                    "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "peak_source": peak_src, "traffic": None}
+    phase = {k: {"ms_per_launch": (v[0] / v[1]) if v[1] else None, "launches": v[1]}
+             for k, v in prof.items() if v[1]}
+    mom_ms = prof["momentum"][0] / max(1, prof["momentum"][1])
+    hbm_peak = FALLBACK_HBM_GBS
+    pk, _ = measured_peaks()
+    if pk and pk.get("hbm_gbs"):
+        hbm_peak = float(pk["hbm_gbs"])
+    phase["momentum"]["achieved_gbs"] = flops.elementwise_bytes(shapes) / (mom_ms / 1e3) / 1e9
+    phase["momentum"]["frac_of_hbm"] = phase["momentum"]["achieved_gbs"] / hbm_peak
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        e2e = run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world)
+
+    line = {
+        "metric": "muon_step_tflops", "value": value, "unit": "TFLOP/s (algorithmic)",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "matrices_per_s": n * args.steps * world / sec,
+        "dense_equiv_tflops": flops.dense_flops(shapes) * args.steps * world / sec / 1e12,
+        "config": {"workload": args.workload, "matrices": n, "ns_steps": 5,
+                   "resident_bytes": resident,
+                   "l2": "inputs larger than L2 (%.1f GB resident W/G/M)" % (resident / 1e9),
+                   "parallelism": "replicas x%d" % world if world > 1 else "single GPU"},
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "phases": phase,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        idx, desc = oracle_sample(args.workload)
+        times, sfl, nm = time_oracle(args.workload, idx, 1)
+        line["cpu_baseline"] = {"value": sfl / times[0] / 1e12, "unit": "TFLOP/s (algorithmic)",
+                                "cores": cpu_threads(), "kind": "oracle", "sample": desc,
+                                "seconds": times[0]}
+    h.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world):
+    """Same step through the public API, with this step's gradients copied in
+    from pinned host memory and the updated weights read back to the host
+    inside the timed region (W and M stay resident as optimizer state)."""
+    import torch
+    import newton_schulz_nesterov_gb300 as dm
+    try:
+        Gh = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in Gs]
+        Wh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in Ws]
+    except Exception as ex:  # host memory too small for pinned copies
+        return {"value": None, "unit": "TFLOP/s (algorithmic)", "error": str(ex)[:200]}
+    for g, gh in zip(Gs, Gh):
+        gh.copy_(g)
+    torch.cuda.synchronize()
+    h2d = sum(g.numel() * 4 for g in Gs)
+    d2h = sum(x.numel() * 4 for x in Ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        for g, gh in zip(Gs, Gh):
+            g.copy_(gh, non_blocking=True)
+        h.step(Ws, Gs, Ms, lr=0.02, mu=0.95, stream=stream)
+        for x, xh in zip(Ws, Wh):
+            xh.copy_(x, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3
+    del Gh, Wh
+    return {"value": fl * args.e2e_steps * world / sec / 1e12, "unit": "TFLOP/s (algorithmic)",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "ms_per_step": 1e3 * sec / args.e2e_steps}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,188 @@
+/*
+ * dmuon.h -- C ABI of the GB300 (sm_103a) owner-side Muon step.
+ *
+ * One call runs, for every matrix of a packed list of mixed-shape fp32
+ * matrices, the step that the owner rank of a Muon-target weight performs
+ * (DMuon "HSDP Training", section "What Happens Under the Hood": the owner
+ * runs momentum, Newton-Schulz, weight decay and the update):
+ *
+ *   M <- mu*M + G                                  (momentum, fp32)
+ *   U  = G + mu*M   (nesterov=1)   or   U = M      (Nesterov input)
+ *   Y  = U^T if rows > cols else U                 (orientation rule)
+ *   X  = Y / (||Y||_F + eps)                       (Frobenius normalisation)
+ *   repeat ns_steps times with per-step (a,b,c):   (quintic Newton-Schulz)
+ *       A = X X^T;  B = b*A + c*A*A;  X = a*X + B*X
+ *   O  = X^T if transposed else X
+ *   W <- (1 - lr*wd)*W - lr*scale(rows,cols)*O     (decoupled decay + update)
+ *
+ * Passages: DMuon "API Reference", section "Muon" (signature defaults
+ * lr=0.02, momentum=0.95, weight_decay=0.0, ns_steps=5, nesterov=True; the
+ * nesterov argument's note on the lookahead input); section
+ * "direct_newton_schulz" (the recurrence, eps=1e-7, coefficient list length
+ * = iteration count); section "gram_newton_schulz_factors" (normaliser
+ * = norm + eps under the orientation rule); section "YOU_COEFFICIENTS" (the
+ * default five-row table used here).
+ *
+ * Precision: momentum and the update are fp32; the Newton-Schulz products
+ * run on bf16 tensor cores with fp32 accumulation, with X, A, B held in bf16
+ * between products; the last iteration's output goes to the update in fp32.
+ *
+ * Threading/streams: a handle is not thread-safe.  Calls on one handle are
+ * asynchronous on the given stream and must be issued on one stream (or be
+ * ordered by the caller), because they share the handle's workspace.
+ *
+ * Return codes: 0 on success, a negative DMUON_ERR_* otherwise.  Every
+ * argument check happens on the host before anything is launched, so an
+ * error return means no kernel of that call ran.
+ */
+#ifndef DMUON_H
+#define DMUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define DMUON_OK               0
+#define DMUON_ERR_ARG         -1  /* null pointer, bad size, bad option      */
+#define DMUON_ERR_ALIGN       -2  /* a matrix pointer is not 16-byte aligned  */
+#define DMUON_ERR_OOM         -3  /* workspace allocation failed              */
+#define DMUON_ERR_CUDA        -4  /* a CUDA runtime/driver call failed        */
+#define DMUON_ERR_NONFINITE   -5  /* an input matrix held Inf/NaN             */
+#define DMUON_ERR_TIMEOUT     -6  /* a kernel's bounded wait ran out          */
+#define DMUON_ERR_UNSUPPORTED -7  /* device is not compute capability 10.3    */
+
+/* Largest accepted sizes: any side up to 2^20, short side up to 32768. */
+#define DMUON_MAX_DIM        (1 << 20)
+#define DMUON_MAX_SHORT_SIDE 32768
+#define DMUON_MAX_NS_STEPS   64
+
+/* Shape of one weight matrix: rows x cols, fp32, contiguous row-major
+ * (the layout of a PyTorch nn.Linear weight, [out_features, in_features]). */
+typedef struct {
+    int64_t rows;
+    int64_t cols;
+} dmuon_shape_t;
+
+/* Options of a step; dmuon_default_opts() fills the pages' defaults. */
+typedef struct {
+    float weight_decay;   /* Muon weight decay; default 0.0                */
+    float eps;            /* normalisation epsilon; default 1e-7           */
+    int   nesterov;       /* 1 = Nesterov lookahead input (default), 0 = M */
+    int   scale_mode;     /* update scale: 0 = sqrt(max(1, rows/cols))
+                           * (default), 1 = 1, 2 = 0.2*sqrt(max(rows,cols)) */
+    const float* coeffs;  /* NULL: the YOU_COEFFICIENTS rows, last row
+                           * repeated past five steps; else host memory of
+                           * ns_steps rows of (a, b, c), row-major          */
+} dmuon_opts_t;
+
+/* Opaque handle: owns the workspace, the plan cache and the status flags. */
+typedef struct dmuon_ctx* dmuon_handle_t;
+
+/* Fill *opts with the defaults (weight_decay 0, eps 1e-7, nesterov 1,
+ * scale_mode 0, coeffs NULL).  No-op on NULL. */
+void dmuon_default_opts(dmuon_opts_t* opts);
+
+/* Create a handle on CUDA device `device` (which becomes current for the
+ * calling thread).  Returns DMUON_ERR_UNSUPPORTED unless the device has
+ * compute capability 10.3.  *out is set to NULL on failure. */
+int dmuon_create(dmuon_handle_t* out, int device);
+
+/* Free the handle and its workspace (synchronises the device first).
+ * NULL is a no-op. */
+void dmuon_destroy(dmuon_handle_t h);
+
+/* Bytes of device workspace a step over `shapes` needs (bf16 X ping/pong,
+ * A and B per matrix, plus small per-matrix arrays).  Host only. */
+int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats,
+                          size_t* out_bytes);
+
+/*
+ * One owner-side Muon step over n_mats matrices (see the top of this file).
+ *
+ *   params[i]   device, fp32 rows_i x cols_i, updated in place   (W)
+ *   grads[i]    device, fp32 rows_i x cols_i, read only          (G)
+ *   momentum[i] device, fp32 rows_i x cols_i, updated in place   (M)
+ *   shapes[i]   host
+ *   params, grads, momentum, shapes: host arrays of n_mats entries.
+ *   lr, mu      Muon learning rate and momentum coefficient.
+ *   ns_steps    number of Newton-Schulz iterations, 0..DMUON_MAX_NS_STEPS.
+ *   opts        NULL = defaults.
+ *   stream      a cudaStream_t (NULL = legacy default stream).
+ *
+ * The caller owns all matrix memory; pointers must be 16-byte aligned and
+ * the three matrices of one entry must not overlap.  n_mats == 0 returns
+ * DMUON_OK without launching.  The first call with a new shape list plans
+ * and allocates the workspace (synchronous); later calls with the same
+ * shapes only launch.  Asynchronous: completion and non-finite detection
+ * are observed through dmuon_get_status().
+ */
+int dmuon_step(dmuon_handle_t h, float* const* params,
+               const float* const* grads, float* const* momentum,
+               const dmuon_shape_t* shapes, int n_mats, float lr, float mu,
+               int ns_steps, const dmuon_opts_t* opts, void* stream);
+
+/*
+ * Standalone Newton-Schulz orthogonalisation (DMuon "API Reference",
+ * section "direct_newton_schulz"): outputs[i] = O of inputs[i], same shape,
+ * fp32.  inputs[i] and outputs[i] are device fp32 rows_i x cols_i,
+ * 16-byte aligned, and may not overlap.  coeffs: NULL = default table as in
+ * dmuon_opts_t, else ns_steps host rows of (a,b,c).  eps <= 0 selects 1e-7.
+ */
+int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs,
+                        float* const* outputs, const dmuon_shape_t* shapes,
+                        int n_mats, int ns_steps, const float* coeffs,
+                        float eps, void* stream);
+
+/*
+ * Wait for the handle's stream work to finish and report what the kernels
+ * recorded since the previous call of this function: per-matrix flags of
+ * the last planned list (bit 0: non-finite input) are copied to
+ * flags[0..min(n_flags, n_mats)) when flags != NULL, then cleared.
+ * Returns DMUON_ERR_TIMEOUT if a kernel's bounded wait ran out,
+ * DMUON_ERR_NONFINITE if any flag is set, DMUON_OK otherwise.
+ */
+int dmuon_get_status(dmuon_handle_t h, int* flags, int n_flags);
+
+/* Kernel launches issued by this handle since creation (a counter). */
+int64_t dmuon_launch_count(dmuon_handle_t h);
+
+/*
+ * Per-phase CUDA-event timing (the counterpart of the pages'
+ * record_step_profile / consume_last_step_profile, DMuon "API Reference",
+ * section "Muon").  While enabled, each launch is bracketed by events on
+ * its stream.  dmuon_profile_read() synchronises, then adds the elapsed
+ * milliseconds and launch counts per kernel kind into ms[k] and count[k]
+ * for k < n_kinds (kinds: 0 momentum+norm, 1 norm finalise, 2 Gram X X^T,
+ * 3 A*A, 4 B*X (+update), 5 update without NS) and resets the record.
+ */
+#define DMUON_KIND_MOMENTUM 0
+#define DMUON_KIND_FINALIZE 1
+#define DMUON_KIND_GRAM     2
+#define DMUON_KIND_GRAM2    3
+#define DMUON_KIND_APPLY    4
+#define DMUON_KIND_UPDATE0  5
+#define DMUON_NUM_KINDS     6
+int dmuon_profile_enable(dmuon_handle_t h, int on);
+int dmuon_profile_read(dmuon_handle_t h, double* ms, int64_t* count,
+                       int n_kinds);
+
+/* Human-readable description of the current plan (matrices, work items
+ * per phase, workspace bytes) into buf (NUL-terminated, truncated to len).
+ * Returns the full length needed. */
+int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len);
+
+/* Static string for a status code. */
+const char* dmuon_error_string(int code);
+
+/* Library version string. */
+const char* dmuon_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMUON_H */

@@ -1,0 +1,291 @@
+"""Python binding of libdmuon.so, the GB300 (sm_103a) owner-side Muon step.
+
+Argument marshalling only: every step of the Muon update runs in the
+library's CUDA kernels.  The functions keep the C names of
+``include/dmuon.h``; PyTorch tensors are accepted for convenience (their
+device pointers and shapes are passed through), raw device pointers with
+explicit shapes are accepted by the ``*_ptrs`` variants.
+
+There is no CPU fallback: if ``lib/libdmuon.so`` has not been built,
+``load()`` raises.
+"""
+import ctypes
+import os
+
+__all__ = [
+    "DmuonError", "load", "lib_path", "dmuon_create", "dmuon_destroy",
+    "dmuon_step", "dmuon_step_ptrs", "dmuon_newton_schulz",
+    "dmuon_newton_schulz_ptrs", "dmuon_get_status", "dmuon_workspace_bytes",
+    "dmuon_launch_count", "dmuon_profile_enable", "dmuon_profile_read",
+    "dmuon_plan_summary", "dmuon_error_string", "dmuon_version", "Handle",
+    "KIND_NAMES", "STATUS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "lib", "libdmuon.so")
+_lib = None
+
+STATUS = {
+    0: "DMUON_OK", -1: "DMUON_ERR_ARG", -2: "DMUON_ERR_ALIGN", -3: "DMUON_ERR_OOM",
+    -4: "DMUON_ERR_CUDA", -5: "DMUON_ERR_NONFINITE", -6: "DMUON_ERR_TIMEOUT",
+    -7: "DMUON_ERR_UNSUPPORTED",
+}
+KIND_NAMES = ("momentum", "finalize", "gram", "gram2", "apply", "update0")
+
+
+class DmuonError(RuntimeError):
+    def __init__(self, code, what=""):
+        self.code = code
+        msg = "%s (%d)" % (STATUS.get(code, "unknown"), code)
+        if _lib is not None:
+            msg += ": " + _lib.dmuon_error_string(code).decode()
+        super().__init__(what + ": " + msg if what else msg)
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [("weight_decay", ctypes.c_float), ("eps", ctypes.c_float),
+                ("nesterov", ctypes.c_int), ("scale_mode", ctypes.c_int),
+                ("coeffs", ctypes.POINTER(ctypes.c_float))]
+
+
+def lib_path():
+    return _LIB_PATH
+
+
+def load(path=None):
+    """Load libdmuon.so (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError("libdmuon.so not built (%s); run __graft_entry__.build()" % p)
+    L = ctypes.CDLL(p)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    L.dmuon_default_opts.argtypes = [ctypes.POINTER(Opts)]
+    L.dmuon_default_opts.restype = None
+    L.dmuon_create.argtypes = [ctypes.POINTER(vp), i32]
+    L.dmuon_create.restype = i32
+    L.dmuon_destroy.argtypes = [vp]
+    L.dmuon_destroy.restype = None
+    L.dmuon_workspace_bytes.argtypes = [ctypes.POINTER(Shape), i32, ctypes.POINTER(ctypes.c_size_t)]
+    L.dmuon_workspace_bytes.restype = i32
+    L.dmuon_step.argtypes = [vp, pp, pp, pp, ctypes.POINTER(Shape), i32, f32, f32, i32,
+                             ctypes.POINTER(Opts), vp]
+    L.dmuon_step.restype = i32
+    L.dmuon_newton_schulz.argtypes = [vp, pp, pp, ctypes.POINTER(Shape), i32, i32,
+                                      ctypes.POINTER(ctypes.c_float), f32, vp]
+    L.dmuon_newton_schulz.restype = i32
+    L.dmuon_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), i32]
+    L.dmuon_get_status.restype = i32
+    L.dmuon_launch_count.argtypes = [vp]
+    L.dmuon_launch_count.restype = i64
+    L.dmuon_profile_enable.argtypes = [vp, i32]
+    L.dmuon_profile_enable.restype = i32
+    L.dmuon_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double),
+                                     ctypes.POINTER(ctypes.c_int64), i32]
+    L.dmuon_profile_read.restype = i32
+    L.dmuon_plan_summary.argtypes = [vp, ctypes.c_char_p, ctypes.c_size_t]
+    L.dmuon_plan_summary.restype = i32
+    L.dmuon_error_string.argtypes = [i32]
+    L.dmuon_error_string.restype = ctypes.c_char_p
+    L.dmuon_version.argtypes = []
+    L.dmuon_version.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(code, what):
+    if code != 0:
+        raise DmuonError(code, what)
+
+
+def _ptr_array(ptrs):
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))()
+    for i, p in enumerate(ptrs):
+        arr[i] = int(p)
+    return arr
+
+
+def _shape_array(shapes):
+    arr = (Shape * max(1, len(shapes)))()
+    for i, (r, c) in enumerate(shapes):
+        arr[i].rows, arr[i].cols = int(r), int(c)
+    return arr
+
+
+def _coeff_array(coeffs):
+    if coeffs is None:
+        return None
+    flat = [float(v) for row in coeffs for v in row]
+    return (ctypes.c_float * max(1, len(flat)))(*flat)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _tensor_args(tensors, name):
+    ptrs, shapes = [], []
+    for t in tensors:
+        if t.dim() != 2 or not t.is_cuda or not t.is_contiguous() or str(t.dtype) != "torch.float32":
+            raise ValueError("%s: each matrix must be a contiguous 2-D float32 CUDA tensor" % name)
+        ptrs.append(t.data_ptr())
+        shapes.append(tuple(t.shape))
+    return ptrs, shapes
+
+
+# ---------------------------------------------------------------- C calls
+
+def dmuon_version():
+    return load().dmuon_version().decode()
+
+
+def dmuon_error_string(code):
+    return load().dmuon_error_string(int(code)).decode()
+
+
+def dmuon_create(device=0):
+    h = ctypes.c_void_p()
+    _check(load().dmuon_create(ctypes.byref(h), int(device)), "dmuon_create")
+    return h
+
+
+def dmuon_destroy(h):
+    if h is not None:
+        load().dmuon_destroy(h)
+
+
+def dmuon_workspace_bytes(shapes):
+    out = ctypes.c_size_t(0)
+    _check(load().dmuon_workspace_bytes(_shape_array(shapes), len(shapes), ctypes.byref(out)),
+           "dmuon_workspace_bytes")
+    return out.value
+
+
+def dmuon_step_ptrs(h, w_ptrs, g_ptrs, m_ptrs, shapes, lr, mu, ns_steps=5,
+                    weight_decay=0.0, eps=1e-7, nesterov=True, scale_mode=0,
+                    coeffs=None, stream=None, check=True):
+    """dmuon_step on raw device pointers; returns the status code."""
+    L = load()
+    opts = Opts()
+    L.dmuon_default_opts(ctypes.byref(opts))
+    opts.weight_decay = float(weight_decay)
+    opts.eps = float(eps)
+    opts.nesterov = 1 if nesterov else 0
+    opts.scale_mode = int(scale_mode)
+    carr = _coeff_array(coeffs)
+    if carr is not None:
+        opts.coeffs = ctypes.cast(carr, ctypes.POINTER(ctypes.c_float))
+    rc = L.dmuon_step(h, _ptr_array(w_ptrs), _ptr_array(g_ptrs), _ptr_array(m_ptrs),
+                      _shape_array(shapes), len(shapes), float(lr), float(mu), int(ns_steps),
+                      ctypes.byref(opts), ctypes.c_void_p(_stream_handle(stream)))
+    if check:
+        _check(rc, "dmuon_step")
+    return rc
+
+
+def dmuon_step(h, params, grads, momentum, lr=0.02, mu=0.95, ns_steps=5, **kw):
+    """One Muon step over lists of CUDA fp32 tensors (updated in place)."""
+    wp, ws = _tensor_args(params, "params")
+    gp, gs = _tensor_args(grads, "grads")
+    mp, ms = _tensor_args(momentum, "momentum")
+    if ws != gs or ws != ms:
+        raise ValueError("params, grads and momentum must have matching shapes")
+    return dmuon_step_ptrs(h, wp, gp, mp, ws, lr, mu, ns_steps, **kw)
+
+
+def dmuon_newton_schulz_ptrs(h, in_ptrs, out_ptrs, shapes, ns_steps=5, coeffs=None,
+                             eps=1e-7, stream=None, check=True):
+    L = load()
+    carr = _coeff_array(coeffs)
+    rc = L.dmuon_newton_schulz(h, _ptr_array(in_ptrs), _ptr_array(out_ptrs), _shape_array(shapes),
+                               len(shapes), int(ns_steps),
+                               None if carr is None else ctypes.cast(carr, ctypes.POINTER(ctypes.c_float)),
+                               float(eps), ctypes.c_void_p(_stream_handle(stream)))
+    if check:
+        _check(rc, "dmuon_newton_schulz")
+    return rc
+
+
+def dmuon_newton_schulz(h, inputs, outputs, ns_steps=5, coeffs=None, eps=1e-7, stream=None):
+    ip, is_ = _tensor_args(inputs, "inputs")
+    op, os_ = _tensor_args(outputs, "outputs")
+    if is_ != os_:
+        raise ValueError("inputs and outputs must have matching shapes")
+    return dmuon_newton_schulz_ptrs(h, ip, op, is_, ns_steps, coeffs, eps, stream)
+
+
+def dmuon_get_status(h, n_flags=0):
+    """Synchronise and return (status_code, per-matrix flags list)."""
+    flags = (ctypes.c_int * max(1, n_flags))()
+    rc = load().dmuon_get_status(h, flags, int(n_flags))
+    return rc, [flags[i] for i in range(n_flags)]
+
+
+def dmuon_launch_count(h):
+    return int(load().dmuon_launch_count(h))
+
+
+def dmuon_profile_enable(h, on=True):
+    _check(load().dmuon_profile_enable(h, 1 if on else 0), "dmuon_profile_enable")
+
+
+def dmuon_profile_read(h):
+    """{kind: (ms_total, launches)} accumulated since the last read."""
+    n = len(KIND_NAMES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _check(load().dmuon_profile_read(h, ms, cnt, n), "dmuon_profile_read")
+    return {KIND_NAMES[k]: (ms[k], cnt[k]) for k in range(n)}
+
+
+def dmuon_plan_summary(h):
+    L = load()
+    need = L.dmuon_plan_summary(h, None, 0)
+    buf = ctypes.create_string_buffer(need + 1)
+    L.dmuon_plan_summary(h, buf, need + 1)
+    return buf.value.decode()
+
+
+class Handle:
+    """Owning wrapper of a dmuon handle (destroyed on close / exit)."""
+
+    def __init__(self, device=0):
+        self.h = dmuon_create(device)
+
+    def close(self):
+        if self.h is not None:
+            dmuon_destroy(self.h)
+            self.h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def step(self, params, grads, momentum, lr=0.02, mu=0.95, ns_steps=5, **kw):
+        return dmuon_step(self.h, params, grads, momentum, lr, mu, ns_steps, **kw)
+
+    def newton_schulz(self, inputs, outputs, ns_steps=5, coeffs=None, eps=1e-7, stream=None):
+        return dmuon_newton_schulz(self.h, inputs, outputs, ns_steps, coeffs, eps, stream)
+
+    def status(self, n_flags=0):
+        return dmuon_get_status(self.h, n_flags)

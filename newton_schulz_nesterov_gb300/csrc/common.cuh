@@ -1,0 +1,127 @@
+// Shared device-side types and PTX helpers of the GB300 Muon step.
+//
+// Plan-time descriptors (one per matrix), per-call pointers, the work-item
+// encoding of the tensor-core phases and thin inline-PTX wrappers for
+// mbarrier, TMA (cp.async.bulk.tensor) and tcgen05 (MMA, TMEM).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dmuon {
+
+// ---------------------------------------------------------------------------
+// Descriptors
+// ---------------------------------------------------------------------------
+
+// One matrix of the packed list, oriented so that the Newton-Schulz iterate
+// X is m x n with m <= n (m = short side).  X, A and B live in the handle's
+// workspace; W, G, M are the caller's (see MatPtrs).
+struct MatDesc {
+  int64_t rows, cols;      // weight shape (row-major fp32)
+  int64_t m, n;            // oriented iterate shape, m = min(rows, cols)
+  int64_t ldx;             // leading dimension (elements) of X buffers
+  int64_t lda;             // leading dimension (elements) of A and B
+  __nv_bfloat16* X[2];     // ping/pong iterate, m x n row-major
+  __nv_bfloat16* A;        // Gram X X^T, m x m
+  __nv_bfloat16* B;        // b*A + c*A*A, m x m
+  int64_t tile0;           // first momentum tile of this matrix
+  int32_t tiles_c;         // momentum tiles along cols
+  int32_t transposed;      // rows > cols
+  float scale;             // update scale of this matrix
+  float pad_;
+};
+
+// Caller pointers of one call (uploaded only when they change).
+struct MatPtrs {
+  float* W;        // parameters (dmuon_step) or output O (newton_schulz)
+  const float* G;  // gradient / NS input
+  float* M;        // momentum buffer (unused by newton_schulz)
+  void* pad_;
+};
+
+// Momentum/normalisation tile: 64 x 64 fp32 elements of W's shape.
+constexpr int kMomTile = 64;
+
+// Work item of a tensor-core phase: {matrix, 128-row tile, 256-col tile,
+// number of 64-wide K blocks}.
+// Tensor-core tile: 128 rows (UMMA M) x 256 cols (UMMA N), K step 64.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;          // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+constexpr int kBox = 64;                        // TMA box is 64 x 64 bf16
+constexpr int kBoxBytes = kBox * kBox * 2;      // 8 KB
+constexpr int kGemmThreads = 192;               // TMA, MMA, 4 epilogue warps
+constexpr int kTmemCols = 512;                  // two 128x256 fp32 accumulators
+constexpr int kEpiWords = 32 * 17;              // per-warp transpose scratch
+constexpr int kGemmSmem =
+    1024 /*align slack*/ + kStages * kStageBytes + 4 * kEpiWords * 4 + 256;
+
+enum Phase : int { kPhaseGram = 0, kPhaseGram2 = 1, kPhaseApply = 2 };
+enum FinalMode : int { kWriteX = 0, kUpdateW = 1, kWriteO = 2 };
+
+// Tensor maps per matrix: X[0], X[1], A, B (box 64x64, 128B swizzle).
+constexpr int kMapsPerMat = 4;
+
+struct GemmArgs {
+  const MatDesc* mats;
+  const MatPtrs* ptrs;
+  const CUtensorMap* tmaps;
+  const int4* items;       // {mat, ti, tj, k_blocks}
+  int n_items;
+  int src;                 // X buffer holding the current iterate
+  float ca, cb, cc;        // this iteration's (a, b, c)
+  int first;               // first iteration: fold the norm scale in
+  int final_mode;          // Apply phase: kWriteX / kUpdateW / kWriteO
+  float lr, decay;         // W <- decay*W - lr*scale*O
+  const float* svec;       // per-matrix 1/(||U||_F + eps)
+  int* err;                // device error word (bit 0: wait timeout)
+};
+
+struct MomArgs {
+  const MatDesc* mats;
+  const MatPtrs* ptrs;
+  const int64_t* tile_prefix;  // n_mats + 1 entries
+  int n_mats;
+  int64_t n_tiles;
+  float mu;
+  int nesterov;
+  int ns_only;                 // 1: U = G (standalone NS), no momentum
+  float* partials;             // per-tile sum of squares of U
+};
+
+struct FinalizeArgs {
+  const MatDesc* mats;
+  const int64_t* tile_prefix;
+  const float* partials;
+  int n_mats;
+  float eps;
+  float* svec;
+  int* flags;
+};
+
+struct Update0Args {          // ns_steps == 0: O = s*U straight to W / out
+  const MatDesc* mats;
+  const MatPtrs* ptrs;
+  const int64_t* tile_prefix;
+  int n_mats;
+  int64_t n_tiles;
+  const float* svec;
+  float lr, decay;
+  int write_o;
+};
+
+// Host launchers (defined in the .cu files).
+cudaError_t launch_mom(const MomArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
+cudaError_t launch_update0(const Update0Args& a, int grid, cudaStream_t s);
+cudaError_t launch_gemm(int phase, const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t gemm_configure();
+
+}  // namespace dmuon

@@ -1,0 +1,567 @@
+// Host side of the C ABI declared in include/dmuon.h: argument checks,
+// planning (orientation, workspace layout, TMA descriptors, work lists),
+// per-call pointer upload and the launch sequence of one step.
+//
+// Launch sequence of one step (all on the caller's stream, no host sync):
+//   mom_norm    M <- mu*M + G, U, X0 = bf16(U or U^T), tile sums of U^2
+//   finalize    s = 1/(||U||_F + eps) per matrix
+//   ns_steps x [ Gram (A = X X^T) -> Gram2 (B = bA + cAA) -> Apply (X' = aX + BX) ]
+//   the last Apply updates W in place (or writes O for the standalone NS)
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/dmuon.h"
+#include "common.cuh"
+
+using namespace dmuon;
+
+namespace {
+
+// DMuon "API Reference", section YOU_COEFFICIENTS: the default table.
+const float kYouCoefficients[5][3] = {
+    {4.0848f, -6.8946f, 2.927f},
+    {3.9505f, -6.3029f, 2.6377f},
+    {3.7418f, -5.5913f, 2.3037f},
+    {2.8769f, -3.1427f, 1.2046f},
+    {2.8366f, -3.0525f, 1.2012f},
+};
+
+const char* kVersion = "dmuon-gb300 0.1.0 (sm_103a, tcgen05/TMA)";
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// bf16 row-major rows x cols with leading dimension ld (elements): 64x64
+// boxes, 128-byte swizzle, zero fill outside the matrix.
+bool encode_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)kBox, (cuuint32_t)kBox};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Layout {
+  std::vector<MatDesc> mats;       // device pointers filled in once allocated
+  std::vector<int64_t> xoff, aoff, boff;  // workspace byte offsets
+  std::vector<int64_t> tile_prefix;
+  size_t ws_bytes = 0;             // big bf16 workspace
+  size_t small_bytes = 0;          // descriptors, maps, lists, partials
+  std::vector<int4> items[3];
+};
+
+void make_layout(const dmuon_shape_t* shapes, int n, Layout& L) {
+  L.mats.assign(n, MatDesc{});
+  L.xoff.resize(n); L.aoff.resize(n); L.boff.resize(n);
+  L.tile_prefix.assign(n + 1, 0);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t o = off; off += (size_t)rup((int64_t)bytes, 256); return (int64_t)o; };
+  for (int i = 0; i < n; ++i) {
+    MatDesc& d = L.mats[i];
+    d.rows = shapes[i].rows;
+    d.cols = shapes[i].cols;
+    d.transposed = d.rows > d.cols ? 1 : 0;
+    d.m = std::min(d.rows, d.cols);
+    d.n = std::max(d.rows, d.cols);
+    d.ldx = rup(d.n, 8);
+    d.lda = rup(d.m, 8);
+    L.xoff[i] = take((size_t)(2 * d.m * d.ldx * 2));  // X[0] and X[1] back to back
+    L.aoff[i] = take((size_t)(d.m * d.lda * 2));
+    L.boff[i] = take((size_t)(d.m * d.lda * 2));
+    d.tiles_c = (int32_t)cdiv(d.cols, kMomTile);
+    d.tile0 = L.tile_prefix[i];
+    L.tile_prefix[i + 1] = L.tile_prefix[i] + cdiv(d.rows, kMomTile) * d.tiles_c;
+  }
+  L.ws_bytes = off;
+  // Work lists.  Symmetric phases: 256x256 super-tiles (I <= J), each as two
+  // 128-row halves; Apply: all 128x256 tiles of the m x n output.
+  for (int p = 0; p < 3; ++p) L.items[p].clear();
+  for (int i = 0; i < n; ++i) {
+    const MatDesc& d = L.mats[i];
+    const int64_t T = cdiv(d.m, 256);
+    const int kg = (int)cdiv(d.n, kBK), km = (int)cdiv(d.m, kBK);
+    for (int64_t I = 0; I < T; ++I)
+      for (int64_t J = I; J < T; ++J)
+        for (int h = 0; h < 2; ++h) {
+          const int64_t ti = 2 * I + h;
+          if (ti * kBM >= d.m) continue;
+          L.items[kPhaseGram].push_back(make_int4(i, (int)ti, (int)J, kg));
+          L.items[kPhaseGram2].push_back(make_int4(i, (int)ti, (int)J, km));
+        }
+    for (int64_t ti = 0; ti < cdiv(d.m, kBM); ++ti)
+      for (int64_t tj = 0; tj < cdiv(d.n, kBN); ++tj)
+        L.items[kPhaseApply].push_back(make_int4(i, (int)ti, (int)tj, km));
+  }
+  for (int p = 0; p < 3; ++p)
+    std::stable_sort(L.items[p].begin(), L.items[p].end(),
+                     [](const int4& x, const int4& y) { return x.w > y.w; });
+  const int64_t nt = L.tile_prefix[n];
+  L.small_bytes = rup(sizeof(MatDesc) * n, 256) + rup(sizeof(MatPtrs) * n, 256) +
+                  rup(sizeof(CUtensorMap) * kMapsPerMat * n, 256) + rup(8 * (n + 1), 256) +
+                  rup(4 * nt, 256) + 2 * rup(4 * n, 256) + 256 +
+                  rup(16 * (L.items[0].size() + L.items[1].size() + L.items[2].size()), 256);
+}
+
+}  // namespace
+
+struct ProfRec {
+  cudaEvent_t a, b;
+  int kind;
+};
+
+struct dmuon_ctx {
+  int device = 0;
+  int num_sms = 0;
+  // plan
+  std::vector<dmuon_shape_t> shapes;
+  Layout L;
+  void* ws = nullptr;
+  void* small = nullptr;
+  MatDesc* d_mats = nullptr;
+  MatPtrs* d_ptrs = nullptr;
+  CUtensorMap* d_maps = nullptr;
+  int64_t* d_prefix = nullptr;
+  float* d_partials = nullptr;
+  float* d_svec = nullptr;
+  int* d_flags = nullptr;
+  int* d_err = nullptr;
+  int4* d_items[3] = {nullptr, nullptr, nullptr};
+  // pointer cache
+  std::vector<MatPtrs> last_ptrs;
+  MatPtrs* h_stage = nullptr;
+  size_t h_stage_cap = 0;
+  cudaEvent_t stage_ev = nullptr;
+  bool stage_pending = false;
+  cudaStream_t last_stream = nullptr;
+  int64_t launches = 0;
+  bool profiling = false;
+  std::vector<ProfRec> prof;
+  std::vector<cudaEvent_t> ev_pool;
+};
+
+namespace {
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? DMUON_OK : (e == cudaErrorMemoryAllocation ? DMUON_ERR_OOM : DMUON_ERR_CUDA); }
+
+void free_plan(dmuon_ctx* h) {
+  if (h->ws || h->small) cudaDeviceSynchronize();
+  if (h->ws) cudaFree(h->ws);
+  if (h->small) cudaFree(h->small);
+  h->ws = h->small = nullptr;
+  h->shapes.clear();
+  h->last_ptrs.clear();
+}
+
+bool same_shapes(const dmuon_ctx* h, const dmuon_shape_t* s, int n) {
+  if ((int)h->shapes.size() != n || !h->small) return false;
+  for (int i = 0; i < n; ++i)
+    if (h->shapes[i].rows != s[i].rows || h->shapes[i].cols != s[i].cols) return false;
+  return true;
+}
+
+int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
+  if (same_shapes(h, shapes, n)) return DMUON_OK;
+  free_plan(h);
+  if (!get_encoder()) return DMUON_ERR_CUDA;
+  Layout& L = h->L;
+  make_layout(shapes, n, L);
+  cudaError_t e = cudaMalloc(&h->ws, std::max<size_t>(L.ws_bytes, 256));
+  if (e != cudaSuccess) { h->ws = nullptr; cudaGetLastError(); return DMUON_ERR_OOM; }
+  e = cudaMalloc(&h->small, L.small_bytes);
+  if (e != cudaSuccess) { cudaFree(h->ws); h->ws = h->small = nullptr; cudaGetLastError(); return DMUON_ERR_OOM; }
+  uint8_t* p = (uint8_t*)h->small;
+  auto carve = [&](size_t bytes) { uint8_t* q = p; p += rup((int64_t)bytes, 256); return q; };
+  const int64_t nt = L.tile_prefix[n];
+  h->d_mats = (MatDesc*)carve(sizeof(MatDesc) * n);
+  h->d_ptrs = (MatPtrs*)carve(sizeof(MatPtrs) * n);
+  h->d_maps = (CUtensorMap*)carve(sizeof(CUtensorMap) * kMapsPerMat * n);
+  h->d_prefix = (int64_t*)carve(8 * (n + 1));
+  h->d_partials = (float*)carve(4 * nt);
+  h->d_svec = (float*)carve(4 * n);
+  h->d_flags = (int*)carve(4 * n);
+  h->d_err = (int*)carve(256);
+  for (int q = 0; q < 3; ++q) h->d_items[q] = (int4*)carve(16 * L.items[q].size());
+
+  std::vector<CUtensorMap> maps(kMapsPerMat * (size_t)n);
+  uint8_t* ws = (uint8_t*)h->ws;
+  for (int i = 0; i < n; ++i) {
+    MatDesc& d = L.mats[i];
+    d.X[0] = (__nv_bfloat16*)(ws + L.xoff[i]);
+    d.X[1] = d.X[0] + d.m * d.ldx;
+    d.A = (__nv_bfloat16*)(ws + L.aoff[i]);
+    d.B = (__nv_bfloat16*)(ws + L.boff[i]);
+    d.scale = 1.f;
+    bool ok = encode_map(&maps[kMapsPerMat * i + 0], d.X[0], d.m, d.n, d.ldx) &&
+              encode_map(&maps[kMapsPerMat * i + 1], d.X[1], d.m, d.n, d.ldx) &&
+              encode_map(&maps[kMapsPerMat * i + 2], d.A, d.m, d.m, d.lda) &&
+              encode_map(&maps[kMapsPerMat * i + 3], d.B, d.m, d.m, d.lda);
+    if (!ok) { free_plan(h); return DMUON_ERR_CUDA; }
+  }
+  e = cudaMemcpy(h->d_mats, L.mats.data(), sizeof(MatDesc) * n, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->d_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->d_prefix, L.tile_prefix.data(), 8 * (n + 1), cudaMemcpyHostToDevice);
+  for (int q = 0; q < 3 && e == cudaSuccess; ++q)
+    if (!L.items[q].empty()) e = cudaMemcpy(h->d_items[q], L.items[q].data(), 16 * L.items[q].size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(h->d_flags, 0, 4 * n);
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, 256);
+  if (e != cudaSuccess) { free_plan(h); return cuda_err(e); }
+  h->shapes.assign(shapes, shapes + n);
+  h->last_ptrs.clear();
+  return DMUON_OK;
+}
+
+// Per-matrix update scale (the pages give none; reading: original Muon
+// sqrt(max(1, rows/cols)) by default).
+float scale_of(const MatDesc& d, int mode) {
+  const double r = (double)d.rows, c = (double)d.cols;
+  if (mode == 1) return 1.f;
+  if (mode == 2) return (float)(0.2 * std::sqrt(std::max(r, c)));
+  return (float)std::sqrt(std::max(1.0, r / c));
+}
+
+cudaEvent_t pool_event(dmuon_ctx* h) {
+  if (!h->ev_pool.empty()) { cudaEvent_t e = h->ev_pool.back(); h->ev_pool.pop_back(); return e; }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct LaunchGuard {  // brackets one launch with profiling events
+  dmuon_ctx* h; cudaStream_t s; ProfRec r; bool on;
+  LaunchGuard(dmuon_ctx* h_, cudaStream_t s_, int kind) : h(h_), s(s_), on(h_->profiling) {
+    if (on) { r.a = pool_event(h); r.b = pool_event(h); r.kind = kind; cudaEventRecord(r.a, s); }
+  }
+  ~LaunchGuard() {
+    ++h->launches;
+    if (on) { cudaEventRecord(r.b, s); h->prof.push_back(r); }
+  }
+};
+
+int check_ptr(const void* p) {
+  if (!p) return DMUON_ERR_ARG;
+  if (((uintptr_t)p & 15u) != 0) return DMUON_ERR_ALIGN;
+  return DMUON_OK;
+}
+
+int check_shapes(const dmuon_shape_t* shapes, int n) {
+  for (int i = 0; i < n; ++i) {
+    const int64_t r = shapes[i].rows, c = shapes[i].cols;
+    if (r <= 0 || c <= 0 || r > DMUON_MAX_DIM || c > DMUON_MAX_DIM) return DMUON_ERR_ARG;
+    if (std::min(r, c) > DMUON_MAX_SHORT_SIDE) return DMUON_ERR_ARG;
+  }
+  return DMUON_OK;
+}
+
+// Shared by dmuon_step (ns_only = 0) and dmuon_newton_schulz (ns_only = 1).
+int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, float lr, float mu,
+        int ns_steps, const float* coeffs, float eps, float wd, int nesterov, int scale_mode,
+        int ns_only, cudaStream_t stream) {
+  if (cudaSetDevice(h->device) != cudaSuccess) return DMUON_ERR_CUDA;
+  int rc = build_plan(h, shapes, n);
+  if (rc) return rc;
+  Layout& L = h->L;
+
+  // Per-matrix update scale depends on the mode: refresh descriptors when
+  // it changes (rare; synchronous copy of a small array).
+  bool scale_dirty = false;
+  for (int i = 0; i < n; ++i) {
+    const float s = scale_of(L.mats[i], scale_mode);
+    if (L.mats[i].scale != s) { L.mats[i].scale = s; scale_dirty = true; }
+  }
+  cudaError_t e = cudaSuccess;
+  if (scale_dirty) {
+    e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaMemcpy(h->d_mats, L.mats.data(), sizeof(MatDesc) * n, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_err(e);
+  }
+
+  // Upload caller pointers only when they differ from the previous call.
+  bool same = (int)h->last_ptrs.size() == n;
+  for (int i = 0; same && i < n; ++i)
+    same = h->last_ptrs[i].W == ptrs[i].W && h->last_ptrs[i].G == ptrs[i].G && h->last_ptrs[i].M == ptrs[i].M;
+  if (!same) {
+    if (h->stage_pending) { cudaEventSynchronize(h->stage_ev); h->stage_pending = false; }
+    if (h->h_stage_cap < (size_t)n) {
+      if (h->h_stage) cudaFreeHost(h->h_stage);
+      h->h_stage = nullptr;
+      if (cudaMallocHost(&h->h_stage, sizeof(MatPtrs) * n) != cudaSuccess) { h->h_stage_cap = 0; return DMUON_ERR_OOM; }
+      h->h_stage_cap = n;
+    }
+    std::memcpy(h->h_stage, ptrs, sizeof(MatPtrs) * n);
+    e = cudaMemcpyAsync(h->d_ptrs, h->h_stage, sizeof(MatPtrs) * n, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaEventRecord(h->stage_ev, stream);
+    if (e != cudaSuccess) return cuda_err(e);
+    h->stage_pending = true;
+    h->last_ptrs.assign(ptrs, ptrs + n);
+  }
+  h->last_stream = stream;
+
+  const int64_t nt = L.tile_prefix[n];
+  {
+    MomArgs a{h->d_mats, h->d_ptrs, h->d_prefix, n, nt, mu, nesterov, ns_only, h->d_partials};
+    const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
+    LaunchGuard g(h, stream, DMUON_KIND_MOMENTUM);
+    if ((e = launch_mom(a, grid, stream)) != cudaSuccess) return cuda_err(e);
+  }
+  {
+    FinalizeArgs a{h->d_mats, h->d_prefix, h->d_partials, n, eps, h->d_svec, h->d_flags};
+    LaunchGuard g(h, stream, DMUON_KIND_FINALIZE);
+    if ((e = launch_finalize(a, stream)) != cudaSuccess) return cuda_err(e);
+  }
+  const float decay = 1.f - lr * wd;
+  if (ns_steps == 0) {
+    Update0Args a{h->d_mats, h->d_ptrs, h->d_prefix, n, nt, h->d_svec, lr, decay, ns_only};
+    const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
+    LaunchGuard g(h, stream, DMUON_KIND_UPDATE0);
+    if ((e = launch_update0(a, grid, stream)) != cudaSuccess) return cuda_err(e);
+    return DMUON_OK;
+  }
+  static const int kKinds[3] = {DMUON_KIND_GRAM, DMUON_KIND_GRAM2, DMUON_KIND_APPLY};
+  for (int k = 0; k < ns_steps; ++k) {
+    const float* row = coeffs ? coeffs + 3 * k : kYouCoefficients[std::min(k, 4)];
+    for (int p = 0; p < 3; ++p) {
+      GemmArgs a{};
+      a.mats = h->d_mats;
+      a.ptrs = h->d_ptrs;
+      a.tmaps = h->d_maps;
+      a.items = h->d_items[p];
+      a.n_items = (int)L.items[p].size();
+      a.src = k & 1;
+      a.ca = row[0]; a.cb = row[1]; a.cc = row[2];
+      a.first = k == 0;
+      a.final_mode = (k == ns_steps - 1) ? (ns_only ? kWriteO : kUpdateW) : kWriteX;
+      a.lr = lr;
+      a.decay = decay;
+      a.svec = h->d_svec;
+      a.err = h->d_err;
+      const int grid = std::min(a.n_items, h->num_sms);
+      if (grid <= 0) continue;
+      LaunchGuard g(h, stream, kKinds[p]);
+      if ((e = launch_gemm(p, a, grid, stream)) != cudaSuccess) return cuda_err(e);
+    }
+  }
+  return DMUON_OK;
+}
+
+bool finite3(const float* c, int rows) {
+  for (int i = 0; i < 3 * rows; ++i)
+    if (!std::isfinite(c[i])) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+void dmuon_default_opts(dmuon_opts_t* o) {
+  if (!o) return;
+  o->weight_decay = 0.f;
+  o->eps = 1e-7f;
+  o->nesterov = 1;
+  o->scale_mode = 0;
+  o->coeffs = nullptr;
+}
+
+int dmuon_create(dmuon_handle_t* out, int device) {
+  if (!out) return DMUON_ERR_ARG;
+  *out = nullptr;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess) { cudaGetLastError(); return DMUON_ERR_CUDA; }
+  if (device < 0 || device >= count) return DMUON_ERR_ARG;
+  if (cudaSetDevice(device) != cudaSuccess) return DMUON_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (major != 10 || minor != 3) return DMUON_ERR_UNSUPPORTED;
+  if (gemm_configure() != cudaSuccess) return DMUON_ERR_CUDA;
+  dmuon_ctx* h = new dmuon_ctx();
+  h->device = device;
+  h->num_sms = sms;
+  if (cudaEventCreateWithFlags(&h->stage_ev, cudaEventDisableTiming) != cudaSuccess) { delete h; return DMUON_ERR_CUDA; }
+  *out = h;
+  return DMUON_OK;
+}
+
+void dmuon_destroy(dmuon_handle_t h) {
+  if (!h) return;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  free_plan(h);
+  if (h->h_stage) cudaFreeHost(h->h_stage);
+  if (h->stage_ev) cudaEventDestroy(h->stage_ev);
+  for (auto& r : h->prof) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
+  for (auto e : h->ev_pool) cudaEventDestroy(e);
+  delete h;
+}
+
+int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats, size_t* out_bytes) {
+  if (!out_bytes || n_mats < 0 || (n_mats > 0 && !shapes)) return DMUON_ERR_ARG;
+  *out_bytes = 0;
+  if (n_mats == 0) return DMUON_OK;
+  if (int rc = check_shapes(shapes, n_mats)) return rc;
+  Layout L;
+  make_layout(shapes, n_mats, L);
+  *out_bytes = L.ws_bytes + L.small_bytes;
+  return DMUON_OK;
+}
+
+int dmuon_step(dmuon_handle_t h, float* const* params, const float* const* grads,
+               float* const* momentum, const dmuon_shape_t* shapes, int n_mats, float lr,
+               float mu, int ns_steps, const dmuon_opts_t* opts, void* stream) {
+  if (!h || n_mats < 0) return DMUON_ERR_ARG;
+  if (n_mats == 0) return DMUON_OK;
+  if (!params || !grads || !momentum || !shapes) return DMUON_ERR_ARG;
+  if (ns_steps < 0 || ns_steps > DMUON_MAX_NS_STEPS) return DMUON_ERR_ARG;
+  if (!std::isfinite(lr) || !std::isfinite(mu)) return DMUON_ERR_ARG;
+  dmuon_opts_t o;
+  dmuon_default_opts(&o);
+  if (opts) o = *opts;
+  if (!std::isfinite(o.weight_decay) || !std::isfinite(o.eps) || o.eps < 0.f) return DMUON_ERR_ARG;
+  if (o.scale_mode < 0 || o.scale_mode > 2) return DMUON_ERR_ARG;
+  if (o.coeffs && !finite3(o.coeffs, ns_steps)) return DMUON_ERR_ARG;
+  if (int rc = check_shapes(shapes, n_mats)) return rc;
+  std::vector<MatPtrs> ptrs(n_mats);
+  for (int i = 0; i < n_mats; ++i) {
+    int rc;
+    if ((rc = check_ptr(params[i])) || (rc = check_ptr(grads[i])) || (rc = check_ptr(momentum[i]))) return rc;
+    if ((const void*)params[i] == (const void*)grads[i] || params[i] == momentum[i] ||
+        (const void*)grads[i] == (const void*)momentum[i])
+      return DMUON_ERR_ARG;
+    ptrs[i] = MatPtrs{params[i], grads[i], momentum[i], nullptr};
+  }
+  return run(h, ptrs.data(), shapes, n_mats, lr, mu, ns_steps, o.coeffs, o.eps, o.weight_decay,
+             o.nesterov ? 1 : 0, o.scale_mode, 0, (cudaStream_t)stream);
+}
+
+int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs, float* const* outputs,
+                        const dmuon_shape_t* shapes, int n_mats, int ns_steps, const float* coeffs,
+                        float eps, void* stream) {
+  if (!h || n_mats < 0) return DMUON_ERR_ARG;
+  if (n_mats == 0) return DMUON_OK;
+  if (!inputs || !outputs || !shapes) return DMUON_ERR_ARG;
+  if (ns_steps < 0 || ns_steps > DMUON_MAX_NS_STEPS) return DMUON_ERR_ARG;
+  if (!std::isfinite(eps)) return DMUON_ERR_ARG;
+  if (eps <= 0.f) eps = 1e-7f;
+  if (coeffs && !finite3(coeffs, ns_steps)) return DMUON_ERR_ARG;
+  if (int rc = check_shapes(shapes, n_mats)) return rc;
+  std::vector<MatPtrs> ptrs(n_mats);
+  for (int i = 0; i < n_mats; ++i) {
+    int rc;
+    if ((rc = check_ptr(inputs[i])) || (rc = check_ptr(outputs[i]))) return rc;
+    if ((const void*)inputs[i] == (const void*)outputs[i]) return DMUON_ERR_ARG;
+    ptrs[i] = MatPtrs{outputs[i], inputs[i], nullptr, nullptr};
+  }
+  return run(h, ptrs.data(), shapes, n_mats, 0.f, 0.f, ns_steps, coeffs, eps, 0.f, 0, 1, 1,
+             (cudaStream_t)stream);
+}
+
+int dmuon_get_status(dmuon_handle_t h, int* flags, int n_flags) {
+  if (!h || n_flags < 0) return DMUON_ERR_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return DMUON_ERR_CUDA;
+  cudaError_t e = h->last_stream ? cudaStreamSynchronize(h->last_stream) : cudaDeviceSynchronize();
+  if (e != cudaSuccess) return DMUON_ERR_CUDA;
+  if (!h->small) return DMUON_OK;
+  const int n = (int)h->shapes.size();
+  std::vector<int> f(n, 0);
+  int err = 0;
+  e = cudaMemcpy(f.data(), h->d_flags, 4 * n, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&err, h->d_err, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->d_flags, 0, 4 * n);
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, 4);
+  if (e != cudaSuccess) return DMUON_ERR_CUDA;
+  if (flags)
+    for (int i = 0; i < std::min(n, n_flags); ++i) flags[i] = f[i];
+  if (err) return DMUON_ERR_TIMEOUT;
+  for (int i = 0; i < n; ++i)
+    if (f[i]) return DMUON_ERR_NONFINITE;
+  return DMUON_OK;
+}
+
+int64_t dmuon_launch_count(dmuon_handle_t h) { return h ? h->launches : -1; }
+
+int dmuon_profile_enable(dmuon_handle_t h, int on) {
+  if (!h) return DMUON_ERR_ARG;
+  h->profiling = on != 0;
+  return DMUON_OK;
+}
+
+int dmuon_profile_read(dmuon_handle_t h, double* ms, int64_t* count, int n_kinds) {
+  if (!h || n_kinds < 0 || (n_kinds > 0 && (!ms || !count))) return DMUON_ERR_ARG;
+  int rc = DMUON_OK;
+  for (auto& r : h->prof) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      rc = DMUON_ERR_CUDA;
+    if (r.kind < n_kinds) { ms[r.kind] += t; count[r.kind] += 1; }
+    h->ev_pool.push_back(r.a);
+    h->ev_pool.push_back(r.b);
+  }
+  h->prof.clear();
+  return rc;
+}
+
+int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len) {
+  if (!h) return DMUON_ERR_ARG;
+  std::string s;
+  char line[256];
+  const int n = (int)h->shapes.size();
+  std::snprintf(line, sizeof line, "device %d, %d SMs; matrices %d; ", h->device, h->num_sms, n);
+  s += line;
+  if (h->small) {
+    std::snprintf(line, sizeof line,
+                  "momentum tiles %lld; items gram %zu gram2 %zu apply %zu; workspace %.3f GB + %.3f MB",
+                  (long long)h->L.tile_prefix[n], h->L.items[0].size(), h->L.items[1].size(),
+                  h->L.items[2].size(), h->L.ws_bytes / 1e9, h->L.small_bytes / 1e6);
+    s += line;
+  } else {
+    s += "no plan";
+  }
+  if (buf && len) {
+    std::strncpy(buf, s.c_str(), len - 1);
+    buf[len - 1] = 0;
+  }
+  return (int)s.size();
+}
+
+const char* dmuon_error_string(int code) {
+  switch (code) {
+    case DMUON_OK: return "ok";
+    case DMUON_ERR_ARG: return "invalid argument";
+    case DMUON_ERR_ALIGN: return "matrix pointer not 16-byte aligned";
+    case DMUON_ERR_OOM: return "out of device memory";
+    case DMUON_ERR_CUDA: return "CUDA error";
+    case DMUON_ERR_NONFINITE: return "non-finite input";
+    case DMUON_ERR_TIMEOUT: return "kernel wait timed out";
+    case DMUON_ERR_UNSUPPORTED: return "device is not compute capability 10.3 (sm_103a)";
+    default: return "unknown status";
+  }
+}
+
+const char* dmuon_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,419 @@
+// Tensor-core phases of quintic Newton-Schulz on sm_103a (tcgen05 + TMEM +
+// TMA), one persistent launch per phase over every matrix of the list.
+//
+// DMuon "API Reference", section "direct_newton_schulz": per step k,
+//   X <- a_k X + b_k (X X^T) X + c_k (X X^T)^2 X
+// computed as three products:
+//   Gram   A = X X^T             symmetric, m x m, K = n
+//   Gram2  B = b A + c A A       symmetric, m x m, K = m (A A = A A^T)
+//   Apply  X' = a X + B X        m x n, K = m  (last step: weight update)
+// The symmetric products compute only the 256x256 super-tiles on or above
+// the diagonal and write the transposed copy of each off-diagonal tile, the
+// tile saving the pages' SYRK kernels describe (section "newton_schulz").
+//
+// CTA layout (192 threads, one CTA per SM, persistent over a static
+// round-robin of work items):
+//   warp 0   TMA producer: 64-wide K blocks of both operands into a
+//            4-stage shared-memory ring (128-byte swizzle, 64x64 boxes)
+//   warp 1   TMEM allocator and single-thread tcgen05.mma issuer
+//            (M=128, N=256, K=16 per instruction, fp32 accumulate)
+//   warps 2-5 epilogue: TMEM -> registers, fused scaling / a*X / b*A terms,
+//            bf16 stores (direct and mirrored) or the fp32 weight update
+// Two 256-column accumulators in TMEM let the epilogue of one tile overlap
+// the main loop of the next.
+//
+// Every mbarrier wait is bounded (kTimeoutNs); on timeout the CTA records
+// bit 0 of *err, stops issuing, drains its own copies and MMAs with bounded
+// waits, frees TMEM and returns.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dmuon {
+
+namespace {
+
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s without progress
+
+struct Smem {
+  uint8_t* stages;     // kStages x (A 16 KB | B 32 KB), 1024-aligned
+  uint32_t* scratch;   // 4 warps x 32 x 17 words
+  uint64_t* bars;      // full[kStages], empty[kStages], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw) {
+  Smem s;
+  const uint32_t a = ptx::smem_addr(raw);
+  uint8_t* base = raw + ((1024u - (a & 1023u)) & 1023u);
+  s.stages = base;
+  s.scratch = reinterpret_cast<uint32_t*>(base + kStages * kStageBytes);
+  s.bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes + 4 * kEpiWords * 4);
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + 2 * kStages + 5);
+  s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+  return s;
+}
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       int* err, bool honour_abort) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try(bar, parity)) return true;
+    if (honour_abort && *abort_flag) return false;
+    if (ptx::globaltimer() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      atomicOr(err, 1);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* err) {
+  if (ptx::mbar_try(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, err, true);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 32 consecutive bf16 of one row -> fp32, zero outside [0, ncols) or when
+// the row is invalid.
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* rowp, int64_t c, int64_t ncols,
+                                           bool row_ok, float (&f)[32]) {
+  if (row_ok && c + 32 <= ncols) {
+    const uint4* p = reinterpret_cast<const uint4*>(rowp + c);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = p[q];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        f[q * 8 + 2 * k] = bf_lo(w[k]);
+        f[q * 8 + 2 * k + 1] = bf_hi(w[k]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      f[j] = (row_ok && c + j < ncols) ? __bfloat162float(rowp[c + j]) : 0.f;
+  }
+}
+
+// Store 32 packed bf16 (16 words) at rowp[c..c+31], clipped to ncols.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* rowp, int64_t c, int64_t ncols,
+                                            bool row_ok, const uint32_t (&w)[16]) {
+  if (!row_ok) return;
+  if (c + 32 <= ncols) {
+    uint4* p = reinterpret_cast<uint4*>(rowp + c);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) p[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  } else {
+    uint16_t* h = reinterpret_cast<uint16_t*>(rowp);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (c + j < ncols) h[c + j] = (uint16_t)((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+  }
+}
+
+// Mirror store of a 32x32 bf16 block held one row per lane: lane L writes
+// column L of the block as row (c + L) of the destination, columns
+// [rbase, rbase+32) clipped to n_lim.  Uses the warp's 32x17-word scratch.
+__device__ __forceinline__ void mirror_store32(__nv_bfloat16* base, int64_t ld, int64_t c,
+                                               int64_t rbase, int64_t n_lim, int lane,
+                                               const uint32_t (&w)[16], uint32_t* scratch) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) scratch[lane * 17 + k] = w[k];
+  __syncwarp();
+  uint32_t t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t w0 = scratch[(2 * i) * 17 + (lane >> 1)];
+    const uint32_t w1 = scratch[(2 * i + 1) * 17 + (lane >> 1)];
+    const uint32_t h0 = (lane & 1) ? (w0 >> 16) : (w0 & 0xFFFFu);
+    const uint32_t h1 = (lane & 1) ? (w1 >> 16) : (w1 & 0xFFFFu);
+    t[i] = h0 | (h1 << 16);
+  }
+  __syncwarp();
+  const int64_t dr = c + lane;
+  store_row32(base + dr * ld, rbase, n_lim, dr < n_lim, t);
+}
+
+template <int PHASE>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item, uint32_t tacc,
+                                              int quad, int lane, uint32_t* scratch) {
+  const MatDesc& d = a.mats[item.x];
+  const int64_t m = d.m, n = d.n;
+  const int64_t row0 = (int64_t)item.y * kBM;
+  const int64_t col0 = (int64_t)item.z * kBN;
+  const int64_t rbase = row0 + quad * 32;
+  const int64_t r = rbase + lane;
+  const bool row_ok = r < m;
+  const uint32_t tq = tacc + ((uint32_t)(quad * 32) << 16);
+
+  if constexpr (PHASE == kPhaseGram || PHASE == kPhaseGram2) {
+    const bool mirror = (item.y >> 1) < item.z;
+    float alpha = 1.f;
+    if (PHASE == kPhaseGram && a.first) {
+      const float s = a.svec[item.x];
+      alpha = s * s;
+    }
+    __nv_bfloat16* dst = (PHASE == kPhaseGram) ? d.A : d.B;
+    const int64_t ld = d.lda;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      const int64_t c = col0 + ch * 32;
+      if (c >= m) break;  // warp-uniform
+      uint32_t v[32];
+      ptx::tmem_ld32(tq + ch * 32, v);
+      float f[32];
+      if constexpr (PHASE == kPhaseGram) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]) * alpha;
+      } else {
+        float av[32];
+        load_row32(d.A + r * ld, c, m, row_ok, av);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = fmaf(a.cc, __uint_as_float(v[j]), a.cb * av[j]);
+      }
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) w[k] = pack2(f[2 * k], f[2 * k + 1]);
+      store_row32(dst + r * ld, c, m, row_ok, w);
+      if (mirror) mirror_store32(dst, ld, c, rbase, m, lane, w, scratch);
+    }
+  } else {
+    const float alpha = a.first ? a.svec[item.x] : 1.f;
+    const __nv_bfloat16* xs = d.X[a.src];
+    __nv_bfloat16* xd = d.X[a.src ^ 1];
+    const int64_t ldx = d.ldx;
+    const MatPtrs& p = a.ptrs[item.x];
+    const float coef = a.lr * d.scale;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      const int64_t c = col0 + ch * 32;
+      if (c >= n) break;  // warp-uniform
+      uint32_t v[32];
+      ptx::tmem_ld32(tq + ch * 32, v);
+      float xv[32];
+      load_row32(xs + r * ldx, c, n, row_ok, xv);
+      float o[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = alpha * fmaf(a.ca, xv[j], __uint_as_float(v[j]));
+      if (a.final_mode == kWriteX) {
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) w[k] = pack2(o[2 * k], o[2 * k + 1]);
+        store_row32(xd + r * ldx, c, n, row_ok, w);
+      } else if (row_ok) {
+        const bool upd = a.final_mode == kUpdateW;
+        if (!d.transposed) {
+          // W is m x n: row r, columns c..c+31.
+          float* wp = p.W + r * d.cols + c;
+          if (c + 32 <= n && (d.cols & 3) == 0) {
+            float4* w4 = reinterpret_cast<float4*>(wp);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float4 o4 = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+              if (upd) {
+                const float4 cur = w4[q];
+                o4.x = fmaf(a.decay, cur.x, -coef * o4.x);
+                o4.y = fmaf(a.decay, cur.y, -coef * o4.y);
+                o4.z = fmaf(a.decay, cur.z, -coef * o4.z);
+                o4.w = fmaf(a.decay, cur.w, -coef * o4.w);
+              }
+              w4[q] = o4;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c + j < n) wp[j] = upd ? fmaf(a.decay, wp[j], -coef * o[j]) : o[j];
+          }
+        } else {
+          // W is n x m: element (c + j, r); lanes hold consecutive r, so
+          // each j is one coalesced 128-byte warp access.
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (c + j < n) {
+              float* wp = p.W + (c + j) * d.cols + r;
+              *wp = upd ? fmaf(a.decay, *wp, -coef * o[j]) : o[j];
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int PHASE>
+__global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem sm = carve(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint64_t* full = sm.bars;
+  uint64_t* empty = sm.bars + kStages;
+  uint64_t* tfull = sm.bars + 2 * kStages;
+  uint64_t* tempty = sm.bars + 2 * kStages + 2;
+  uint64_t* drain = sm.bars + 2 * kStages + 4;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(ptx::smem_addr(full + s), 1);
+      ptx::mbar_init(ptx::smem_addr(empty + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_addr(tfull + i), 1);
+      ptx::mbar_init(ptx::smem_addr(tempty + i), 4);
+    }
+    ptx::mbar_init(ptx::smem_addr(drain), 1);
+    *sm.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(sm.tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      uint32_t it = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
+        const int4 item = a.items[w];
+        const CUtensorMap* maps = a.tmaps + (size_t)item.x * kMapsPerMat;
+        const CUtensorMap* mapA;
+        const CUtensorMap* mapB;
+        if (PHASE == kPhaseGram) {
+          mapA = maps + a.src; mapB = maps + a.src;
+        } else if (PHASE == kPhaseGram2) {
+          mapA = maps + 2; mapB = maps + 2;
+        } else {
+          mapA = maps + 3; mapB = maps + a.src;
+        }
+        const int row0 = item.y * kBM;
+        const int col0 = item.z * kBN;
+        for (int kb = 0; kb < item.w; ++kb, ++it) {
+          const uint32_t s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!wait_bar(ptx::smem_addr(empty + s), ph ^ 1u, sm.abort_flag, a.err)) { ok = false; break; }
+          const uint32_t fb = ptx::smem_addr(full + s);
+          ptx::mbar_expect_tx(fb, kStageBytes);
+          const uint32_t sa = ptx::smem_addr(sm.stages + s * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          const int k0 = kb * kBK;
+          ptx::tma_load_2d(sa, mapA, k0, row0, fb);
+          ptx::tma_load_2d(sa + kBoxBytes, mapA, k0, row0 + kBox, fb);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (PHASE == kPhaseApply)
+              ptx::tma_load_2d(sb + q * kBoxBytes, mapB, col0 + q * kBox, k0, fb);
+            else
+              ptx::tma_load_2d(sb + q * kBoxBytes, mapB, k0, col0 + q * kBox, fb);
+          }
+        }
+      }
+      if (!ok || *sm.abort_flag) {
+        // Drain: wait (bounded, ignoring the abort flag) for the copies of
+        // the last issued stages so none lands after the CTA exits.
+        const uint32_t n_out = it < (uint32_t)kStages ? it : (uint32_t)kStages;
+        for (uint32_t i = it - n_out; i < it; ++i)
+          wait_slow(ptx::smem_addr(full + (i % kStages)), (i / kStages) & 1u, sm.abort_flag,
+                    a.err, false);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = ptx::idesc_bf16(kBM, kBN, PHASE == kPhaseApply ? 1 : 0);
+      uint32_t it = 0, tc = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x, ++tc) {
+        const int4 item = a.items[w];
+        const uint32_t acc = tc & 1u;
+        if (!wait_bar(ptx::smem_addr(tempty + acc), ((tc >> 1) & 1u) ^ 1u, sm.abort_flag, a.err)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t dt = tmem_base + acc * kBN;
+        for (int kb = 0; kb < item.w; ++kb, ++it) {
+          const uint32_t s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!wait_bar(ptx::smem_addr(full + s), ph, sm.abort_flag, a.err)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_addr(sm.stages + s * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = ptx::desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = (PHASE == kPhaseApply) ? ptx::desc_sw128(sb + kk * 2048, 8192, 1024)
+                                                       : ptx::desc_sw128(sb + kk * 32, 16, 1024);
+            ptx::mma_bf16(dt, ad, bd, idesc, (kb | kk) != 0);
+          }
+          issued = true;
+          ptx::mma_commit(ptx::smem_addr(empty + s));
+        }
+        if (!ok) break;
+        ptx::mma_commit(ptx::smem_addr(tfull + acc));
+      }
+      if (issued && (!ok || *sm.abort_flag)) {
+        ptx::mma_commit(ptx::smem_addr(drain));
+        wait_slow(ptx::smem_addr(drain), 0, sm.abort_flag, a.err, false);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 for this warp
+    uint32_t* scratch = sm.scratch + (warp - 2) * kEpiWords;
+    uint32_t tc = 0;
+    for (int w = blockIdx.x; w < a.n_items; w += gridDim.x, ++tc) {
+      const int4 item = a.items[w];
+      const uint32_t acc = tc & 1u;
+      if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err)) break;
+      ptx::tc_fence_after();
+      epilogue_tile<PHASE>(a, item, tmem_base + acc * kBN, quad, lane, scratch);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(tempty + acc));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t gemm_configure() {
+  cudaError_t e;
+  e = cudaFuncSetAttribute(ns_gemm_kernel<kPhaseGram>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ns_gemm_kernel<kPhaseGram2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(ns_gemm_kernel<kPhaseApply>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+}
+
+cudaError_t launch_gemm(int phase, const GemmArgs& a, int grid, cudaStream_t s) {
+  switch (phase) {
+    case kPhaseGram: ns_gemm_kernel<kPhaseGram><<<grid, kGemmThreads, kGemmSmem, s>>>(a); break;
+    case kPhaseGram2: ns_gemm_kernel<kPhaseGram2><<<grid, kGemmThreads, kGemmSmem, s>>>(a); break;
+    default: ns_gemm_kernel<kPhaseApply><<<grid, kGemmThreads, kGemmSmem, s>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dmuon

@@ -1,0 +1,35 @@
+"""FLOP accounting of one Muon step (measurement only).
+
+Per matrix with short side m and long side n, one Newton-Schulz iteration
+forms A = X X^T (m x m, K = n), A*A (m x m, K = m) and B*X (m x n, K = m).
+The symmetric products are counted as one triangle (m^2 n and m^3 flops),
+B*X densely (2 m^2 n), so the algorithmic count is ns*(3 m^2 n + m^3); the
+dense-equivalent count is ns*(4 m^2 n + 2 m^3).
+"""
+
+
+def algorithmic_flops(shapes, ns_steps=5):
+    tot = 0
+    for r, c in shapes:
+        m, n = min(r, c), max(r, c)
+        tot += ns_steps * (3 * m * m * n + m ** 3)
+    return tot
+
+
+def dense_flops(shapes, ns_steps=5):
+    tot = 0
+    for r, c in shapes:
+        m, n = min(r, c), max(r, c)
+        tot += ns_steps * (4 * m * m * n + 2 * m ** 3)
+    return tot
+
+
+def apply_flops(shapes, ns_steps=5):
+    """Flops of the B*X products alone (2 m^2 n per iteration)."""
+    return sum(ns_steps * 2 * min(r, c) ** 2 * max(r, c) for r, c in shapes)
+
+
+def elementwise_bytes(shapes):
+    """Algorithmic HBM bytes of the momentum/normalise pass: read G and M,
+    write M (fp32) and the bf16 iterate: 14 bytes per element."""
+    return sum(14 * r * c for r, c in shapes)

@@ -1,0 +1,149 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must build for sm_103a, load, and export every function that
+include/dmuon.h declares; the host-only entry points (defaults, workspace
+sizing, error strings) and the argument checks that run before any device
+work are exercised here.  Compute calls are left to the gpu-marked tests.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import newton_schulz_nesterov_gb300 as dm
+from newton_schulz_nesterov_gb300 import _build, flops, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return dm.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "dmuon.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dmuon_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("dmuon_create", "dmuon_destroy", "dmuon_step", "dmuon_newton_schulz",
+                 "dmuon_get_status", "dmuon_workspace_bytes", "dmuon_error_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_error_strings(lib):
+    assert "sm_103a" in dm.dmuon_version()
+    for code in dm.STATUS:
+        s = dm.dmuon_error_string(code)
+        assert s and s != "unknown status"
+    assert dm.dmuon_error_string(12345) == "unknown status"
+
+
+def test_default_opts_are_the_pages_defaults(lib, golden_dir):
+    gold = {}
+    for line in open(os.path.join(golden_dir, "muon_defaults.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, v = line.split()
+            gold[k] = float(v)
+    o = dm.Opts()
+    o.eps = -1.0
+    o.nesterov = 7
+    lib.dmuon_default_opts(ctypes.byref(o))
+    assert o.weight_decay == gold["weight_decay"]
+    assert o.eps == pytest.approx(gold["eps"], rel=1e-7)
+    assert o.nesterov == int(gold["nesterov"])
+    assert o.scale_mode == 0
+    assert not o.coeffs
+    lib.dmuon_default_opts(None)  # no-op, no crash
+
+
+def test_workspace_bytes_covers_the_buffers(lib):
+    for name in ("tinymlp_d128", "tinymlp_d512", "llama3_8b", "tp_70b_mixed"):
+        shapes = workloads.get(name).shapes
+        got = dm.dmuon_workspace_bytes(list(shapes))
+        need = sum(2 * (2 * min(r, c) * max(r, c) + 2 * min(r, c) ** 2) for r, c in shapes)
+        assert need <= got <= need * 1.05 + 64 * 1024 * 1024
+    assert dm.dmuon_workspace_bytes([]) == 0
+
+
+def test_workspace_bytes_rejects_bad_shapes(lib):
+    for bad in ([(0, 4)], [(4, -1)], [(1 << 21, 8)], [(40000, 40000)]):
+        with pytest.raises(dm.DmuonError) as e:
+            dm.dmuon_workspace_bytes(bad)
+        assert e.value.code == -1
+    out = ctypes.c_size_t()
+    assert lib.dmuon_workspace_bytes(None, -1, ctypes.byref(out)) == -1
+    assert lib.dmuon_workspace_bytes(None, 3, ctypes.byref(out)) == -1
+    assert lib.dmuon_workspace_bytes(None, 0, None) == -1
+
+
+def test_null_handle_is_rejected(lib):
+    assert lib.dmuon_step(None, None, None, None, None, 0, 0.02, 0.95, 5, None, None) == -1
+    assert lib.dmuon_newton_schulz(None, None, None, None, 1, 5, None, 1e-7, None) == -1
+    assert lib.dmuon_get_status(None, None, 0) == -1
+    assert lib.dmuon_launch_count(None) == -1
+    assert lib.dmuon_profile_enable(None, 1) == -1
+    assert lib.dmuon_plan_summary(None, None, 0) == -1
+    lib.dmuon_destroy(None)
+
+
+def test_create_without_a_gpu_fails_cleanly(lib):
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    h = ctypes.c_void_p(1)
+    rc = lib.dmuon_create(ctypes.byref(h), 0)
+    assert rc in (-1, -4, -7)
+    assert not h.value
+    assert lib.dmuon_create(None, 0) == -1
+
+
+def test_workload_shapes_and_flop_totals():
+    """Shape lists and the algorithmic / dense FLOP totals of each workload
+    (totals computed by hand from the shape lists)."""
+    w1 = workloads.get("tinymlp_d128").shapes
+    assert len(w1) == 12 and w1.count((512, 128)) == 8 and w1.count((128, 512)) == 4
+    w3 = workloads.get("llama3_8b").shapes
+    assert len(w3) == 224 and sum(r * c for r, c in w3) == 6979321856
+    w5 = workloads.get("tp_70b_mixed").shapes
+    assert len(w5) == 513 and w5[0] == (28672, 8192)
+    # 5*(3 m^2 n + m^3), one TinyMLP-128 matrix: m=128, n=512
+    assert flops.algorithmic_flops([(512, 128)]) == 5 * (3 * 128 * 128 * 512 + 128 ** 3)
+    assert flops.algorithmic_flops(w1) == 1_635_778_560
+    assert round(flops.algorithmic_flops(w3) / 1e12, 1) == 471.8
+    assert round(flops.dense_flops(w3) / 1e12, 1) == 665.9
+    assert round(flops.algorithmic_flops(workloads.get("spiked_4096").shapes) / 1e12, 1) == 88.0
+    assert round(flops.algorithmic_flops(w5) / 1e12, 1) == 31.6
+
+
+def test_inputs_are_seeded_and_shaped():
+    torch = pytest.importorskip("torch")
+    w = workloads.get("tinymlp_d128")
+    a = workloads.grad(w, 2, 0)
+    b = workloads.grad(w, 2, 0)
+    c = workloads.grad(w, 2, 1)
+    assert a.shape == (128, 512) and a.dtype == torch.float32
+    assert torch.equal(a, b) and not torch.equal(a, c)
+    W = workloads.weight(w, 0)
+    assert float(W.abs().max()) <= 1.0 / 128 ** 0.5
+    s = workloads.get("spiked_4096")
+    # rank-16 spike on a small stand-in shape: top singular value near 1e2
+    small = workloads.Workload("s", ((256, 256),), 0.0, "zero", 0, spike_rank=16)
+    g = workloads.grad(small, 0)
+    sv = torch.linalg.svdvals(g.double())
+    assert abs(float(sv[0]) - 100.0) < 1e-3 and abs(float(sv[15]) - 1e-3) < 1e-5
+    assert s.spike_rank == 16

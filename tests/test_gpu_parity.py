@@ -1,0 +1,279 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Same seeded inputs on both sides.  Bars (per matrix):
+  momentum buffer   relative Frobenius error <= 1e-6   (fp32 arithmetic)
+  NS output O and the weight update W' - W
+                    relative Frobenius error <= 3e-2   (bf16 tensor cores)
+The small cases span several 128x256 tiles and ragged tails; the full-size
+cases run every matrix of a workload in the bench's launch configuration
+and compare sampled matrices with the oracle.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import newton_schulz_nesterov_gb300 as dm  # noqa: E402
+from newton_schulz_nesterov_gb300 import _build, workloads  # noqa: E402
+import oracle  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+MOM_TOL = 1e-6
+NS_TOL = 3e-2
+F32 = lambda x: float(np.float32(x))  # noqa: E731  (the ABI takes fp32 scalars)
+
+
+def rel_fro(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    nr = np.linalg.norm(ref)
+    d = np.linalg.norm(got - ref)
+    return d / nr if nr > 0 else d
+
+
+@pytest.fixture(scope="module")
+def handle():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _build.build()
+    h = dm.Handle(0)
+    yield h
+    h.close()
+
+
+def _to_dev(ts):
+    return [t.clone().cuda() for t in ts]
+
+
+def _step_and_check(handle, Ws, Gs, Ms, lr=0.02, mu=0.95, ns_steps=5, wd=0.0, nesterov=True,
+                    scale_mode=0, coeffs=None, ns_tol=NS_TOL):
+    Wd, Gd, Md = _to_dev(Ws), _to_dev(Gs), _to_dev(Ms)
+    handle.step(Wd, Gd, Md, lr=lr, mu=mu, ns_steps=ns_steps, weight_decay=wd,
+                nesterov=nesterov, scale_mode=scale_mode, coeffs=coeffs)
+    rc, flags = handle.status(len(Ws))
+    assert rc == 0 and not any(flags)
+    worst = 0.0
+    for i in range(len(Ws)):
+        ref = oracle.muon_step(Ws[i].numpy(), Gs[i].numpy(), Ms[i].numpy(), lr=F32(lr), mu=F32(mu),
+                               wd=F32(wd), ns_steps=ns_steps, coeffs=coeffs, nesterov=nesterov,
+                               scale_mode=scale_mode)
+        W0 = Ws[i].numpy().astype(np.float64)
+        assert rel_fro(Md[i].cpu().numpy(), ref["M"]) <= MOM_TOL, ("momentum", i)
+        e_upd = rel_fro(Wd[i].cpu().numpy().astype(np.float64) - W0, ref["W"] - W0)
+        e_w = rel_fro(Wd[i].cpu().numpy(), ref["W"])
+        assert e_upd <= ns_tol, ("update", i, Ws[i].shape, e_upd)
+        assert e_w <= ns_tol, ("weight", i, e_w)
+        worst = max(worst, e_upd)
+    return worst
+
+
+def test_tinymlp_d128_step(handle):
+    w = workloads.get("tinymlp_d128")
+    n = len(w.shapes)
+    Ws = [workloads.weight(w, i) for i in range(n)]
+    Gs = [workloads.grad(w, i) for i in range(n)]
+    Ms = [workloads.momentum(w, i) for i in range(n)]
+    worst = _step_and_check(handle, Ws, Gs, Ms)
+    assert worst < NS_TOL
+
+
+def test_tinymlp_d512_three_steps(handle):
+    """Zero momentum, three steps with fresh gradients; the oracle runs the
+    same three steps from the same initial state."""
+    w = workloads.get("tinymlp_d512")
+    n = len(w.shapes)
+    W0 = [workloads.weight(w, i) for i in range(n)]
+    M0 = [workloads.momentum(w, i) for i in range(n)]
+    Wd, Md = _to_dev(W0), _to_dev(M0)
+    Wr = [x.numpy().astype(np.float64) for x in W0]
+    Mr = [x.numpy().astype(np.float64) for x in M0]
+    for step in range(w.warm_steps + 1):
+        Gs = [workloads.grad(w, i, step) for i in range(n)]
+        Gd = _to_dev(Gs)
+        handle.step(Wd, Gd, Md, lr=0.02, mu=0.95, ns_steps=5)
+        for i in range(n):
+            out = oracle.muon_step(Wr[i], Gs[i].numpy(), Mr[i], lr=F32(0.02), mu=F32(0.95))
+            Wr[i], Mr[i] = out["W"], out["M"]
+    rc, _ = handle.status()
+    assert rc == 0
+    for i in range(n):
+        W0i = W0[i].numpy().astype(np.float64)
+        assert rel_fro(Md[i].cpu().numpy(), Mr[i]) <= MOM_TOL
+        assert rel_fro(Wd[i].cpu().numpy().astype(np.float64) - W0i, Wr[i] - W0i) <= NS_TOL
+
+
+RAGGED = [(1, 1), (1, 37), (37, 1), (3, 5), (5, 3), (64, 256), (256, 64), (128, 512),
+          (129, 257), (300, 700), (700, 300), (200, 200), (513, 1000), (1000, 513),
+          (255, 2050), (8, 4100), (384, 384), (640, 96)]
+
+
+def test_newton_schulz_ragged_shapes(handle):
+    gen = torch.Generator().manual_seed(7)
+    ins = [torch.randn(s, generator=gen) for s in RAGGED]
+    outs = [torch.empty(s, device="cuda") for s in RAGGED]
+    handle.newton_schulz(_to_dev(ins), outs)
+    rc, _ = handle.status()
+    assert rc == 0
+    for x, o, s in zip(ins, outs, RAGGED):
+        ref = oracle.newton_schulz(x.numpy())
+        e = rel_fro(o.cpu().numpy(), ref)
+        assert e <= NS_TOL, (s, e)
+
+
+def test_newton_schulz_scaled_inputs(handle):
+    """The normalisation is folded into the first iteration: tiny and huge
+    input scales give the same O."""
+    gen = torch.Generator().manual_seed(9)
+    base = torch.randn((300, 520), generator=gen)
+    for scale in (1e-6, 1e-3, 1.0, 1e3):
+        x = (base * scale).cuda()
+        o = torch.empty_like(x)
+        handle.newton_schulz([x], [o])
+        assert rel_fro(o.cpu().numpy(), oracle.newton_schulz(x.cpu().numpy())) <= NS_TOL
+
+
+def test_zero_input_gives_zero_output(handle):
+    x = torch.zeros((260, 300), device="cuda")
+    o = torch.full_like(x, 5.0)
+    handle.newton_schulz([x], [o])
+    assert float(o.abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(ns_steps=0), dict(ns_steps=1), dict(ns_steps=2), dict(ns_steps=7),
+    dict(nesterov=False), dict(wd=0.1), dict(scale_mode=1), dict(scale_mode=2),
+    dict(coeffs=[(3.4445, -4.7750, 2.0315)] * 5),
+    dict(ns_steps=3, coeffs=[(3.0, -3.2, 1.2), (2.5, -2.0, 0.5), (1.875, -1.25, 0.375)]),
+])
+def test_step_options(handle, kw):
+    gen = torch.Generator().manual_seed(11)
+    shapes = [(384, 200), (200, 640), (96, 96), (130, 70)]
+    Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
+    Gs = [torch.randn(s, generator=gen) for s in shapes]
+    Ms = [torch.randn(s, generator=gen) for s in shapes]
+    _step_and_check(handle, Ws, Gs, Ms, lr=0.05, mu=0.9, **kw)
+
+
+def test_deterministic_bitwise(handle):
+    w = workloads.get("tinymlp_d128")
+    n = len(w.shapes)
+    Ws = [workloads.weight(w, i) for i in range(n)]
+    Gs = _to_dev([workloads.grad(w, i) for i in range(n)])
+    Ms = [workloads.momentum(w, i) for i in range(n)]
+    res = []
+    for _ in range(2):
+        Wd, Md = _to_dev(Ws), _to_dev(Ms)
+        handle.step(Wd, Gs, Md)
+        torch.cuda.synchronize()
+        res.append(([x.cpu() for x in Wd], [x.cpu() for x in Md]))
+    for a, b in zip(res[0][0] + res[0][1], res[1][0] + res[1][1]):
+        assert torch.equal(a, b)
+
+
+def test_nonfinite_is_flagged(handle):
+    shapes = [(64, 96), (96, 64), (128, 128)]
+    Ws = [torch.zeros(s, device="cuda") for s in shapes]
+    Gs = [torch.ones(s, device="cuda") for s in shapes]
+    Ms = [torch.zeros(s, device="cuda") for s in shapes]
+    Gs[1][3, 5] = float("nan")
+    handle.step(Ws, Gs, Ms)
+    rc, flags = handle.status(3)
+    assert rc == -5 and flags == [0, 1, 0]
+    rc, flags = handle.status(3)  # flags are cleared by the read
+    assert rc == 0 and flags == [0, 0, 0]
+
+
+def test_argument_errors_with_live_handle(handle):
+    h = handle.h
+    W = torch.zeros((64, 64), device="cuda")
+    G = torch.zeros((64, 64), device="cuda")
+    M = torch.zeros((64, 64), device="cuda")
+    p = lambda t: t.data_ptr()  # noqa: E731
+    call = lambda **k: dm.dmuon_step_ptrs(h, k.get("w", [p(W)]), k.get("g", [p(G)]),  # noqa: E731
+                                          k.get("m", [p(M)]), k.get("s", [(64, 64)]), 0.02, 0.95,
+                                          k.get("ns", 5), scale_mode=k.get("sm", 0),
+                                          coeffs=k.get("c"), check=False)
+    before = dm.dmuon_launch_count(h)
+    assert call(w=[p(W) + 4]) == -2
+    assert call(s=[(0, 64)]) == -1
+    assert call(s=[(64, 40000)]) == -1
+    assert call(ns=65) == -1
+    assert call(ns=-1) == -1
+    assert call(sm=3) == -1
+    assert call(c=[(1.0, float("nan"), 0.0)] * 5) == -1
+    assert call(g=[p(W)]) == -1
+    assert call(w=[0]) == -1
+    assert dm.dmuon_step_ptrs(h, [], [], [], [], 0.02, 0.95, check=False) == 0
+    assert dm.dmuon_launch_count(h) == before  # nothing launched
+
+
+def test_launch_count_and_profile(handle):
+    shapes = [(256, 512), (512, 256)]
+    Ws = [torch.zeros(s, device="cuda") for s in shapes]
+    Gs = [torch.randn(s, device="cuda") for s in shapes]
+    Ms = [torch.zeros(s, device="cuda") for s in shapes]
+    dm.dmuon_profile_enable(handle.h, True)
+    dm.dmuon_profile_read(handle.h)
+    before = dm.dmuon_launch_count(handle.h)
+    handle.step(Ws, Gs, Ms, ns_steps=5)
+    assert dm.dmuon_launch_count(handle.h) - before == 2 + 3 * 5
+    prof = dm.dmuon_profile_read(handle.h)
+    dm.dmuon_profile_enable(handle.h, False)
+    assert prof["momentum"][1] == 1 and prof["gram"][1] == 5 and prof["apply"][1] == 5
+    assert all(v[0] >= 0 for v in prof.values())
+    assert "matrices 2" in dm.dmuon_plan_summary(handle.h)
+
+
+# ---------------------------------------------------------------- full size
+
+def _full_size_sampled(handle, name, sample, steps_before=None):
+    """Run the whole workload (bench launch configuration) on the GPU with
+    seeded device inputs; compare the sampled matrices' last-step update and
+    momentum with the oracle run from the same seeded inputs."""
+    w = workloads.get(name)
+    n = len(w.shapes)
+    warm = w.warm_steps if steps_before is None else steps_before
+    dev = "cuda"
+    Wd = [workloads.weight(w, i, dev) for i in range(n)]
+    Md = [workloads.momentum(w, i, dev) for i in range(n)]
+    for step in range(warm):
+        Gd = [workloads.grad(w, i, step, dev) for i in range(n)]
+        handle.step(Wd, Gd, Md)
+        del Gd
+    Gd = [workloads.grad(w, i, warm, dev) for i in range(n)]
+    W_before = {i: Wd[i].cpu() for i in sample}
+    handle.step(Wd, Gd, Md)
+    rc, _ = handle.status()
+    assert rc == 0
+    for i in sample:
+        # momentum history from the seeded inputs alone
+        M = workloads.momentum(w, i, dev).cpu().numpy().astype(np.float64)
+        for step in range(warm):
+            M = oracle.momentum_update(M, workloads.grad(w, i, step, dev).cpu().numpy(), F32(0.95))
+        G = Gd[i].cpu().numpy()
+        r, c = w.shapes[i]
+        ref = oracle.muon_step(np.zeros((r, c)), G, M, lr=F32(0.02), mu=F32(0.95))
+        upd = Wd[i].cpu().numpy().astype(np.float64) - W_before[i].numpy().astype(np.float64)
+        e_m = rel_fro(Md[i].cpu().numpy(), ref["M"])
+        e_u = rel_fro(upd, ref["W"])
+        assert e_m <= MOM_TOL, (name, i, e_m)
+        assert e_u <= NS_TOL, (name, i, w.shapes[i], e_u)
+    del Wd, Md, Gd
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_full_llama3_8b_sampled(handle):
+    # layer 0: q, k, v, gate (transposed path), down; layer 31: k
+    _full_size_sampled(handle, "llama3_8b", [0, 1, 2, 4, 6, 218])
+
+
+@pytest.mark.slow
+def test_full_spiked_4096_sampled(handle):
+    _full_size_sampled(handle, "spiked_4096", [0, 63])
+
+
+@pytest.mark.slow
+def test_full_tp_70b_mixed_small_sampled(handle):
+    _full_size_sampled(handle, "tp_70b_mixed", [1, 2, 256, 512])
