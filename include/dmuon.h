@@ -147,6 +147,10 @@ int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs,
  */
 int dmuon_get_status(dmuon_handle_t h, int* flags, int n_flags);
 
+/* Text describing the most recent failure on this handle (which call or
+ * CUDA error), "" if none; valid until the next call on the handle. */
+const char* dmuon_last_error(dmuon_handle_t h);
+
 /* Kernel launches issued by this handle since creation (a counter). */
 int64_t dmuon_launch_count(dmuon_handle_t h);
 

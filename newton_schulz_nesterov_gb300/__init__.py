@@ -16,7 +16,7 @@ __all__ = [
     "DmuonError", "load", "lib_path", "dmuon_create", "dmuon_destroy",
     "dmuon_step", "dmuon_step_ptrs", "dmuon_newton_schulz",
     "dmuon_newton_schulz_ptrs", "dmuon_get_status", "dmuon_workspace_bytes",
-    "dmuon_launch_count", "dmuon_profile_enable", "dmuon_profile_read",
+    "dmuon_launch_count", "dmuon_last_error", "dmuon_profile_enable", "dmuon_profile_read",
     "dmuon_plan_summary", "dmuon_error_string", "dmuon_version", "Handle",
     "KIND_NAMES", "STATUS",
 ]
@@ -83,6 +83,8 @@ def load(path=None):
     L.dmuon_newton_schulz.restype = i32
     L.dmuon_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), i32]
     L.dmuon_get_status.restype = i32
+    L.dmuon_last_error.argtypes = [vp]
+    L.dmuon_last_error.restype = ctypes.c_char_p
     L.dmuon_launch_count.argtypes = [vp]
     L.dmuon_launch_count.restype = i64
     L.dmuon_profile_enable.argtypes = [vp, i32]
@@ -100,8 +102,10 @@ def load(path=None):
     return L
 
 
-def _check(code, what):
+def _check(code, what, h=None):
     if code != 0:
+        if h is not None and _lib is not None:
+            what = what + " [" + _lib.dmuon_last_error(h).decode() + "]"
         raise DmuonError(code, what)
 
 
@@ -191,7 +195,7 @@ def dmuon_step_ptrs(h, w_ptrs, g_ptrs, m_ptrs, shapes, lr, mu, ns_steps=5,
                       _shape_array(shapes), len(shapes), float(lr), float(mu), int(ns_steps),
                       ctypes.byref(opts), ctypes.c_void_p(_stream_handle(stream)))
     if check:
-        _check(rc, "dmuon_step")
+        _check(rc, "dmuon_step", h)
     return rc
 
 
@@ -214,7 +218,7 @@ def dmuon_newton_schulz_ptrs(h, in_ptrs, out_ptrs, shapes, ns_steps=5, coeffs=No
                                None if carr is None else ctypes.cast(carr, ctypes.POINTER(ctypes.c_float)),
                                float(eps), ctypes.c_void_p(_stream_handle(stream)))
     if check:
-        _check(rc, "dmuon_newton_schulz")
+        _check(rc, "dmuon_newton_schulz", h)
     return rc
 
 
@@ -231,6 +235,10 @@ def dmuon_get_status(h, n_flags=0):
     flags = (ctypes.c_int * max(1, n_flags))()
     rc = load().dmuon_get_status(h, flags, int(n_flags))
     return rc, [flags[i] for i in range(n_flags)]
+
+
+def dmuon_last_error(h):
+    return load().dmuon_last_error(h).decode()
 
 
 def dmuon_launch_count(h):

@@ -122,8 +122,8 @@ void make_layout(const dmuon_shape_t* shapes, int n, Layout& L) {
   const int64_t nt = L.tile_prefix[n];
   L.small_bytes = rup(sizeof(MatDesc) * n, 256) + rup(sizeof(MatPtrs) * n, 256) +
                   rup(sizeof(CUtensorMap) * kMapsPerMat * n, 256) + rup(8 * (n + 1), 256) +
-                  rup(4 * nt, 256) + 2 * rup(4 * n, 256) + 256 +
-                  rup(16 * (L.items[0].size() + L.items[1].size() + L.items[2].size()), 256);
+                  rup(4 * nt, 256) + 2 * rup(4 * n, 256) + 256 + rup(16 * L.items[0].size(), 256) +
+                  rup(16 * L.items[1].size(), 256) + rup(16 * L.items[2].size(), 256);
 }
 
 }  // namespace
@@ -161,11 +161,23 @@ struct dmuon_ctx {
   bool profiling = false;
   std::vector<ProfRec> prof;
   std::vector<cudaEvent_t> ev_pool;
+  std::string last_error;
 };
 
 namespace {
 
 int cuda_err(cudaError_t e) { return e == cudaSuccess ? DMUON_OK : (e == cudaErrorMemoryAllocation ? DMUON_ERR_OOM : DMUON_ERR_CUDA); }
+
+// Record what failed (readable through dmuon_last_error) and return `code`.
+int fail(dmuon_ctx* h, int code, const char* what, cudaError_t e = cudaSuccess) {
+  char buf[384];
+  if (e != cudaSuccess)
+    std::snprintf(buf, sizeof buf, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+  else
+    std::snprintf(buf, sizeof buf, "%s", what);
+  h->last_error = buf;
+  return code;
+}
 
 void free_plan(dmuon_ctx* h) {
   if (h->ws || h->small) cudaDeviceSynchronize();
@@ -186,13 +198,13 @@ bool same_shapes(const dmuon_ctx* h, const dmuon_shape_t* s, int n) {
 int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
   if (same_shapes(h, shapes, n)) return DMUON_OK;
   free_plan(h);
-  if (!get_encoder()) return DMUON_ERR_CUDA;
+  if (!get_encoder()) return fail(h, DMUON_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
   Layout& L = h->L;
   make_layout(shapes, n, L);
   cudaError_t e = cudaMalloc(&h->ws, std::max<size_t>(L.ws_bytes, 256));
-  if (e != cudaSuccess) { h->ws = nullptr; cudaGetLastError(); return DMUON_ERR_OOM; }
+  if (e != cudaSuccess) { h->ws = nullptr; cudaGetLastError(); return fail(h, DMUON_ERR_OOM, "workspace cudaMalloc", e); }
   e = cudaMalloc(&h->small, L.small_bytes);
-  if (e != cudaSuccess) { cudaFree(h->ws); h->ws = h->small = nullptr; cudaGetLastError(); return DMUON_ERR_OOM; }
+  if (e != cudaSuccess) { cudaFree(h->ws); h->ws = h->small = nullptr; cudaGetLastError(); return fail(h, DMUON_ERR_OOM, "descriptor cudaMalloc", e); }
   uint8_t* p = (uint8_t*)h->small;
   auto carve = [&](size_t bytes) { uint8_t* q = p; p += rup((int64_t)bytes, 256); return q; };
   const int64_t nt = L.tile_prefix[n];
@@ -219,7 +231,13 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
               encode_map(&maps[kMapsPerMat * i + 1], d.X[1], d.m, d.n, d.ldx) &&
               encode_map(&maps[kMapsPerMat * i + 2], d.A, d.m, d.m, d.lda) &&
               encode_map(&maps[kMapsPerMat * i + 3], d.B, d.m, d.m, d.lda);
-    if (!ok) { free_plan(h); return DMUON_ERR_CUDA; }
+    if (!ok) {
+      char what[160];
+      std::snprintf(what, sizeof what, "cuTensorMapEncodeTiled failed for matrix %d (%lld x %lld)", i,
+                    (long long)d.rows, (long long)d.cols);
+      free_plan(h);
+      return fail(h, DMUON_ERR_CUDA, what);
+    }
   }
   e = cudaMemcpy(h->d_mats, L.mats.data(), sizeof(MatDesc) * n, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->d_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice);
@@ -228,7 +246,7 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
     if (!L.items[q].empty()) e = cudaMemcpy(h->d_items[q], L.items[q].data(), 16 * L.items[q].size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(h->d_flags, 0, 4 * n);
   if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, 256);
-  if (e != cudaSuccess) { free_plan(h); return cuda_err(e); }
+  if (e != cudaSuccess) { free_plan(h); return fail(h, cuda_err(e), "plan upload", e); }
   h->shapes.assign(shapes, shapes + n);
   h->last_ptrs.clear();
   return DMUON_OK;
@@ -280,7 +298,7 @@ int check_shapes(const dmuon_shape_t* shapes, int n) {
 int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, float lr, float mu,
         int ns_steps, const float* coeffs, float eps, float wd, int nesterov, int scale_mode,
         int ns_only, cudaStream_t stream) {
-  if (cudaSetDevice(h->device) != cudaSuccess) return DMUON_ERR_CUDA;
+  if (cudaSetDevice(h->device) != cudaSuccess) return fail(h, DMUON_ERR_CUDA, "cudaSetDevice");
   int rc = build_plan(h, shapes, n);
   if (rc) return rc;
   Layout& L = h->L;
@@ -296,7 +314,7 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
   if (scale_dirty) {
     e = cudaStreamSynchronize(stream);
     if (e == cudaSuccess) e = cudaMemcpy(h->d_mats, L.mats.data(), sizeof(MatDesc) * n, cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return cuda_err(e);
+    if (e != cudaSuccess) return fail(h, cuda_err(e), "descriptor refresh", e);
   }
 
   // Upload caller pointers only when they differ from the previous call.
@@ -314,7 +332,7 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
     std::memcpy(h->h_stage, ptrs, sizeof(MatPtrs) * n);
     e = cudaMemcpyAsync(h->d_ptrs, h->h_stage, sizeof(MatPtrs) * n, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) e = cudaEventRecord(h->stage_ev, stream);
-    if (e != cudaSuccess) return cuda_err(e);
+    if (e != cudaSuccess) return fail(h, cuda_err(e), "pointer upload", e);
     h->stage_pending = true;
     h->last_ptrs.assign(ptrs, ptrs + n);
   }
@@ -325,19 +343,19 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
     MomArgs a{h->d_mats, h->d_ptrs, h->d_prefix, n, nt, mu, nesterov, ns_only, h->d_partials};
     const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
     LaunchGuard g(h, stream, DMUON_KIND_MOMENTUM);
-    if ((e = launch_mom(a, grid, stream)) != cudaSuccess) return cuda_err(e);
+    if ((e = launch_mom(a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "mom_norm launch", e);
   }
   {
     FinalizeArgs a{h->d_mats, h->d_prefix, h->d_partials, n, eps, h->d_svec, h->d_flags};
     LaunchGuard g(h, stream, DMUON_KIND_FINALIZE);
-    if ((e = launch_finalize(a, stream)) != cudaSuccess) return cuda_err(e);
+    if ((e = launch_finalize(a, stream)) != cudaSuccess) return fail(h, cuda_err(e), "finalize launch", e);
   }
   const float decay = 1.f - lr * wd;
   if (ns_steps == 0) {
     Update0Args a{h->d_mats, h->d_ptrs, h->d_prefix, n, nt, h->d_svec, lr, decay, ns_only};
     const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
     LaunchGuard g(h, stream, DMUON_KIND_UPDATE0);
-    if ((e = launch_update0(a, grid, stream)) != cudaSuccess) return cuda_err(e);
+    if ((e = launch_update0(a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "update0 launch", e);
     return DMUON_OK;
   }
   static const int kKinds[3] = {DMUON_KIND_GRAM, DMUON_KIND_GRAM2, DMUON_KIND_APPLY};
@@ -361,7 +379,7 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
       const int grid = std::min(a.n_items, h->num_sms);
       if (grid <= 0) continue;
       LaunchGuard g(h, stream, kKinds[p]);
-      if ((e = launch_gemm(p, a, grid, stream)) != cudaSuccess) return cuda_err(e);
+      if ((e = launch_gemm(p, a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "ns_gemm launch", e);
     }
   }
   return DMUON_OK;
@@ -484,7 +502,7 @@ int dmuon_get_status(dmuon_handle_t h, int* flags, int n_flags) {
   if (!h || n_flags < 0) return DMUON_ERR_ARG;
   if (cudaSetDevice(h->device) != cudaSuccess) return DMUON_ERR_CUDA;
   cudaError_t e = h->last_stream ? cudaStreamSynchronize(h->last_stream) : cudaDeviceSynchronize();
-  if (e != cudaSuccess) return DMUON_ERR_CUDA;
+  if (e != cudaSuccess) return fail(h, DMUON_ERR_CUDA, "stream synchronize", e);
   if (!h->small) return DMUON_OK;
   const int n = (int)h->shapes.size();
   std::vector<int> f(n, 0);
@@ -503,6 +521,11 @@ int dmuon_get_status(dmuon_handle_t h, int* flags, int n_flags) {
 }
 
 int64_t dmuon_launch_count(dmuon_handle_t h) { return h ? h->launches : -1; }
+
+const char* dmuon_last_error(dmuon_handle_t h) {
+  if (!h) return "null handle";
+  return h->last_error.c_str();
+}
 
 int dmuon_profile_enable(dmuon_handle_t h, int on) {
   if (!h) return DMUON_ERR_ARG;

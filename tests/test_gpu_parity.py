@@ -197,7 +197,8 @@ def test_argument_errors_with_live_handle(handle):
     before = dm.dmuon_launch_count(h)
     assert call(w=[p(W) + 4]) == -2
     assert call(s=[(0, 64)]) == -1
-    assert call(s=[(64, 40000)]) == -1
+    assert call(s=[(40000, 40000)]) == -1          # short side above the limit
+    assert call(s=[(64, (1 << 20) + 1)]) == -1     # long side above the limit
     assert call(ns=65) == -1
     assert call(ns=-1) == -1
     assert call(sm=3) == -1
