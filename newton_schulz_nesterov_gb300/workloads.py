@@ -17,6 +17,8 @@ Linear(ff, d) [d, ff] -- and Llama-3 projection shapes):
                   o 4096x4096, gate 14336x4096, up 14336x4096,
                   down 4096x14336} = 224 matrices; grads N(0, 1e-3^2);
                   momentum starts at zero with one warm step
+  llama3_8b_1layer  the first layer of llama3_8b alone (7 matrices, 1.6 GB
+                  of W/G/M: larger than L2, small enough to profile)
   spiked_4096     64 x 4096x4096; grads N(0, 1) plus a rank-16 spike
                   sum_i s_i u_i v_i^T, u, v orthonormal, s_i log-spaced from
                   1e2 down to 1e-3; momentum zero
@@ -66,6 +68,8 @@ WORKLOADS = {
                              note="TinyMLP d=512 ff=2048, 12 matrices, 3rd step"),
     "llama3_8b": Workload("llama3_8b", _llama3_8b(), 1e-3, "zero", 1, seed=1237,
                           note="Llama-3-8B projections, 224 matrices"),
+    "llama3_8b_1layer": Workload("llama3_8b_1layer", _llama3_8b()[:7], 1e-3, "zero", 1, seed=1237,
+                                 note="one Llama-3-8B layer, 7 matrices (profiling case)"),
     "spiked_4096": Workload("spiked_4096", tuple([(4096, 4096)] * 64), 1.0, "zero", 0,
                             spike_rank=16, seed=1238,
                             note="64 x 4096^2 with rank-16 spike"),
