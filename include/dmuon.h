@@ -138,6 +138,41 @@ int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs,
                         float eps, void* stream);
 
 /*
+ * Allocation-free standalone Newton-Schulz of ONE matrix.  The pages have no
+ * counterpart of this entry point; it exists for callers that may not call
+ * cudaMalloc (a host framework whose allocator owns all device memory, a
+ * plugin that is handed only its input and output buffers, a latency path
+ * that cannot take cudaMalloc's implicit synchronisation).  It needs no
+ * handle and allocates nothing: its scratch (bf16 iterate, products, tile
+ * sums, descriptor, tensor maps, work lists) is one file-scope static device
+ * array of about 12.9 MB that every GPU loading the library holds until
+ * process exit.
+ *
+ *   input, output  device fp32 rows x cols, row-major, 16-byte aligned, not
+ *                  overlapping; output = O of input (same maths and
+ *                  arithmetic as dmuon_newton_schulz)
+ *   limits         min(rows, cols) <= 1024 and rows*cols <= 2^21, else
+ *                  DMUON_ERR_ARG before anything is launched
+ *   ns_steps, coeffs, eps   as in dmuon_newton_schulz
+ *   sync_status    0: asynchronous on `stream`, device-side problems are not
+ *                  reported; non-zero: the call waits for its work and
+ *                  returns DMUON_ERR_NONFINITE / DMUON_ERR_TIMEOUT if the
+ *                  kernels recorded one
+ *   stream         a cudaStream_t on the current device
+ *
+ * The first call on a device does a one-time set-up with that device current
+ * (cudaGetSymbolAddress of the array, kernel attributes); make that first
+ * call before any stream capture.  Every call shares the array and leaves
+ * its contents behind; each call zeroes what must start at zero.  Calls
+ * whose GPU work overlaps in time (unordered streams, several host threads)
+ * race on the array.
+ */
+int dmuon_newton_schulz_noalloc(const float* input, float* output,
+                                int64_t rows, int64_t cols, int ns_steps,
+                                const float* coeffs, float eps,
+                                int sync_status, void* stream);
+
+/*
  * Wait for the handle's stream work to finish and report what the kernels
  * recorded since the previous call of this function: per-matrix flags of
  * the last planned list (bit 0: non-finite input) are copied to

@@ -15,7 +15,8 @@ import os
 __all__ = [
     "DmuonError", "load", "lib_path", "dmuon_create", "dmuon_destroy",
     "dmuon_step", "dmuon_step_ptrs", "dmuon_newton_schulz",
-    "dmuon_newton_schulz_ptrs", "dmuon_get_status", "dmuon_workspace_bytes",
+    "dmuon_newton_schulz_ptrs", "dmuon_newton_schulz_noalloc", "dmuon_get_status",
+    "dmuon_workspace_bytes",
     "dmuon_launch_count", "dmuon_last_error", "dmuon_profile_enable", "dmuon_profile_read",
     "dmuon_plan_summary", "dmuon_error_string", "dmuon_version", "Handle",
     "KIND_NAMES", "STATUS",
@@ -81,6 +82,9 @@ def load(path=None):
     L.dmuon_newton_schulz.argtypes = [vp, pp, pp, ctypes.POINTER(Shape), i32, i32,
                                       ctypes.POINTER(ctypes.c_float), f32, vp]
     L.dmuon_newton_schulz.restype = i32
+    L.dmuon_newton_schulz_noalloc.argtypes = [vp, vp, i64, i64, i32, ctypes.POINTER(ctypes.c_float),
+                                              f32, i32, vp]
+    L.dmuon_newton_schulz_noalloc.restype = i32
     L.dmuon_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), i32]
     L.dmuon_get_status.restype = i32
     L.dmuon_last_error.argtypes = [vp]
@@ -228,6 +232,17 @@ def dmuon_newton_schulz(h, inputs, outputs, ns_steps=5, coeffs=None, eps=1e-7, s
     if is_ != os_:
         raise ValueError("inputs and outputs must have matching shapes")
     return dmuon_newton_schulz_ptrs(h, ip, op, is_, ns_steps, coeffs, eps, stream)
+
+
+def dmuon_newton_schulz_noalloc(input_ptr, output_ptr, rows, cols, ns_steps=5, coeffs=None,
+                                eps=1e-7, sync_status=True, stream=None):
+    """Allocation-free standalone NS of one matrix (raw device pointers);
+    returns the status code."""
+    carr = _coeff_array(coeffs)
+    return load().dmuon_newton_schulz_noalloc(
+        ctypes.c_void_p(int(input_ptr)), ctypes.c_void_p(int(output_ptr)), int(rows), int(cols),
+        int(ns_steps), None if carr is None else ctypes.cast(carr, ctypes.POINTER(ctypes.c_float)),
+        float(eps), 1 if sync_status else 0, ctypes.c_void_p(_stream_handle(stream)))
 
 
 def dmuon_get_status(h, n_flags=0):
