@@ -112,8 +112,10 @@ void make_layout(const dmuon_shape_t* shapes, int n, Layout& L) {
           L.items[kPhaseGram].push_back(make_int4(i, (int)ti, (int)J, kg));
           L.items[kPhaseGram2].push_back(make_int4(i, (int)ti, (int)J, km));
         }
-    for (int64_t ti = 0; ti < cdiv(d.m, kBM); ++ti)
-      for (int64_t tj = 0; tj < cdiv(d.n, kBN); ++tj)
+    // Column-panel-major: CTAs running together share 256-column panels of
+    // X (each read from DRAM once) while B (m x m) stays resident in L2.
+    for (int64_t tj = 0; tj < cdiv(d.n, kBN); ++tj)
+      for (int64_t ti = 0; ti < cdiv(d.m, kBM); ++ti)
         L.items[kPhaseApply].push_back(make_int4(i, (int)ti, (int)tj, km));
   }
   for (int p = 0; p < 3; ++p)

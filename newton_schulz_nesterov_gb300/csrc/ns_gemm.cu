@@ -211,39 +211,49 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
         for (int k = 0; k < 16; ++k) w[k] = pack2(o[2 * k], o[2 * k + 1]);
         store_row32(xd + r * ldx, c, n, row_ok, w);
       } else if (row_ok) {
+        // All loads of W for this chunk are issued before any store, so the
+        // 32 reads are in flight together instead of one round trip each.
         const bool upd = a.final_mode == kUpdateW;
         if (!d.transposed) {
           // W is m x n: row r, columns c..c+31.
           float* wp = p.W + r * d.cols + c;
           if (c + 32 <= n && (d.cols & 3) == 0) {
             float4* w4 = reinterpret_cast<float4*>(wp);
+            float4 cur[8];
+            if (upd) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) cur[q] = __ldcs(w4 + q);
+            }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               float4 o4 = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
               if (upd) {
-                const float4 cur = w4[q];
-                o4.x = fmaf(a.decay, cur.x, -coef * o4.x);
-                o4.y = fmaf(a.decay, cur.y, -coef * o4.y);
-                o4.z = fmaf(a.decay, cur.z, -coef * o4.z);
-                o4.w = fmaf(a.decay, cur.w, -coef * o4.w);
+                o4.x = fmaf(a.decay, cur[q].x, -coef * o4.x);
+                o4.y = fmaf(a.decay, cur[q].y, -coef * o4.y);
+                o4.z = fmaf(a.decay, cur[q].z, -coef * o4.z);
+                o4.w = fmaf(a.decay, cur[q].w, -coef * o4.w);
               }
-              w4[q] = o4;
+              __stcs(w4 + q, o4);
             }
           } else {
+            float cur[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cur[j] = (upd && c + j < n) ? wp[j] : 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (c + j < n) wp[j] = upd ? fmaf(a.decay, wp[j], -coef * o[j]) : o[j];
+              if (c + j < n) wp[j] = upd ? fmaf(a.decay, cur[j], -coef * o[j]) : o[j];
           }
         } else {
           // W is n x m: element (c + j, r); lanes hold consecutive r, so
           // each j is one coalesced 128-byte warp access.
+          float* wcol = p.W + c * d.cols + r;
+          const int64_t ldw = d.cols;
+          float cur[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (c + j < n) {
-              float* wp = p.W + (c + j) * d.cols + r;
-              *wp = upd ? fmaf(a.decay, *wp, -coef * o[j]) : o[j];
-            }
-          }
+          for (int j = 0; j < 32; ++j) cur[j] = (upd && c + j < n) ? __ldcs(wcol + j * ldw) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c + j < n) __stcs(wcol + j * ldw, upd ? fmaf(a.decay, cur[j], -coef * o[j]) : o[j]);
         }
       }
     }
