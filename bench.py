@@ -194,6 +194,28 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ ranks
+def rank_workload(name, rank):
+    """Rank r's own problem: the named workload's shapes with inputs drawn
+    from a rank-specific seed (independent problems per rank, weak scaling)."""
+    import dataclasses
+    from newton_schulz_nesterov_gb300 import workloads
+    w = workloads.get(name)
+    return w if rank == 0 else dataclasses.replace(w, seed=w.seed + 7919 * rank)
+
+
+def max_over_ranks(value, world):
+    """Max of a per-rank float over the process group (identity at N = 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ ours
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -203,7 +225,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     _build.build()
-    w = workloads.get(args.workload)
+    w = rank_workload(args.workload, rank)
     n = len(w.shapes)
     shapes = list(w.shapes)
     lr, mu = 0.02, 0.95
@@ -263,11 +285,7 @@ def run_ours(args, rank, world, local_rank):
     rc, _ = h.status()
     if rc != 0:
         raise RuntimeError("timed status %d" % rc)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     sec = ms / 1e3
     fl = flops.algorithmic_flops(shapes)
     value = fl * args.steps * world / sec / 1e12

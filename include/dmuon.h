@@ -186,6 +186,14 @@ int dmuon_get_status(dmuon_handle_t h, int* flags, int n_flags);
  * CUDA error), "" if none; valid until the next call on the handle. */
 const char* dmuon_last_error(dmuon_handle_t h);
 
+/* Bounded waits: how long a tensor-core kernel's pipeline wait may go without
+ * progress before the kernel gives up, drains its own copies, frees its
+ * tensor memory, returns, and dmuon_get_status reports DMUON_ERR_TIMEOUT.
+ * ns == 0 restores the default (4 s).  Applies to later launches of the
+ * handle; a tiny value makes the first non-immediate wait give up, which
+ * is how the failure path is exercised without faulting the GPU. */
+int dmuon_set_wait_timeout(dmuon_handle_t h, uint64_t ns);
+
 /* Kernel launches issued by this handle since creation (a counter). */
 int64_t dmuon_launch_count(dmuon_handle_t h);
 

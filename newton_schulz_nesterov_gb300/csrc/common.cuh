@@ -82,6 +82,7 @@ struct GemmArgs {
   float lr, decay;         // W <- decay*W - lr*scale*O
   const float* svec;       // per-matrix 1/(||U||_F + eps)
   int* err;                // device error word (bit 0: wait timeout)
+  unsigned long long timeout_ns;  // wait without progress before giving up (0 = 4 s)
 };
 
 struct MomArgs {

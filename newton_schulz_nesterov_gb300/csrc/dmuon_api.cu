@@ -164,6 +164,7 @@ struct dmuon_ctx {
   std::vector<ProfRec> prof;
   std::vector<cudaEvent_t> ev_pool;
   std::string last_error;
+  unsigned long long wait_timeout_ns = 0;  // 0: kernels' default (4 s)
 };
 
 namespace {
@@ -378,6 +379,7 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
       a.decay = decay;
       a.svec = h->d_svec;
       a.err = h->d_err;
+      a.timeout_ns = h->wait_timeout_ns;
       const int grid = std::min(a.n_items, h->num_sms);
       if (grid <= 0) continue;
       LaunchGuard g(h, stream, kKinds[p]);
@@ -527,6 +529,12 @@ int64_t dmuon_launch_count(dmuon_handle_t h) { return h ? h->launches : -1; }
 const char* dmuon_last_error(dmuon_handle_t h) {
   if (!h) return "null handle";
   return h->last_error.c_str();
+}
+
+int dmuon_set_wait_timeout(dmuon_handle_t h, uint64_t ns) {
+  if (!h) return DMUON_ERR_ARG;
+  h->wait_timeout_ns = ns;
+  return DMUON_OK;
 }
 
 int dmuon_profile_enable(dmuon_handle_t h, int on) {

@@ -22,7 +22,8 @@
 // Two 256-column accumulators in TMEM let the epilogue of one tile overlap
 // the main loop of the next.
 //
-// Every mbarrier wait is bounded (kTimeoutNs); on timeout the CTA records
+// Every mbarrier wait is bounded (GemmArgs::timeout_ns, default 4 s without
+// progress); on timeout the CTA records
 // bit 0 of *err, stops issuing, drains its own copies and MMAs with bounded
 // waits, frees TMEM and returns.
 #include "common.cuh"
@@ -32,7 +33,8 @@ namespace dmuon {
 
 namespace {
 
-constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s without progress
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // default: 4 s without progress
+constexpr uint64_t kDrainTimeoutNs = 4000000000ull;  // drains after an abort
 
 struct Smem {
   uint8_t* stages;     // kStages x (A 16 KB | B 32 KB), 1024-aligned
@@ -55,12 +57,12 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 }
 
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       int* err, bool honour_abort) {
+                                       int* err, bool honour_abort, uint64_t limit_ns) {
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
     if (ptx::mbar_try(bar, parity)) return true;
     if (honour_abort && *abort_flag) return false;
-    if (ptx::globaltimer() - t0 > kTimeoutNs) {
+    if (ptx::globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(err, 1);
       return false;
@@ -69,9 +71,9 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
 }
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         int* err) {
+                                         int* err, uint64_t limit_ns) {
   if (ptx::mbar_try(bar, parity)) return true;
-  return wait_slow(bar, parity, abort_flag, err, true);
+  return wait_slow(bar, parity, abort_flag, err, true, limit_ns);
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -144,7 +146,7 @@ __device__ __forceinline__ void mirror_store32(__nv_bfloat16* base, int64_t ld, 
   store_row32(base + dr * ld, rbase, n_lim, dr < n_lim, t);
 }
 
-template <int PHASE>
+template <int PHASE, int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item, uint32_t tacc,
                                               int quad, int lane, uint32_t* scratch) {
   const MatDesc& d = a.mats[item.x];
@@ -205,7 +207,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
       float o[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) o[j] = alpha * fmaf(a.ca, xv[j], __uint_as_float(v[j]));
-      if (a.final_mode == kWriteX) {
+      if constexpr (MODE == kWriteX) {
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) w[k] = pack2(o[2 * k], o[2 * k + 1]);
@@ -213,7 +215,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
       } else if (row_ok) {
         // All loads of W for this chunk are issued before any store, so the
         // 32 reads are in flight together instead of one round trip each.
-        const bool upd = a.final_mode == kUpdateW;
+        constexpr bool upd = MODE == kUpdateW;
         if (!d.transposed) {
           // W is m x n: row r, columns c..c+31.
           float* wp = p.W + r * d.cols + c;
@@ -260,12 +262,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
   }
 }
 
-template <int PHASE>
+template <int PHASE, int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const Smem sm = carve(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint64_t tmo = a.timeout_ns ? a.timeout_ns : kTimeoutNs;
 
   uint64_t* full = sm.bars;
   uint64_t* empty = sm.bars + kStages;
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         for (int kb = 0; kb < item.w; ++kb, ++it) {
           const uint32_t s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          if (!wait_bar(ptx::smem_addr(empty + s), ph ^ 1u, sm.abort_flag, a.err)) { ok = false; break; }
+          if (!wait_bar(ptx::smem_addr(empty + s), ph ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
           const uint32_t fb = ptx::smem_addr(full + s);
           ptx::mbar_expect_tx(fb, kStageBytes);
           const uint32_t sa = ptx::smem_addr(sm.stages + s * kStageBytes);
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         const uint32_t n_out = it < (uint32_t)kStages ? it : (uint32_t)kStages;
         for (uint32_t i = it - n_out; i < it; ++i)
           wait_slow(ptx::smem_addr(full + (i % kStages)), (i / kStages) & 1u, sm.abort_flag,
-                    a.err, false);
+                    a.err, false, kDrainTimeoutNs);
       }
     }
   } else if (warp == 1) {
@@ -353,13 +356,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x, ++tc) {
         const int4 item = a.items[w];
         const uint32_t acc = tc & 1u;
-        if (!wait_bar(ptx::smem_addr(tempty + acc), ((tc >> 1) & 1u) ^ 1u, sm.abort_flag, a.err)) { ok = false; break; }
+        if (!wait_bar(ptx::smem_addr(tempty + acc), ((tc >> 1) & 1u) ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t dt = tmem_base + acc * kBN;
         for (int kb = 0; kb < item.w; ++kb, ++it) {
           const uint32_t s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          if (!wait_bar(ptx::smem_addr(full + s), ph, sm.abort_flag, a.err)) { ok = false; break; }
+          if (!wait_bar(ptx::smem_addr(full + s), ph, sm.abort_flag, a.err, tmo)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t sa = ptx::smem_addr(sm.stages + s * kStageBytes);
           const uint32_t sb = sa + kABytes;
@@ -378,7 +381,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       }
       if (issued && (!ok || *sm.abort_flag)) {
         ptx::mma_commit(ptx::smem_addr(drain));
-        wait_slow(ptx::smem_addr(drain), 0, sm.abort_flag, a.err, false);
+        wait_slow(ptx::smem_addr(drain), 0, sm.abort_flag, a.err, false, kDrainTimeoutNs);
       }
     }
   } else {
@@ -389,9 +392,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     for (int w = blockIdx.x; w < a.n_items; w += gridDim.x, ++tc) {
       const int4 item = a.items[w];
       const uint32_t acc = tc & 1u;
-      if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err)) break;
+      if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err, tmo)) break;
       ptx::tc_fence_after();
-      epilogue_tile<PHASE>(a, item, tmem_base + acc * kBN, quad, lane, scratch);
+      epilogue_tile<PHASE, MODE>(a, item, tmem_base + acc * kBN, quad, lane, scratch);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(tempty + acc));
@@ -408,20 +411,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 
 }  // namespace
 
-cudaError_t gemm_configure() {
-  cudaError_t e;
-  e = cudaFuncSetAttribute(ns_gemm_kernel<kPhaseGram>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(ns_gemm_kernel<kPhaseGram2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(ns_gemm_kernel<kPhaseApply>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+template <int PHASE, int MODE>
+cudaError_t configure_one() {
+  return cudaFuncSetAttribute(ns_gemm_kernel<PHASE, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kGemmSmem);
 }
 
+cudaError_t gemm_configure() {
+  cudaError_t e;
+  if ((e = configure_one<kPhaseGram, kWriteX>()) != cudaSuccess) return e;
+  if ((e = configure_one<kPhaseGram2, kWriteX>()) != cudaSuccess) return e;
+  if ((e = configure_one<kPhaseApply, kWriteX>()) != cudaSuccess) return e;
+  if ((e = configure_one<kPhaseApply, kUpdateW>()) != cudaSuccess) return e;
+  return configure_one<kPhaseApply, kWriteO>();
+}
+
+// Apply launches pick the kernel variant of their final mode, so each
+// variant carries only the epilogue it runs.
 cudaError_t launch_gemm(int phase, const GemmArgs& a, int grid, cudaStream_t s) {
-  switch (phase) {
-    case kPhaseGram: ns_gemm_kernel<kPhaseGram><<<grid, kGemmThreads, kGemmSmem, s>>>(a); break;
-    case kPhaseGram2: ns_gemm_kernel<kPhaseGram2><<<grid, kGemmThreads, kGemmSmem, s>>>(a); break;
-    default: ns_gemm_kernel<kPhaseApply><<<grid, kGemmThreads, kGemmSmem, s>>>(a); break;
+  if (phase == kPhaseGram) {
+    ns_gemm_kernel<kPhaseGram, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+  } else if (phase == kPhaseGram2) {
+    ns_gemm_kernel<kPhaseGram2, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+  } else if (a.final_mode == kUpdateW) {
+    ns_gemm_kernel<kPhaseApply, kUpdateW><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+  } else if (a.final_mode == kWriteO) {
+    ns_gemm_kernel<kPhaseApply, kWriteO><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+  } else {
+    ns_gemm_kernel<kPhaseApply, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
   }
   return cudaGetLastError();
 }

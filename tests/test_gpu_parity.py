@@ -209,6 +209,27 @@ def test_argument_errors_with_live_handle(handle):
     assert dm.dmuon_launch_count(h) == before  # nothing launched
 
 
+def test_wait_timeout_is_reported_and_context_recovers(handle):
+    """A 1 ns wait limit makes the GEMM kernels give up at their first
+    non-immediate wait: they drain, free TMEM and return; the host reads
+    DMUON_ERR_TIMEOUT, and with the default limit restored the next step is
+    correct again."""
+    shapes = [(384, 200), (200, 640)]
+    gen = torch.Generator().manual_seed(3)
+    Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
+    Gs = [torch.randn(s, generator=gen) for s in shapes]
+    Ms = [torch.randn(s, generator=gen) for s in shapes]
+    dm.dmuon_set_wait_timeout(handle.h, 1)
+    try:
+        handle.step(_to_dev(Ws), _to_dev(Gs), _to_dev(Ms))
+        rc, _ = handle.status(2)
+    finally:
+        dm.dmuon_set_wait_timeout(handle.h, 0)
+    assert rc == -6
+    assert handle.status(2)[0] == 0   # the error word was cleared by the read
+    _step_and_check(handle, Ws, Gs, Ms)
+
+
 def test_launch_count_and_profile(handle):
     shapes = [(256, 512), (512, 256)]
     Ws = [torch.zeros(s, device="cuda") for s in shapes]
