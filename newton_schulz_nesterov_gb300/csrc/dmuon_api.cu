@@ -35,6 +35,9 @@ const float kYouCoefficients[5][3] = {
 
 const char* kVersion = "dmuon-gb300 0.1.0 (sm_103a, tcgen05/TMA)";
 
+// Cached caller pointer sets per plan (see run()).
+constexpr int kPtrSlots = 64;
+
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
@@ -122,7 +125,7 @@ void make_layout(const dmuon_shape_t* shapes, int n, Layout& L) {
     std::stable_sort(L.items[p].begin(), L.items[p].end(),
                      [](const int4& x, const int4& y) { return x.w > y.w; });
   const int64_t nt = L.tile_prefix[n];
-  L.small_bytes = rup(sizeof(MatDesc) * n, 256) + rup(sizeof(MatPtrs) * n, 256) +
+  L.small_bytes = rup(sizeof(MatDesc) * n, 256) + rup(sizeof(MatPtrs) * n * kPtrSlots, 256) +
                   rup(sizeof(CUtensorMap) * kMapsPerMat * n, 256) + rup(8 * (n + 1), 256) +
                   rup(4 * nt, 256) + 2 * rup(4 * n, 256) + 256 + rup(16 * L.items[0].size(), 256) +
                   rup(16 * L.items[1].size(), 256) + rup(16 * L.items[2].size(), 256);
@@ -153,11 +156,13 @@ struct dmuon_ctx {
   int* d_err = nullptr;
   int4* d_items[3] = {nullptr, nullptr, nullptr};
   // pointer cache
-  std::vector<MatPtrs> last_ptrs;
-  MatPtrs* h_stage = nullptr;
-  size_t h_stage_cap = 0;
-  cudaEvent_t stage_ev = nullptr;
-  bool stage_pending = false;
+  // pointer-set cache: kPtrSlots device slots of n MatPtrs each
+  std::vector<MatPtrs> slot_ptrs[kPtrSlots];
+  uint64_t slot_use[kPtrSlots] = {};
+  bool slot_pending[kPtrSlots] = {};
+  cudaEvent_t slot_ev[kPtrSlots] = {};
+  uint64_t use_clock = 0;
+  MatPtrs* h_stage = nullptr;  // pinned staging, kPtrSlots x n
   cudaStream_t last_stream = nullptr;
   int64_t launches = 0;
   bool profiling = false;
@@ -188,7 +193,14 @@ void free_plan(dmuon_ctx* h) {
   if (h->small) cudaFree(h->small);
   h->ws = h->small = nullptr;
   h->shapes.clear();
-  h->last_ptrs.clear();
+  for (int k = 0; k < kPtrSlots; ++k) {
+    if (h->slot_pending[k]) cudaEventSynchronize(h->slot_ev[k]);
+    h->slot_pending[k] = false;
+    h->slot_ptrs[k].clear();
+    h->slot_use[k] = 0;
+  }
+  if (h->h_stage) cudaFreeHost(h->h_stage);
+  h->h_stage = nullptr;
 }
 
 bool same_shapes(const dmuon_ctx* h, const dmuon_shape_t* s, int n) {
@@ -212,7 +224,7 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
   auto carve = [&](size_t bytes) { uint8_t* q = p; p += rup((int64_t)bytes, 256); return q; };
   const int64_t nt = L.tile_prefix[n];
   h->d_mats = (MatDesc*)carve(sizeof(MatDesc) * n);
-  h->d_ptrs = (MatPtrs*)carve(sizeof(MatPtrs) * n);
+  h->d_ptrs = (MatPtrs*)carve(sizeof(MatPtrs) * n * kPtrSlots);
   h->d_maps = (CUtensorMap*)carve(sizeof(CUtensorMap) * kMapsPerMat * n);
   h->d_prefix = (int64_t*)carve(8 * (n + 1));
   h->d_partials = (float*)carve(4 * nt);
@@ -250,8 +262,12 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
   if (e == cudaSuccess) e = cudaMemset(h->d_flags, 0, 4 * n);
   if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, 256);
   if (e != cudaSuccess) { free_plan(h); return fail(h, cuda_err(e), "plan upload", e); }
+  if (cudaMallocHost(&h->h_stage, sizeof(MatPtrs) * n * kPtrSlots) != cudaSuccess) {
+    h->h_stage = nullptr;
+    free_plan(h);
+    return fail(h, DMUON_ERR_OOM, "pinned pointer staging");
+  }
   h->shapes.assign(shapes, shapes + n);
-  h->last_ptrs.clear();
   return DMUON_OK;
 }
 
@@ -320,30 +336,39 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
     if (e != cudaSuccess) return fail(h, cuda_err(e), "descriptor refresh", e);
   }
 
-  // Upload caller pointers only when they differ from the previous call.
-  bool same = (int)h->last_ptrs.size() == n;
-  for (int i = 0; same && i < n; ++i)
-    same = h->last_ptrs[i].W == ptrs[i].W && h->last_ptrs[i].G == ptrs[i].G && h->last_ptrs[i].M == ptrs[i].M;
-  if (!same) {
-    if (h->stage_pending) { cudaEventSynchronize(h->stage_ev); h->stage_pending = false; }
-    if (h->h_stage_cap < (size_t)n) {
-      if (h->h_stage) cudaFreeHost(h->h_stage);
-      h->h_stage = nullptr;
-      if (cudaMallocHost(&h->h_stage, sizeof(MatPtrs) * n) != cudaSuccess) { h->h_stage_cap = 0; return DMUON_ERR_OOM; }
-      h->h_stage_cap = n;
-    }
-    std::memcpy(h->h_stage, ptrs, sizeof(MatPtrs) * n);
-    e = cudaMemcpyAsync(h->d_ptrs, h->h_stage, sizeof(MatPtrs) * n, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaEventRecord(h->stage_ev, stream);
-    if (e != cudaSuccess) return fail(h, cuda_err(e), "pointer upload", e);
-    h->stage_pending = true;
-    h->last_ptrs.assign(ptrs, ptrs + n);
+  // Caller pointer sets are cached in kPtrSlots device slots (least recently
+  // used is replaced), so alternating between a few lists of buffers -- e.g.
+  // one call per layer -- uploads nothing after the first round.
+  int slot = -1;
+  for (int k = 0; k < kPtrSlots && slot < 0; ++k) {
+    const std::vector<MatPtrs>& sp = h->slot_ptrs[k];
+    if ((int)sp.size() != n) continue;
+    bool same = true;
+    for (int i = 0; same && i < n; ++i)
+      same = sp[i].W == ptrs[i].W && sp[i].G == ptrs[i].G && sp[i].M == ptrs[i].M;
+    if (same) slot = k;
   }
+  if (slot < 0) {
+    slot = 0;
+    for (int k = 1; k < kPtrSlots; ++k)
+      if (h->slot_use[k] < h->slot_use[slot]) slot = k;
+    // The slot's pinned staging may still feed an earlier copy.
+    if (h->slot_pending[slot]) { cudaEventSynchronize(h->slot_ev[slot]); h->slot_pending[slot] = false; }
+    MatPtrs* stage = h->h_stage + (size_t)slot * n;
+    std::memcpy(stage, ptrs, sizeof(MatPtrs) * n);
+    e = cudaMemcpyAsync(h->d_ptrs + (size_t)slot * n, stage, sizeof(MatPtrs) * n, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaEventRecord(h->slot_ev[slot], stream);
+    if (e != cudaSuccess) return fail(h, cuda_err(e), "pointer upload", e);
+    h->slot_pending[slot] = true;
+    h->slot_ptrs[slot].assign(ptrs, ptrs + n);
+  }
+  h->slot_use[slot] = ++h->use_clock;
+  const MatPtrs* dptrs = h->d_ptrs + (size_t)slot * n;
   h->last_stream = stream;
 
   const int64_t nt = L.tile_prefix[n];
   {
-    MomArgs a{h->d_mats, h->d_ptrs, h->d_prefix, n, nt, mu, nesterov, ns_only, h->d_partials};
+    MomArgs a{h->d_mats, dptrs, h->d_prefix, n, nt, mu, nesterov, ns_only, h->d_partials};
     const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
     LaunchGuard g(h, stream, DMUON_KIND_MOMENTUM);
     if ((e = launch_mom(a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "mom_norm launch", e);
@@ -355,7 +380,7 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
   }
   const float decay = 1.f - lr * wd;
   if (ns_steps == 0) {
-    Update0Args a{h->d_mats, h->d_ptrs, h->d_prefix, n, nt, h->d_svec, lr, decay, ns_only};
+    Update0Args a{h->d_mats, dptrs, h->d_prefix, n, nt, h->d_svec, lr, decay, ns_only};
     const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
     LaunchGuard g(h, stream, DMUON_KIND_UPDATE0);
     if ((e = launch_update0(a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "update0 launch", e);
@@ -367,7 +392,7 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
     for (int p = 0; p < 3; ++p) {
       GemmArgs a{};
       a.mats = h->d_mats;
-      a.ptrs = h->d_ptrs;
+      a.ptrs = dptrs;
       a.tmaps = h->d_maps;
       a.items = h->d_items[p];
       a.n_items = (int)L.items[p].size();
@@ -424,7 +449,13 @@ int dmuon_create(dmuon_handle_t* out, int device) {
   dmuon_ctx* h = new dmuon_ctx();
   h->device = device;
   h->num_sms = sms;
-  if (cudaEventCreateWithFlags(&h->stage_ev, cudaEventDisableTiming) != cudaSuccess) { delete h; return DMUON_ERR_CUDA; }
+  for (int k = 0; k < kPtrSlots; ++k) {
+    if (cudaEventCreateWithFlags(&h->slot_ev[k], cudaEventDisableTiming) != cudaSuccess) {
+      for (int j = 0; j < k; ++j) cudaEventDestroy(h->slot_ev[j]);
+      delete h;
+      return DMUON_ERR_CUDA;
+    }
+  }
   *out = h;
   return DMUON_OK;
 }
@@ -434,8 +465,8 @@ void dmuon_destroy(dmuon_handle_t h) {
   cudaSetDevice(h->device);
   cudaDeviceSynchronize();
   free_plan(h);
-  if (h->h_stage) cudaFreeHost(h->h_stage);
-  if (h->stage_ev) cudaEventDestroy(h->stage_ev);
+  for (int k = 0; k < kPtrSlots; ++k)
+    if (h->slot_ev[k]) cudaEventDestroy(h->slot_ev[k]);
   for (auto& r : h->prof) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
   for (auto e : h->ev_pool) cudaEventDestroy(e);
   delete h;

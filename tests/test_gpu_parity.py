@@ -171,6 +171,34 @@ def test_deterministic_bitwise(handle):
         assert torch.equal(a, b)
 
 
+def test_alternating_pointer_sets(handle):
+    """Per-group calls (same shapes, different buffers) reuse cached pointer
+    slots: 70 groups cycle through the 64 slots twice, so slots are evicted
+    and refilled, and every group must still get its own result."""
+    gen = torch.Generator().manual_seed(17)
+    shapes = [(192, 320), (320, 96)]
+    groups = []
+    for _ in range(70):
+        Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
+        Gs = [torch.randn(s, generator=gen) for s in shapes]
+        Ms = [torch.randn(s, generator=gen) for s in shapes]
+        groups.append((Ws, Gs, Ms, _to_dev(Ws), _to_dev(Gs), _to_dev(Ms)))
+    for _ in range(2):
+        for Ws, Gs, Ms, Wd, Gd, Md in groups:
+            handle.step(Wd, Gd, Md)
+    assert handle.status()[0] == 0
+    for Ws, Gs, Ms, Wd, Gd, Md in groups:
+        W, M = [w.numpy() for w in Ws], [m.numpy() for m in Ms]
+        for _ in range(2):
+            for i in range(2):
+                out = oracle.muon_step(W[i], Gs[i].numpy(), M[i], lr=F32(0.02), mu=F32(0.95))
+                W[i], M[i] = out["W"], out["M"]
+        for i in range(2):
+            W0 = Ws[i].numpy().astype(np.float64)
+            assert rel_fro(Md[i].cpu().numpy(), M[i]) <= MOM_TOL
+            assert rel_fro(Wd[i].cpu().numpy().astype(np.float64) - W0, W[i] - W0) <= NS_TOL
+
+
 def test_nonfinite_is_flagged(handle):
     shapes = [(64, 96), (96, 64), (128, 128)]
     Ws = [torch.zeros(s, device="cuda") for s in shapes]
