@@ -194,6 +194,13 @@ const char* dmuon_last_error(dmuon_handle_t h);
  * is how the failure path is exercised without faulting the GPU. */
 int dmuon_set_wait_timeout(dmuon_handle_t h, uint64_t ns);
 
+/* Tensor-core tiling of later plans: 0 = automatic (CTA pairs when the device
+ * can co-schedule 2-CTA clusters, the default), 1 = single CTAs computing
+ * 128x256 tiles, 2 = CTA pairs computing 256x256 tiles (cta_group::2).  The
+ * result is the same maths with the same roundings; the choice only changes
+ * speed.  DMUON_ERR_UNSUPPORTED if pairs are requested but unavailable. */
+int dmuon_set_tile_mode(dmuon_handle_t h, int mode);
+
 /* Kernel launches issued by this handle since creation (a counter). */
 int64_t dmuon_launch_count(dmuon_handle_t h);
 

@@ -89,6 +89,8 @@ def load(path=None):
     L.dmuon_get_status.restype = i32
     L.dmuon_last_error.argtypes = [vp]
     L.dmuon_last_error.restype = ctypes.c_char_p
+    L.dmuon_set_tile_mode.argtypes = [vp, i32]
+    L.dmuon_set_tile_mode.restype = i32
     L.dmuon_set_wait_timeout.argtypes = [vp, ctypes.c_uint64]
     L.dmuon_set_wait_timeout.restype = i32
     L.dmuon_launch_count.argtypes = [vp]
@@ -252,6 +254,11 @@ def dmuon_get_status(h, n_flags=0):
     flags = (ctypes.c_int * max(1, n_flags))()
     rc = load().dmuon_get_status(h, flags, int(n_flags))
     return rc, [flags[i] for i in range(n_flags)]
+
+
+def dmuon_set_tile_mode(h, mode):
+    """0 automatic (CTA pairs), 1 single-CTA 128x256 tiles, 2 CTA-pair 256x256 tiles."""
+    _check(load().dmuon_set_tile_mode(h, int(mode)), "dmuon_set_tile_mode")
 
 
 def dmuon_set_wait_timeout(h, ns):

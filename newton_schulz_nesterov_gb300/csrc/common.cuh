@@ -63,6 +63,18 @@ constexpr int kEpiWords = 32 * 17;              // per-warp transpose scratch
 constexpr int kGemmSmem =
     1024 /*align slack*/ + kStages * kStageBytes + 4 * kEpiWords * 4 + 256;
 
+// CTA-pair variant (cta_group::2): a 2-CTA cluster computes a 256x256 tile,
+// each CTA loading its 128 rows of A and its 128-row half of B per K block,
+// so a stage is 32 KB per CTA and six stages fit.
+constexpr int kPairStages = 6;
+constexpr int kPairHalfBytes = 128 * kBK * 2;            // 16 KB
+constexpr int kPairStageBytes = 2 * kPairHalfBytes;      // 32 KB per CTA
+// The 16 KB guard after the stages keeps any operand read that overruns a
+// stage inside this CTA's shared memory.
+constexpr int kPairGuardBytes = 16384;
+constexpr int kPairSmem = 1024 /*align slack*/ + kPairStages * kPairStageBytes + kPairGuardBytes +
+                          4 * kEpiWords * 4 + 256;
+
 enum Phase : int { kPhaseGram = 0, kPhaseGram2 = 1, kPhaseApply = 2 };
 enum FinalMode : int { kWriteX = 0, kUpdateW = 1, kWriteO = 2 };
 
@@ -124,5 +136,9 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 cudaError_t launch_update0(const Update0Args& a, int grid, cudaStream_t s);
 cudaError_t launch_gemm(int phase, const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t gemm_configure();
+// CTA-pair kernels: items are {matrix, 256-row tile, 256-col tile, K blocks};
+// `clusters` 2-CTA clusters are launched.
+cudaError_t launch_gemm_pair(int phase, const GemmArgs& a, int clusters, cudaStream_t s);
+cudaError_t gemm_pair_configure(int* max_clusters);
 
 }  // namespace dmuon

@@ -77,7 +77,7 @@ struct Layout {
   std::vector<int4> items[3];
 };
 
-void make_layout(const dmuon_shape_t* shapes, int n, Layout& L) {
+void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair) {
   L.mats.assign(n, MatDesc{});
   L.xoff.resize(n); L.aoff.resize(n); L.boff.resize(n);
   L.tile_prefix.assign(n + 1, 0);
@@ -100,13 +100,25 @@ void make_layout(const dmuon_shape_t* shapes, int n, Layout& L) {
     L.tile_prefix[i + 1] = L.tile_prefix[i] + cdiv(d.rows, kMomTile) * d.tiles_c;
   }
   L.ws_bytes = off;
-  // Work lists.  Symmetric phases: 256x256 super-tiles (I <= J), each as two
-  // 128-row halves; Apply: all 128x256 tiles of the m x n output.
+  // Work lists.  Symmetric phases: 256x256 super-tiles (I <= J); Apply: the
+  // m x n output.  CTA pairs take a whole 256x256 tile per item; single CTAs
+  // take one 128-row half of it.
   for (int p = 0; p < 3; ++p) L.items[p].clear();
   for (int i = 0; i < n; ++i) {
     const MatDesc& d = L.mats[i];
     const int64_t T = cdiv(d.m, 256);
     const int kg = (int)cdiv(d.n, kBK), km = (int)cdiv(d.m, kBK);
+    if (pair) {
+      for (int64_t I = 0; I < T; ++I)
+        for (int64_t J = I; J < T; ++J) {
+          L.items[kPhaseGram].push_back(make_int4(i, (int)I, (int)J, kg));
+          L.items[kPhaseGram2].push_back(make_int4(i, (int)I, (int)J, km));
+        }
+      for (int64_t tj = 0; tj < cdiv(d.n, kBN); ++tj)
+        for (int64_t I = 0; I < T; ++I)
+          L.items[kPhaseApply].push_back(make_int4(i, (int)I, (int)tj, km));
+      continue;
+    }
     for (int64_t I = 0; I < T; ++I)
       for (int64_t J = I; J < T; ++J)
         for (int h = 0; h < 2; ++h) {
@@ -155,7 +167,6 @@ struct dmuon_ctx {
   int* d_flags = nullptr;
   int* d_err = nullptr;
   int4* d_items[3] = {nullptr, nullptr, nullptr};
-  // pointer cache
   // pointer-set cache: kPtrSlots device slots of n MatPtrs each
   std::vector<MatPtrs> slot_ptrs[kPtrSlots];
   uint64_t slot_use[kPtrSlots] = {};
@@ -170,6 +181,9 @@ struct dmuon_ctx {
   std::vector<cudaEvent_t> ev_pool;
   std::string last_error;
   unsigned long long wait_timeout_ns = 0;  // 0: kernels' default (4 s)
+  int max_clusters = 0;                     // resident 2-CTA clusters (0: pairs unavailable)
+  int tile_mode = 0;                        // requested: 0 auto, 1 single CTA, 2 CTA pairs
+  bool plan_pair = false;                   // tile kind of the current plan
 };
 
 namespace {
@@ -203,8 +217,19 @@ void free_plan(dmuon_ctx* h) {
   h->h_stage = nullptr;
 }
 
+// CTA pairs unless single CTAs are requested, pairs are unavailable, or (in
+// automatic mode) every short side fits one 128-row tile, where a pair's
+// second CTA would only compute padding.
+bool use_pairs(const dmuon_ctx* h, const dmuon_shape_t* s, int n) {
+  if (h->max_clusters <= 0 || h->tile_mode == 1) return false;
+  if (h->tile_mode == 2) return true;
+  for (int i = 0; i < n; ++i)
+    if (std::min(s[i].rows, s[i].cols) > kBM) return true;
+  return false;
+}
+
 bool same_shapes(const dmuon_ctx* h, const dmuon_shape_t* s, int n) {
-  if ((int)h->shapes.size() != n || !h->small) return false;
+  if ((int)h->shapes.size() != n || !h->small || h->plan_pair != use_pairs(h, s, n)) return false;
   for (int i = 0; i < n; ++i)
     if (h->shapes[i].rows != s[i].rows || h->shapes[i].cols != s[i].cols) return false;
   return true;
@@ -215,7 +240,8 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
   free_plan(h);
   if (!get_encoder()) return fail(h, DMUON_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
   Layout& L = h->L;
-  make_layout(shapes, n, L);
+  h->plan_pair = use_pairs(h, shapes, n);
+  make_layout(shapes, n, L, h->plan_pair);
   cudaError_t e = cudaMalloc(&h->ws, std::max<size_t>(L.ws_bytes, 256));
   if (e != cudaSuccess) { h->ws = nullptr; cudaGetLastError(); return fail(h, DMUON_ERR_OOM, "workspace cudaMalloc", e); }
   e = cudaMalloc(&h->small, L.small_bytes);
@@ -405,10 +431,16 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
       a.svec = h->d_svec;
       a.err = h->d_err;
       a.timeout_ns = h->wait_timeout_ns;
-      const int grid = std::min(a.n_items, h->num_sms);
-      if (grid <= 0) continue;
+      if (a.n_items <= 0) continue;
       LaunchGuard g(h, stream, kKinds[p]);
-      if ((e = launch_gemm(p, a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "ns_gemm launch", e);
+      if (h->plan_pair) {
+        const int clusters = std::min(a.n_items, h->max_clusters);
+        if ((e = launch_gemm_pair(p, a, clusters, stream)) != cudaSuccess)
+          return fail(h, cuda_err(e), "ns_gemm_pair launch", e);
+      } else {
+        const int grid = std::min(a.n_items, h->num_sms);
+        if ((e = launch_gemm(p, a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "ns_gemm launch", e);
+      }
     }
   }
   return DMUON_OK;
@@ -446,9 +478,15 @@ int dmuon_create(dmuon_handle_t* out, int device) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (major != 10 || minor != 3) return DMUON_ERR_UNSUPPORTED;
   if (gemm_configure() != cudaSuccess) return DMUON_ERR_CUDA;
+  int clusters = 0;
+  if (gemm_pair_configure(&clusters) != cudaSuccess) {
+    cudaGetLastError();
+    clusters = 0;
+  }
   dmuon_ctx* h = new dmuon_ctx();
   h->device = device;
   h->num_sms = sms;
+  h->max_clusters = clusters;
   for (int k = 0; k < kPtrSlots; ++k) {
     if (cudaEventCreateWithFlags(&h->slot_ev[k], cudaEventDisableTiming) != cudaSuccess) {
       for (int j = 0; j < k; ++j) cudaEventDestroy(h->slot_ev[j]);
@@ -478,8 +516,10 @@ int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats, size_t* out_b
   if (n_mats == 0) return DMUON_OK;
   if (int rc = check_shapes(shapes, n_mats)) return rc;
   Layout L;
-  make_layout(shapes, n_mats, L);
-  *out_bytes = L.ws_bytes + L.small_bytes;
+  make_layout(shapes, n_mats, L, false);
+  size_t single = L.ws_bytes + L.small_bytes;
+  make_layout(shapes, n_mats, L, true);
+  *out_bytes = std::max(single, L.ws_bytes + L.small_bytes);
   return DMUON_OK;
 }
 
@@ -568,6 +608,13 @@ int dmuon_set_wait_timeout(dmuon_handle_t h, uint64_t ns) {
   return DMUON_OK;
 }
 
+int dmuon_set_tile_mode(dmuon_handle_t h, int mode) {
+  if (!h || mode < 0 || mode > 2) return DMUON_ERR_ARG;
+  if (mode == 2 && h->max_clusters <= 0) return DMUON_ERR_UNSUPPORTED;
+  h->tile_mode = mode;
+  return DMUON_OK;
+}
+
 int dmuon_profile_enable(dmuon_handle_t h, int on) {
   if (!h) return DMUON_ERR_ARG;
   h->profiling = on != 0;
@@ -594,7 +641,8 @@ int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len) {
   std::string s;
   char line[256];
   const int n = (int)h->shapes.size();
-  std::snprintf(line, sizeof line, "device %d, %d SMs; matrices %d; ", h->device, h->num_sms, n);
+  std::snprintf(line, sizeof line, "device %d, %d SMs, %d 2-CTA clusters; matrices %d; tiles %s; ", h->device,
+                h->num_sms, h->max_clusters, n, h->plan_pair ? "256x256 CTA pairs" : "128x256 single CTAs");
   s += line;
   if (h->small) {
     std::snprintf(line, sizeof line,

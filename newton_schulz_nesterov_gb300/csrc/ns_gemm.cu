@@ -409,6 +409,193 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair kernel (cta_group::2).  A 2-CTA cluster owns one 256x256 output
+// tile per work item: rank r holds rows [256*ti + 128*r, +128) of it in its
+// TMEM.  Per 64-wide K block each rank loads its 128 rows of A and a 128-row
+// half of B into its own shared memory; the transaction bytes of both ranks
+// complete on rank 0's `full` barrier, rank 0 issues M=256, N=256 MMAs that
+// read both ranks' shared memory, and its commits are multicast to both
+// ranks' `empty` (stage free) and `tfull` (accumulator ready) barriers.  Both
+// ranks' epilogue warps release an accumulator on rank 0's `tempty` barrier.
+// Six 32 KB stages per CTA keep 192 KB of operands in flight per SM.
+// ---------------------------------------------------------------------------
+struct PairSmem {
+  uint8_t* stages;     // kPairStages x (A half 16 KB | B half 16 KB), 1024-aligned
+  uint32_t* scratch;   // 4 warps x 32 x 17 words
+  uint64_t* bars;      // full[6], empty[6], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+};
+
+__device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
+  PairSmem s;
+  const uint32_t a = ptx::smem_addr(raw);
+  uint8_t* base = raw + ((1024u - (a & 1023u)) & 1023u);
+  s.stages = base;
+  uint8_t* after = base + kPairStages * kPairStageBytes + kPairGuardBytes;
+  s.scratch = reinterpret_cast<uint32_t*>(after);
+  s.bars = reinterpret_cast<uint64_t*>(after + 4 * kEpiWords * 4);
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + 2 * kPairStages + 5);
+  s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+  return s;
+}
+
+template <int PHASE, int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __grid_constant__ GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const PairSmem sm = carve_pair(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t tmo = a.timeout_ns ? a.timeout_ns : kTimeoutNs;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  uint64_t* full = sm.bars;
+  uint64_t* empty = sm.bars + kPairStages;
+  uint64_t* tfull = sm.bars + 2 * kPairStages;
+  uint64_t* tempty = sm.bars + 2 * kPairStages + 2;
+  uint64_t* drain = sm.bars + 2 * kPairStages + 4;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      ptx::mbar_init(ptx::smem_addr(full + s), 1);
+      ptx::mbar_init(ptx::smem_addr(empty + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_addr(tfull + i), 1);
+      ptx::mbar_init(ptx::smem_addr(tempty + i), 8);  // 4 epilogue warps x 2 ranks
+    }
+    ptx::mbar_init(ptx::smem_addr(drain), 1);
+    *sm.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {  // one warp of each rank allocates the pair's TMEM together
+    ptx::tmem_alloc_pair(ptx::smem_addr(sm.tmem_slot), kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both ranks' barriers exist before any remote signal
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      uint32_t it = 0;
+      bool ok = true;
+      for (int w = pair; ok && w < a.n_items; w += npairs) {
+        const int4 item = a.items[w];
+        const CUtensorMap* maps = a.tmaps + (size_t)item.x * kMapsPerMat;
+        const CUtensorMap* mapA;
+        const CUtensorMap* mapB;
+        if (PHASE == kPhaseGram) {
+          mapA = maps + a.src; mapB = maps + a.src;
+        } else if (PHASE == kPhaseGram2) {
+          mapA = maps + 2; mapB = maps + 2;
+        } else {
+          mapA = maps + 3; mapB = maps + a.src;
+        }
+        const int rowA = item.y * 256 + (int)rank * 128;
+        const int rowB = item.z * 256 + (int)rank * 128;
+        for (int kb = 0; kb < item.w; ++kb, ++it) {
+          const uint32_t s = it % kPairStages;
+          const uint32_t ph = (it / kPairStages) & 1u;
+          if (!wait_bar(ptx::smem_addr(empty + s), ph ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
+          const uint32_t fb_local = ptx::smem_addr(full + s);
+          const uint32_t fb = ptx::mapa_shared(fb_local, 0);
+          if (leader) ptx::mbar_expect_tx(fb_local, 2 * kPairStageBytes);
+          const uint32_t sa = ptx::smem_addr(sm.stages + s * kPairStageBytes);
+          const uint32_t sb = sa + kPairHalfBytes;
+          const int k0 = kb * kBK;
+          ptx::tma_load_2d_pair(sa, mapA, k0, rowA, fb);
+          ptx::tma_load_2d_pair(sa + kBoxBytes, mapA, k0, rowA + kBox, fb);
+          if (PHASE == kPhaseApply) {
+            ptx::tma_load_2d_pair(sb, mapB, rowB, k0, fb);
+            ptx::tma_load_2d_pair(sb + kBoxBytes, mapB, rowB + kBox, k0, fb);
+          } else {
+            ptx::tma_load_2d_pair(sb, mapB, k0, rowB, fb);
+            ptx::tma_load_2d_pair(sb + kBoxBytes, mapB, k0, rowB + kBox, fb);
+          }
+        }
+      }
+      if (leader && (!ok || *sm.abort_flag)) {
+        // Drain: the last issued stages' bytes (both ranks') must land before
+        // exit; bounded, ignoring the abort flag.
+        const uint32_t n_out = it < (uint32_t)kPairStages ? it : (uint32_t)kPairStages;
+        for (uint32_t i = it - n_out; i < it; ++i)
+          wait_slow(ptx::smem_addr(full + (i % kPairStages)), (i / kPairStages) & 1u, sm.abort_flag,
+                    a.err, false, kDrainTimeoutNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = ptx::idesc_bf16(256, kBN, PHASE == kPhaseApply ? 1 : 0);
+      uint32_t it = 0, tc = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int w = pair; ok && w < a.n_items; w += npairs, ++tc) {
+        const int4 item = a.items[w];
+        const uint32_t acc = tc & 1u;
+        if (!wait_bar(ptx::smem_addr(tempty + acc), ((tc >> 1) & 1u) ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t dt = tmem_base + acc * kBN;
+        for (int kb = 0; kb < item.w; ++kb, ++it) {
+          const uint32_t s = it % kPairStages;
+          const uint32_t ph = (it / kPairStages) & 1u;
+          if (!wait_bar(ptx::smem_addr(full + s), ph, sm.abort_flag, a.err, tmo)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_addr(sm.stages + s * kPairStageBytes);
+          const uint32_t sb = sa + kPairHalfBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = ptx::desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = (PHASE == kPhaseApply) ? ptx::desc_sw128(sb + kk * 2048, 8192, 1024)
+                                                       : ptx::desc_sw128(sb + kk * 32, 16, 1024);
+            ptx::mma_bf16_pair(dt, ad, bd, idesc, (kb | kk) != 0);
+          }
+          issued = true;
+          ptx::mma_commit_multicast(ptx::smem_addr(empty + s), 0x3);
+        }
+        if (!ok) break;
+        ptx::mma_commit_multicast(ptx::smem_addr(tfull + acc), 0x3);
+      }
+      if (issued && (!ok || *sm.abort_flag)) {
+        ptx::mma_commit_pair(ptx::smem_addr(drain));
+        wait_slow(ptx::smem_addr(drain), 0, sm.abort_flag, a.err, false, kDrainTimeoutNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 for this warp
+    uint32_t* scratch = sm.scratch + (warp - 2) * kEpiWords;
+    uint32_t tc = 0;
+    for (int w = pair; w < a.n_items; w += npairs, ++tc) {
+      int4 item = a.items[w];
+      const uint32_t acc = tc & 1u;
+      if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err, tmo)) break;
+      ptx::tc_fence_after();
+      item.y = item.y * 2 + (int)rank;  // this rank's 128-row tile
+      epilogue_tile<PHASE, MODE>(a, item, tmem_base + acc * kBN, quad, lane, scratch);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_addr(tempty + acc), 0));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // no rank frees TMEM or exits while its pair is busy
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 }  // namespace
 
 template <int PHASE, int MODE>
@@ -441,6 +628,59 @@ cudaError_t launch_gemm(int phase, const GemmArgs& a, int grid, cudaStream_t s) 
     ns_gemm_kernel<kPhaseApply, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
   }
   return cudaGetLastError();
+}
+
+template <int PHASE, int MODE>
+cudaError_t configure_pair_one(int* max_clusters) {
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<PHASE, MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  if (e != cudaSuccess || !max_clusters) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(max_clusters, ns_gemm_pair_kernel<PHASE, MODE>, &cfg);
+}
+
+cudaError_t gemm_pair_configure(int* max_clusters) {
+  cudaError_t e;
+  if ((e = configure_pair_one<kPhaseGram, kWriteX>(max_clusters)) != cudaSuccess) return e;
+  if ((e = configure_pair_one<kPhaseGram2, kWriteX>(nullptr)) != cudaSuccess) return e;
+  if ((e = configure_pair_one<kPhaseApply, kWriteX>(nullptr)) != cudaSuccess) return e;
+  if ((e = configure_pair_one<kPhaseApply, kUpdateW>(nullptr)) != cudaSuccess) return e;
+  return configure_pair_one<kPhaseApply, kWriteO>(nullptr);
+}
+
+template <int PHASE, int MODE>
+cudaError_t launch_pair_one(const GemmArgs& a, int clusters, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<PHASE, MODE>, a);
+}
+
+cudaError_t launch_gemm_pair(int phase, const GemmArgs& a, int clusters, cudaStream_t s) {
+  if (phase == kPhaseGram) return launch_pair_one<kPhaseGram, kWriteX>(a, clusters, s);
+  if (phase == kPhaseGram2) return launch_pair_one<kPhaseGram2, kWriteX>(a, clusters, s);
+  if (a.final_mode == kUpdateW) return launch_pair_one<kPhaseApply, kUpdateW>(a, clusters, s);
+  if (a.final_mode == kWriteO) return launch_pair_one<kPhaseApply, kWriteO>(a, clusters, s);
+  return launch_pair_one<kPhaseApply, kWriteX>(a, clusters, s);
 }
 
 }  // namespace dmuon

@@ -121,6 +121,28 @@ def test_newton_schulz_ragged_shapes(handle):
         assert e <= NS_TOL, (s, e)
 
 
+@pytest.mark.parametrize("mode", [1, 2])
+def test_tile_modes_match_oracle(handle, mode):
+    """Single-CTA 128x256 tiles (mode 1) and CTA-pair 256x256 tiles (mode 2)
+    both meet the bar on ragged shapes and a full step."""
+    gen = torch.Generator().manual_seed(23)
+    ins = [torch.randn(s, generator=gen) for s in RAGGED]
+    outs = [torch.empty(s, device="cuda") for s in RAGGED]
+    with dm.Handle(0) as h2:
+        dm.dmuon_set_tile_mode(h2.h, mode)
+        h2.newton_schulz(_to_dev(ins), outs)
+        assert h2.status()[0] == 0
+        assert (("pairs" in dm.dmuon_plan_summary(h2.h)) == (mode == 2))
+        for x, o, s in zip(ins, outs, RAGGED):
+            e = rel_fro(o.cpu().numpy(), oracle.newton_schulz(x.numpy()))
+            assert e <= NS_TOL, (mode, s, e)
+        shapes = [(512, 128), (128, 512), (300, 1000), (1000, 300)]
+        Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
+        Gs = [torch.randn(s, generator=gen) for s in shapes]
+        Ms = [torch.randn(s, generator=gen) for s in shapes]
+        _step_and_check(h2, Ws, Gs, Ms)
+
+
 def test_newton_schulz_scaled_inputs(handle):
     """The normalisation is folded into the first iteration: tiny and huge
     input scales give the same O."""
