@@ -69,6 +69,27 @@ def tensor_peak():
     return FALLBACK_BF16_TFLOPS_SUSTAINED, "of fallback (sustained bf16, 1.7 PFLOP/s)"
 
 
+def apply_traffic(workload):
+    """DRAM bytes per Apply launch from the committed ncu summary, scaled by
+    layers processed; None unless the kernel sources are the ones captured."""
+    import hashlib
+    import re
+    layers = {"llama3_8b": 32, "llama3_8b_1layer": 1}.get(workload)
+    path = os.path.join(ROOT, "profiles", "ns_gemm_pair_llama3_8b_1layer.md")
+    if layers is None or not os.path.exists(path):
+        return None
+    text = open(path).read()
+    sha = re.search(r"source_sha1:\s*([0-9a-f]{40})", text)
+    per = re.search(r"dram_bytes_per_layer:\s*(\d+)", text)
+    if not sha or not per:
+        return None
+    csrc = os.path.join(ROOT, "newton_schulz_nesterov_gb300", "csrc")
+    src = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("ns_gemm.cu", "common.cuh", "ptx.cuh"))
+    if hashlib.sha1(src).hexdigest() != sha.group(1):
+        return None
+    return int(per.group(1)) * layers
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi sampled every 200 ms during the timed region."""
@@ -292,22 +313,32 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- dominant kernel roofline (B*X apply phase; tensor-bound)
     peak, peak_src = tensor_peak()
+    # Each phase launches once per chunk and iteration; achieved rates divide
+    # the phase's algorithmic work over the timed steps by its summed time.
     apply_ms, apply_n = prof["apply"]
     roofline = None
     if apply_n:
-        per_launch_flops = flops.apply_flops(shapes, 1)
-        achieved = per_launch_flops / (apply_ms / apply_n / 1e3) / 1e12
-        roofline = {"kernel": "ns_gemm_kernel<Apply> (B*X + a*X)", "bound": "tensor",
+        achieved = flops.apply_flops(shapes, 5) * args.steps / (apply_ms / 1e3) / 1e12
+        launches_per_step = apply_n / args.steps
+        kname = ("ns_gemm_pair_kernel<Apply> (B*X + a*X, 256x256 CTA-pair tiles)"
+                 if "pairs" in dm.dmuon_plan_summary(h.h) else
+                 "ns_gemm_kernel<Apply> (B*X + a*X, 128x256 tiles)")
+        step_traffic = apply_traffic(args.workload)  # DRAM bytes of one iteration's Apply over all matrices
+        roofline = {"kernel": kname, "bound": "tensor",
                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "peak_source": peak_src, "traffic": None}
-    phase = {k: {"ms_per_launch": (v[0] / v[1]) if v[1] else None, "launches": v[1]}
+                    "frac": achieved / peak, "peak_source": peak_src,
+                    "traffic": (step_traffic * 5 / launches_per_step) if step_traffic else None,
+                    "launches_per_step": launches_per_step,
+                    "avg_launch_ms": apply_ms / apply_n}
+    phase = {k: {"ms_per_launch": (v[0] / v[1]) if v[1] else None, "launches": v[1],
+                 "ms_per_step": v[0] / args.steps}
              for k, v in prof.items() if v[1]}
-    mom_ms = prof["momentum"][0] / max(1, prof["momentum"][1])
+    mom_ms_step = prof["momentum"][0] / args.steps
     hbm_peak = FALLBACK_HBM_GBS
     pk, _ = measured_peaks()
     if pk and pk.get("hbm_gbs"):
         hbm_peak = float(pk["hbm_gbs"])
-    phase["momentum"]["achieved_gbs"] = flops.elementwise_bytes(shapes) / (mom_ms / 1e3) / 1e9
+    phase["momentum"]["achieved_gbs"] = flops.elementwise_bytes(shapes) / (mom_ms_step / 1e3) / 1e9
     phase["momentum"]["frac_of_hbm"] = phase["momentum"]["achieved_gbs"] / hbm_peak
 
     # ---- end to end through the public API with host buffers

@@ -95,8 +95,9 @@ int dmuon_create(dmuon_handle_t* out, int device);
  * NULL is a no-op. */
 void dmuon_destroy(dmuon_handle_t h);
 
-/* Bytes of device workspace a step over `shapes` needs (bf16 X ping/pong,
- * A and B per matrix, plus small per-matrix arrays).  Host only. */
+/* Bytes of device memory a step over `shapes` allocates with the default
+ * chunking (bf16 X ping/pong, A and B for the largest chunk, plus small
+ * per-matrix arrays), for either tiling.  Host only. */
 int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats,
                           size_t* out_bytes);
 
@@ -200,6 +201,14 @@ int dmuon_set_wait_timeout(dmuon_handle_t h, uint64_t ns);
  * result is the same maths with the same roundings; the choice only changes
  * speed.  DMUON_ERR_UNSUPPORTED if pairs are requested but unavailable. */
 int dmuon_set_tile_mode(dmuon_handle_t h, int mode);
+
+/* Chunking of later plans: the matrix list is cut into contiguous chunks of
+ * at most `elems` matrix elements (a larger matrix is a chunk of its own);
+ * each chunk runs its whole launch sequence before the next starts, and all
+ * chunks share one workspace sized for the largest.  0 selects the default
+ * (2^29 elements); a value above the list's total gives one chunk.  The
+ * result does not depend on the chunking. */
+int dmuon_set_chunk_elements(dmuon_handle_t h, int64_t elems);
 
 /* Kernel launches issued by this handle since creation (a counter). */
 int64_t dmuon_launch_count(dmuon_handle_t h);

@@ -89,6 +89,8 @@ def load(path=None):
     L.dmuon_get_status.restype = i32
     L.dmuon_last_error.argtypes = [vp]
     L.dmuon_last_error.restype = ctypes.c_char_p
+    L.dmuon_set_chunk_elements.argtypes = [vp, i64]
+    L.dmuon_set_chunk_elements.restype = i32
     L.dmuon_set_tile_mode.argtypes = [vp, i32]
     L.dmuon_set_tile_mode.restype = i32
     L.dmuon_set_wait_timeout.argtypes = [vp, ctypes.c_uint64]
@@ -254,6 +256,11 @@ def dmuon_get_status(h, n_flags=0):
     flags = (ctypes.c_int * max(1, n_flags))()
     rc = load().dmuon_get_status(h, flags, int(n_flags))
     return rc, [flags[i] for i in range(n_flags)]
+
+
+def dmuon_set_chunk_elements(h, elems):
+    """Chunk size of later plans in matrix elements (0 = default 2^29)."""
+    _check(load().dmuon_set_chunk_elements(h, int(elems)), "dmuon_set_chunk_elements")
 
 
 def dmuon_set_tile_mode(h, mode):
