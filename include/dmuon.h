@@ -139,6 +139,42 @@ int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs,
                         float eps, void* stream);
 
 /*
+ * AdamW on a list of flat fp32 tensors, in place (the non-Muon half of
+ * Muon.step: DMuon "API Reference", section "Muon", defaults adamw_lr 1e-3,
+ * adamw_betas (0.9, 0.999), adamw_weight_decay 0.01, adamw_eps 1e-8).
+ * Decoupled decay and bias correction, as PyTorch's AdamW:
+ *   p *= 1 - lr*wd;  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+ *   p -= lr/(1-b1^step) * m / (sqrt(v)/sqrt(1-b2^step) + eps)
+ * params, grads, exp_avg, exp_avg_sq: host arrays of n device pointers to
+ * numels[i] fp32 elements (4-byte aligned; 16-byte aligned with numel % 4 ==
+ * 0 takes the vector path), pairwise distinct.  step >= 1 is the step count
+ * after this update; 0 <= beta < 1.  Asynchronous on `stream`.
+ */
+int dmuon_adamw_step(dmuon_handle_t h, float* const* params,
+                     const float* const* grads, float* const* exp_avg,
+                     float* const* exp_avg_sq, const int64_t* numels, int n,
+                     float lr, float beta1, float beta2, float eps,
+                     float weight_decay, int step, void* stream);
+
+/*
+ * Segmented gradient-norm clipping (DMuon "API Reference", sections
+ * "clip_grad_norm_" and "clip_grad_norm_buckets_"): for every bucket b,
+ * norm_b = ||concatenation of its gradients||_2 (fixed-order fp64 sum of
+ * fixed-order fp32 tile sums), coef_b = max_norm / (norm_b + 1e-6), and its
+ * gradients are scaled by coef_b in place when coef_b < 1.
+ *   grads[i]  device fp32, numels[i] elements, 4-byte aligned
+ *   buckets   host, n bucket indices in [0, n_buckets); NULL = one bucket
+ *   max_norm  <= 0: statistics only (no scaling; coef reported as -1)
+ *   norms_out, coefs_out  host, n_buckets floats each, or NULL.  When either
+ *             is given the call waits for the stream and fills them; a
+ *             non-finite norm reports an Inf/NaN gradient (found_inf).
+ */
+int dmuon_clip_grad_norm(dmuon_handle_t h, float* const* grads,
+                         const int64_t* numels, int n, const int* buckets,
+                         int n_buckets, float max_norm, float* norms_out,
+                         float* coefs_out, void* stream);
+
+/*
  * Allocation-free standalone Newton-Schulz of ONE matrix.  The pages have no
  * counterpart of this entry point; it exists for callers that may not call
  * cudaMalloc (a host framework whose allocator owns all device memory, a
@@ -220,7 +256,8 @@ int64_t dmuon_launch_count(dmuon_handle_t h);
  * its stream.  dmuon_profile_read() synchronises, then adds the elapsed
  * milliseconds and launch counts per kernel kind into ms[k] and count[k]
  * for k < n_kinds (kinds: 0 momentum+norm, 1 norm finalise, 2 Gram X X^T,
- * 3 A*A, 4 B*X (+update), 5 update without NS) and resets the record.
+ * 3 A*A, 4 B*X (+update), 5 update without NS, 6 AdamW, 7 clipping, the
+ * last bracketing its whole launch sequence) and resets the record.
  */
 #define DMUON_KIND_MOMENTUM 0
 #define DMUON_KIND_FINALIZE 1
@@ -228,7 +265,9 @@ int64_t dmuon_launch_count(dmuon_handle_t h);
 #define DMUON_KIND_GRAM2    3
 #define DMUON_KIND_APPLY    4
 #define DMUON_KIND_UPDATE0  5
-#define DMUON_NUM_KINDS     6
+#define DMUON_KIND_ADAMW    6
+#define DMUON_KIND_CLIP     7
+#define DMUON_NUM_KINDS     8
 int dmuon_profile_enable(dmuon_handle_t h, int on);
 int dmuon_profile_read(dmuon_handle_t h, double* ms, int64_t* count,
                        int n_kinds);

@@ -16,6 +16,7 @@ __all__ = [
     "DmuonError", "load", "lib_path", "dmuon_create", "dmuon_destroy",
     "dmuon_step", "dmuon_step_ptrs", "dmuon_newton_schulz",
     "dmuon_newton_schulz_ptrs", "dmuon_newton_schulz_noalloc", "dmuon_get_status",
+    "dmuon_adamw_step", "dmuon_adamw_step_ptrs", "dmuon_clip_grad_norm", "dmuon_clip_grad_norm_ptrs",
     "dmuon_workspace_bytes",
     "dmuon_launch_count", "dmuon_last_error", "dmuon_profile_enable", "dmuon_profile_read",
     "dmuon_plan_summary", "dmuon_error_string", "dmuon_version", "Handle",
@@ -31,7 +32,7 @@ STATUS = {
     -4: "DMUON_ERR_CUDA", -5: "DMUON_ERR_NONFINITE", -6: "DMUON_ERR_TIMEOUT",
     -7: "DMUON_ERR_UNSUPPORTED",
 }
-KIND_NAMES = ("momentum", "finalize", "gram", "gram2", "apply", "update0")
+KIND_NAMES = ("momentum", "finalize", "gram", "gram2", "apply", "update0", "adamw", "clip")
 
 
 class DmuonError(RuntimeError):
@@ -85,6 +86,12 @@ def load(path=None):
     L.dmuon_newton_schulz_noalloc.argtypes = [vp, vp, i64, i64, i32, ctypes.POINTER(ctypes.c_float),
                                               f32, i32, vp]
     L.dmuon_newton_schulz_noalloc.restype = i32
+    L.dmuon_adamw_step.argtypes = [vp, pp, pp, pp, pp, ctypes.POINTER(i64), i32, f32, f32, f32, f32,
+                                   f32, i32, vp]
+    L.dmuon_adamw_step.restype = i32
+    L.dmuon_clip_grad_norm.argtypes = [vp, pp, ctypes.POINTER(i64), i32, ctypes.POINTER(ctypes.c_int), i32,
+                                       f32, ctypes.POINTER(f32), ctypes.POINTER(f32), vp]
+    L.dmuon_clip_grad_norm.restype = i32
     L.dmuon_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), i32]
     L.dmuon_get_status.restype = i32
     L.dmuon_last_error.argtypes = [vp]
@@ -249,6 +256,65 @@ def dmuon_newton_schulz_noalloc(input_ptr, output_ptr, rows, cols, ns_steps=5, c
         ctypes.c_void_p(int(input_ptr)), ctypes.c_void_p(int(output_ptr)), int(rows), int(cols),
         int(ns_steps), None if carr is None else ctypes.cast(carr, ctypes.POINTER(ctypes.c_float)),
         float(eps), 1 if sync_status else 0, ctypes.c_void_p(_stream_handle(stream)))
+
+
+def _flat_args(tensors, name):
+    ptrs, numels = [], []
+    for t in tensors:
+        if not t.is_cuda or not t.is_contiguous() or str(t.dtype) != "torch.float32":
+            raise ValueError("%s: each tensor must be a contiguous float32 CUDA tensor" % name)
+        ptrs.append(t.data_ptr())
+        numels.append(t.numel())
+    return ptrs, numels
+
+
+def dmuon_adamw_step_ptrs(h, p_ptrs, g_ptrs, m_ptrs, v_ptrs, numels, lr=1e-3, beta1=0.9,
+                          beta2=0.999, eps=1e-8, weight_decay=0.01, step=1, stream=None, check=True):
+    n = len(numels)
+    nums = (ctypes.c_int64 * max(1, n))(*[int(x) for x in numels])
+    rc = load().dmuon_adamw_step(h, _ptr_array(p_ptrs), _ptr_array(g_ptrs), _ptr_array(m_ptrs),
+                                 _ptr_array(v_ptrs), nums, n, float(lr), float(beta1), float(beta2),
+                                 float(eps), float(weight_decay), int(step),
+                                 ctypes.c_void_p(_stream_handle(stream)))
+    if check:
+        _check(rc, "dmuon_adamw_step", h)
+    return rc
+
+
+def dmuon_adamw_step(h, params, grads, exp_avg, exp_avg_sq, **kw):
+    """AdamW over lists of contiguous fp32 CUDA tensors (updated in place)."""
+    pp_, nums = _flat_args(params, "params")
+    gp, gn = _flat_args(grads, "grads")
+    mp, mn = _flat_args(exp_avg, "exp_avg")
+    vp_, vn = _flat_args(exp_avg_sq, "exp_avg_sq")
+    if not (nums == gn == mn == vn):
+        raise ValueError("params, grads, exp_avg, exp_avg_sq must have matching sizes")
+    return dmuon_adamw_step_ptrs(h, pp_, gp, mp, vp_, nums, **kw)
+
+
+def dmuon_clip_grad_norm_ptrs(h, g_ptrs, numels, max_norm, buckets=None, n_buckets=None,
+                              stats=True, stream=None, check=True):
+    """Returns (status, norms, coefs); norms/coefs are None when stats=False."""
+    n = len(numels)
+    nb = 1 if buckets is None else int(n_buckets if n_buckets is not None else max(buckets) + 1)
+    nums = (ctypes.c_int64 * max(1, n))(*[int(x) for x in numels])
+    bk = None if buckets is None else (ctypes.c_int * max(1, n))(*[int(b) for b in buckets])
+    norms = (ctypes.c_float * nb)() if stats else None
+    coefs = (ctypes.c_float * nb)() if stats else None
+    rc = load().dmuon_clip_grad_norm(h, _ptr_array(g_ptrs), nums, n, bk, nb, float(max_norm),
+                                     norms, coefs, ctypes.c_void_p(_stream_handle(stream)))
+    if check:
+        _check(rc, "dmuon_clip_grad_norm", h)
+    if not stats:
+        return rc, None, None
+    return rc, [norms[i] for i in range(nb)], [coefs[i] for i in range(nb)]
+
+
+def dmuon_clip_grad_norm(h, grads, max_norm, buckets=None, n_buckets=None, stats=True, stream=None):
+    """Segmented clipping of CUDA fp32 gradients in place; returns (norms, coefs)."""
+    gp, nums = _flat_args(grads, "grads")
+    _, norms, coefs = dmuon_clip_grad_norm_ptrs(h, gp, nums, max_norm, buckets, n_buckets, stats, stream)
+    return norms, coefs
 
 
 def dmuon_get_status(h, n_flags=0):

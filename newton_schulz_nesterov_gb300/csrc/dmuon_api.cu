@@ -18,6 +18,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/dmuon.h"
+#include "aux.cuh"
 #include "common.cuh"
 
 using namespace dmuon;
@@ -195,6 +196,13 @@ struct dmuon_ctx {
   int64_t chunk_elems = 0;                  // requested chunk size (0: default)
   bool plan_pair = false;                   // tile kind of the current plan
   int64_t plan_chunk_elems = 0;             // chunk size of the current plan
+  // AdamW / clipping: descriptor buffer (device), pinned staging, results
+  void* aux_dev = nullptr;
+  size_t aux_dev_cap = 0;
+  uint8_t* aux_host = nullptr;
+  size_t aux_host_cap = 0;
+  cudaEvent_t aux_ev = nullptr;
+  bool aux_pending = false;
 };
 
 namespace {
@@ -415,6 +423,91 @@ int check_shapes(const dmuon_shape_t* shapes, int n) {
   return DMUON_OK;
 }
 
+// Device buffer for a flat call: host part (descriptors, prefix, bucket
+// lists) staged through pinned memory; `dev_extra` bytes of device-only
+// scratch follow.  Returns the device base (nullptr on failure).
+uint8_t* aux_buffers(dmuon_ctx* h, const std::vector<uint8_t>& host_part, size_t dev_extra,
+                     cudaStream_t stream, int* rc) {
+  const size_t need = rup((int64_t)host_part.size(), 256) + dev_extra;
+  cudaError_t e;
+  if (h->aux_dev_cap < need) {
+    if (h->aux_dev) {
+      e = cudaStreamSynchronize(stream);  // earlier work may still read it
+      cudaFree(h->aux_dev);
+    }
+    h->aux_dev = nullptr;
+    h->aux_dev_cap = 0;
+    if ((e = cudaMalloc(&h->aux_dev, need)) != cudaSuccess) {
+      h->aux_dev = nullptr;
+      cudaGetLastError();
+      *rc = fail(h, DMUON_ERR_OOM, "aux cudaMalloc", e);
+      return nullptr;
+    }
+    h->aux_dev_cap = need;
+  }
+  if (h->aux_pending) { cudaEventSynchronize(h->aux_ev); h->aux_pending = false; }
+  if (h->aux_host_cap < host_part.size()) {
+    if (h->aux_host) cudaFreeHost(h->aux_host);
+    h->aux_host = nullptr;
+    h->aux_host_cap = 0;
+    if (cudaMallocHost(&h->aux_host, host_part.size()) != cudaSuccess) {
+      *rc = fail(h, DMUON_ERR_OOM, "aux pinned staging");
+      return nullptr;
+    }
+    h->aux_host_cap = host_part.size();
+  }
+  std::memcpy(h->aux_host, host_part.data(), host_part.size());
+  e = cudaMemcpyAsync(h->aux_dev, h->aux_host, host_part.size(), cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaEventRecord(h->aux_ev, stream);
+  if (e != cudaSuccess) {
+    *rc = fail(h, cuda_err(e), "aux upload", e);
+    return nullptr;
+  }
+  h->aux_pending = true;
+  *rc = DMUON_OK;
+  return (uint8_t*)h->aux_dev;
+}
+
+// Flat descriptors + tile prefix for a tensor list.
+struct FlatPlan {
+  std::vector<uint8_t> host;
+  size_t off_prefix = 0, off_bstart = 0, off_members = 0;
+  int64_t n_tiles = 0;
+};
+
+void flat_plan(FlatPlan& fp, const std::vector<FlatDesc>& descs, const std::vector<int>* buckets,
+               int n_buckets) {
+  const int n = (int)descs.size();
+  std::vector<int64_t> prefix(n + 1, 0);
+  for (int i = 0; i < n; ++i) prefix[i + 1] = prefix[i] + cdiv(descs[i].numel, kFlatTile);
+  fp.n_tiles = prefix[n];
+  size_t off = rup(sizeof(FlatDesc) * n, 256);
+  fp.off_prefix = off;
+  off += rup(8 * (n + 1), 256);
+  std::vector<int> bstart, members;
+  if (buckets) {
+    bstart.assign(n_buckets + 1, 0);
+    for (int i = 0; i < n; ++i) ++bstart[(*buckets)[i] + 1];
+    for (int b = 0; b < n_buckets; ++b) bstart[b + 1] += bstart[b];
+    members.resize(n);
+    std::vector<int> fill(bstart.begin(), bstart.end() - 1);
+    for (int i = 0; i < n; ++i) members[fill[(*buckets)[i]]++] = i;
+    fp.off_bstart = off;
+    off += rup(4 * (n_buckets + 1), 256);
+    fp.off_members = off;
+    off += rup(4 * n, 256);
+  }
+  fp.host.assign(off, 0);
+  std::memcpy(fp.host.data(), descs.data(), sizeof(FlatDesc) * n);
+  std::memcpy(fp.host.data() + fp.off_prefix, prefix.data(), 8 * (n + 1));
+  if (buckets) {
+    std::memcpy(fp.host.data() + fp.off_bstart, bstart.data(), 4 * (n_buckets + 1));
+    std::memcpy(fp.host.data() + fp.off_members, members.data(), 4 * n);
+  }
+}
+
+bool is_vec4(const void* p, int64_t numel) { return (((uintptr_t)p & 15u) == 0) && (numel % 4 == 0); }
+
 // The launch sequence of one chunk: momentum/normalise, norm, then
 // ns_steps x (Gram, Gram2, Apply), the last Apply writing W (or O).
 int run_chunk(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, float mu, int ns_steps,
@@ -585,6 +678,11 @@ int dmuon_create(dmuon_handle_t* out, int device) {
       return DMUON_ERR_CUDA;
     }
   }
+  if (cudaEventCreateWithFlags(&h->aux_ev, cudaEventDisableTiming) != cudaSuccess) {
+    for (int k = 0; k < kPtrSlots; ++k) cudaEventDestroy(h->slot_ev[k]);
+    delete h;
+    return DMUON_ERR_CUDA;
+  }
   *out = h;
   return DMUON_OK;
 }
@@ -596,6 +694,9 @@ void dmuon_destroy(dmuon_handle_t h) {
   free_plan(h);
   for (int k = 0; k < kPtrSlots; ++k)
     if (h->slot_ev[k]) cudaEventDestroy(h->slot_ev[k]);
+  if (h->aux_ev) cudaEventDestroy(h->aux_ev);
+  if (h->aux_dev) cudaFree(h->aux_dev);
+  if (h->aux_host) cudaFreeHost(h->aux_host);
   for (auto& r : h->prof) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
   for (auto e : h->ev_pool) cudaEventDestroy(e);
   delete h;
@@ -661,6 +762,128 @@ int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs, float* con
   }
   return run(h, ptrs.data(), shapes, n_mats, 0.f, 0.f, ns_steps, coeffs, eps, 0.f, 0, 1, 1,
              (cudaStream_t)stream);
+}
+
+int dmuon_adamw_step(dmuon_handle_t h, float* const* params, const float* const* grads,
+                     float* const* exp_avg, float* const* exp_avg_sq, const int64_t* numels, int n,
+                     float lr, float beta1, float beta2, float eps, float weight_decay, int step,
+                     void* stream_) {
+  if (!h || n < 0) return DMUON_ERR_ARG;
+  if (n == 0) return DMUON_OK;
+  if (!params || !grads || !exp_avg || !exp_avg_sq || !numels) return DMUON_ERR_ARG;
+  if (step < 1 || !std::isfinite(lr) || !std::isfinite(beta1) || !std::isfinite(beta2) ||
+      !std::isfinite(eps) || !std::isfinite(weight_decay) || beta1 < 0.f || beta1 >= 1.f ||
+      beta2 < 0.f || beta2 >= 1.f)
+    return DMUON_ERR_ARG;
+  std::vector<FlatDesc> descs(n);
+  for (int i = 0; i < n; ++i) {
+    const void* ps[4] = {params[i], grads[i], exp_avg[i], exp_avg_sq[i]};
+    if (numels[i] <= 0) return DMUON_ERR_ARG;
+    for (int k = 0; k < 4; ++k) {
+      if (!ps[k]) return DMUON_ERR_ARG;
+      if ((uintptr_t)ps[k] & 3u) return DMUON_ERR_ALIGN;
+      for (int j = 0; j < k; ++j)
+        if (ps[j] == ps[k]) return DMUON_ERR_ARG;
+    }
+    bool v4 = true;
+    for (int k = 0; k < 4; ++k) v4 = v4 && is_vec4(ps[k], numels[i]);
+    descs[i] = FlatDesc{params[i], grads[i], exp_avg[i], exp_avg_sq[i], numels[i], 0, v4 ? 1 : 0};
+  }
+  if (cudaSetDevice(h->device) != cudaSuccess) return fail(h, DMUON_ERR_CUDA, "cudaSetDevice");
+  cudaStream_t stream = (cudaStream_t)stream_;
+  FlatPlan fp;
+  flat_plan(fp, descs, nullptr, 0);
+  int rc;
+  uint8_t* base = aux_buffers(h, fp.host, 0, stream, &rc);
+  if (!base) return rc;
+  AdamWArgs a{};
+  a.descs = (const FlatDesc*)base;
+  a.tile_prefix = (const int64_t*)(base + fp.off_prefix);
+  a.n = n;
+  a.n_tiles = fp.n_tiles;
+  a.decay = 1.f - lr * weight_decay;
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.step_size = (float)((double)lr / (1.0 - std::pow((double)beta1, step)));
+  a.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(1.0 - std::pow((double)beta2, step)));
+  a.eps = eps;
+  const int grid = (int)std::min<int64_t>(fp.n_tiles, (int64_t)h->num_sms * 8);
+  LaunchGuard g(h, stream, DMUON_KIND_ADAMW);
+  cudaError_t e = launch_adamw(a, grid, stream);
+  if (e != cudaSuccess) return fail(h, cuda_err(e), "adamw launch", e);
+  h->last_stream = stream;
+  return DMUON_OK;
+}
+
+int dmuon_clip_grad_norm(dmuon_handle_t h, float* const* grads, const int64_t* numels, int n,
+                         const int* buckets, int n_buckets, float max_norm, float* norms_out,
+                         float* coefs_out, void* stream_) {
+  if (!h || n < 0) return DMUON_ERR_ARG;
+  if (!buckets) n_buckets = 1;
+  if (n_buckets < 1 || !std::isfinite(max_norm)) return DMUON_ERR_ARG;
+  if (n == 0) {
+    for (int b = 0; b < n_buckets; ++b) {
+      if (norms_out) norms_out[b] = 0.f;
+      if (coefs_out) coefs_out[b] = max_norm > 0.f ? (float)(max_norm / 1e-6) : -1.f;
+    }
+    return DMUON_OK;
+  }
+  if (!grads || !numels) return DMUON_ERR_ARG;
+  std::vector<FlatDesc> descs(n);
+  std::vector<int> bk(n, 0);
+  for (int i = 0; i < n; ++i) {
+    if (!grads[i] || numels[i] <= 0) return DMUON_ERR_ARG;
+    if ((uintptr_t)grads[i] & 3u) return DMUON_ERR_ALIGN;
+    if (buckets) {
+      if (buckets[i] < 0 || buckets[i] >= n_buckets) return DMUON_ERR_ARG;
+      bk[i] = buckets[i];
+    }
+    descs[i] = FlatDesc{nullptr, grads[i], nullptr, nullptr, numels[i], bk[i],
+                        is_vec4(grads[i], numels[i]) ? 1 : 0};
+  }
+  if (cudaSetDevice(h->device) != cudaSuccess) return fail(h, DMUON_ERR_CUDA, "cudaSetDevice");
+  cudaStream_t stream = (cudaStream_t)stream_;
+  FlatPlan fp;
+  flat_plan(fp, descs, &bk, n_buckets);
+  const size_t off_part = rup((int64_t)fp.host.size(), 256);
+  const size_t off_norms = off_part + rup(4 * fp.n_tiles, 256);
+  const size_t off_coefs = off_norms + rup(4 * n_buckets, 256);
+  const size_t extra = off_coefs + rup(4 * n_buckets, 256) - off_part;
+  int rc;
+  uint8_t* base = aux_buffers(h, fp.host, extra, stream, &rc);
+  if (!base) return rc;
+  ClipArgs a{};
+  a.descs = (const FlatDesc*)base;
+  a.tile_prefix = (const int64_t*)(base + fp.off_prefix);
+  a.n = n;
+  a.n_tiles = fp.n_tiles;
+  a.bucket_start = (const int*)(base + fp.off_bstart);
+  a.bucket_members = (const int*)(base + fp.off_members);
+  a.n_buckets = n_buckets;
+  a.max_norm = max_norm;
+  a.partials = (float*)(base + off_part);
+  a.norms = (float*)(base + off_norms);
+  a.coefs = (float*)(base + off_coefs);
+  const int grid = (int)std::min<int64_t>(fp.n_tiles, (int64_t)h->num_sms * 8);
+  cudaError_t e;
+  {
+    LaunchGuard g(h, stream, DMUON_KIND_CLIP);
+    h->launches += max_norm > 0.f ? 2 : 1;  // sum of squares, finalise, (scale)
+    if ((e = launch_clip(a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "clip launch", e);
+  }
+  h->last_stream = stream;
+  if (norms_out || coefs_out) {
+    std::vector<float> nb(n_buckets), cb(n_buckets);
+    e = cudaMemcpyAsync(nb.data(), a.norms, 4 * n_buckets, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(cb.data(), a.coefs, 4 * n_buckets, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(h, cuda_err(e), "clip readback", e);
+    for (int b = 0; b < n_buckets; ++b) {
+      if (norms_out) norms_out[b] = nb[b];
+      if (coefs_out) coefs_out[b] = cb[b];
+    }
+  }
+  return DMUON_OK;
 }
 
 int dmuon_get_status(dmuon_handle_t h, int* flags, int n_flags) {
