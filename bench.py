@@ -46,6 +46,7 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-aux", action="store_true")
     return p.parse_args()
 
 
@@ -341,6 +342,11 @@ def run_ours(args, rank, world, local_rank):
     phase["momentum"]["achieved_gbs"] = flops.elementwise_bytes(shapes) / (mom_ms_step / 1e3) / 1e9
     phase["momentum"]["frac_of_hbm"] = phase["momentum"]["achieved_gbs"] / hbm_peak
 
+    # ---- the rest of Muon.step: AdamW and clipping rooflines (HBM-bound)
+    aux = None
+    if args.workload == "llama3_8b" and not args.no_aux:
+        aux = run_aux(args, h, Gs, stream, hbm_peak)
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
@@ -362,6 +368,7 @@ def run_ours(args, rank, world, local_rank):
         "phases": phase,
         "clocks": clk,
         "e2e": e2e,
+        "aux": aux,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         idx, desc = oracle_sample(args.workload)
@@ -372,6 +379,60 @@ def run_ours(args, rank, world, local_rank):
     h.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_aux(args, h, Gs, stream, hbm_peak):
+    """AdamW over the Llama-3-8B non-Muon parameters (embeddings, LM head,
+    RMSNorm weights: 1.05 G elements, 28 B each per step) and segmented
+    clipping of the 224 Muon gradients (one bucket per layer; sum of squares
+    4 B/element + scaling 8 B/element), timed with the library's per-launch
+    CUDA events."""
+    import torch
+    import newton_schulz_nesterov_gb300 as dm
+    dev = Gs[0].device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    shapes = [(128256, 4096), (128256, 4096)] + [(4096,)] * 65
+    P = [torch.randn(s, device=dev, generator=gen) * 0.02 for s in shapes]
+    G = [torch.randn(s, device=dev, generator=gen) * 1e-3 for s in shapes]
+    M = [torch.zeros(s, device=dev) for s in shapes]
+    V = [torch.zeros(s, device=dev) for s in shapes]
+    n_el = sum(p.numel() for p in P)
+    steps = args.steps
+    for t in range(1, 4):
+        dm.dmuon_adamw_step(h.h, P, G, M, V, step=t, stream=stream)
+    dm.dmuon_profile_read(h.h)
+    dm.dmuon_profile_enable(h.h, True)
+    for t in range(4, 4 + steps):
+        dm.dmuon_adamw_step(h.h, P, G, M, V, step=t, stream=stream)
+    torch.cuda.synchronize()
+    prof = dm.dmuon_profile_read(h.h)
+    adamw_ms = prof["adamw"][0] / max(1, prof["adamw"][1])
+    del P, G, M, V
+    buckets = [i // 7 for i in range(len(Gs))]
+    gp = [g.data_ptr() for g in Gs]
+    nums = [g.numel() for g in Gs]
+    saved = [g.clone() for g in Gs[:7]]
+    for _ in range(2):
+        dm.dmuon_clip_grad_norm_ptrs(h.h, gp, nums, 1e30, buckets, 32, stats=False, stream=stream)
+    dm.dmuon_profile_read(h.h)
+    for _ in range(steps):   # max_norm far above the norms: sum of squares, finalise, no scaling
+        dm.dmuon_clip_grad_norm_ptrs(h.h, gp, nums, 1e30, buckets, 32, stats=False, stream=stream)
+    torch.cuda.synchronize()
+    prof = dm.dmuon_profile_read(h.h)
+    dm.dmuon_profile_enable(h.h, False)
+    clip_ms = prof["clip"][0] / max(1, prof["clip"][1])
+    for g, s0 in zip(Gs[:7], saved):
+        assert torch.equal(g, s0)  # statistics-only clipping left the gradients unchanged
+    g_el = sum(nums)
+    return {
+        "adamw": {"elements": n_el, "ms_per_step": adamw_ms, "bytes_per_element": 28,
+                  "achieved_gbs": 28 * n_el / (adamw_ms / 1e3) / 1e9,
+                  "frac_of_hbm": 28 * n_el / (adamw_ms / 1e3) / 1e9 / hbm_peak, "bound": "hbm"},
+        "clip_norms": {"elements": g_el, "buckets": 32, "ms_per_call": clip_ms, "bytes_per_element": 4,
+                       "achieved_gbs": 4 * g_el / (clip_ms / 1e3) / 1e9,
+                       "frac_of_hbm": 4 * g_el / (clip_ms / 1e3) / 1e9 / hbm_peak, "bound": "hbm"},
+    }
 
 
 def step_groups(shapes, target_groups=32):

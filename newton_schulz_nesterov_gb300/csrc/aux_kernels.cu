@@ -87,13 +87,31 @@ __global__ void __launch_bounds__(256) sumsq_kernel(const ClipArgs a) {
     const int64_t len = min((int64_t)kFlatTile, d.numel - base);
     float ss = 0.f;
     if (d.vec4) {
+      // Four float4 per thread per round (a full tile is 2048 float4 over 256
+      // threads = 2 rounds), all loaded before any is summed so that four
+      // 16-byte reads per thread are in flight.
       const float4* g4 = reinterpret_cast<const float4*>(d.g + base);
-      for (int64_t i = threadIdx.x; i < len / 4; i += blockDim.x) {
-        const float4 g = __ldcs(g4 + i);
-        ss = fmaf(g.x, g.x, ss);
-        ss = fmaf(g.y, g.y, ss);
-        ss = fmaf(g.z, g.z, ss);
-        ss = fmaf(g.w, g.w, ss);
+      const int64_t nv = len / 4;
+      const int64_t bd = blockDim.x;
+      int64_t i = threadIdx.x;
+      for (; i + 3 * bd < nv; i += 4 * bd) {
+        float4 q[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q[k] = __ldcs(g4 + i + k * bd);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          ss = fmaf(q[k].x, q[k].x, ss);
+          ss = fmaf(q[k].y, q[k].y, ss);
+          ss = fmaf(q[k].z, q[k].z, ss);
+          ss = fmaf(q[k].w, q[k].w, ss);
+        }
+      }
+      for (; i < nv; i += bd) {
+        const float4 a = __ldcs(g4 + i);
+        ss = fmaf(a.x, a.x, ss);
+        ss = fmaf(a.y, a.y, ss);
+        ss = fmaf(a.z, a.z, ss);
+        ss = fmaf(a.w, a.w, ss);
       }
     } else {
       for (int64_t i = threadIdx.x; i < len; i += blockDim.x) {
