@@ -120,6 +120,12 @@ int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats,
  * and allocates the workspace (synchronous); later calls with the same
  * shapes only launch.  Asynchronous: completion and non-finite detection
  * are observed through dmuon_get_status().
+ *
+ * CUDA graphs: while `stream` is being captured the call only records its
+ * kernel launches; the plan, the update scales and the pointer set must
+ * already exist from an earlier uncaptured call with the same shapes,
+ * scale_mode and buffers, else DMUON_ERR_ARG.  lr, mu, the coefficients and
+ * the other scalars are recorded by value in the graph.
  */
 int dmuon_step(dmuon_handle_t h, float* const* params,
                const float* const* grads, float* const* momentum,

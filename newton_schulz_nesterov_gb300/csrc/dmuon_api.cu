@@ -397,9 +397,14 @@ cudaEvent_t pool_event(dmuon_ctx* h) {
   return e;
 }
 
-struct LaunchGuard {  // brackets one launch with profiling events
+bool capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus c = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(s, &c) == cudaSuccess && c != cudaStreamCaptureStatusNone;
+}
+
+struct LaunchGuard {  // brackets one launch with profiling events (not under capture)
   dmuon_ctx* h; cudaStream_t s; ProfRec r; bool on;
-  LaunchGuard(dmuon_ctx* h_, cudaStream_t s_, int kind) : h(h_), s(s_), on(h_->profiling) {
+  LaunchGuard(dmuon_ctx* h_, cudaStream_t s_, int kind) : h(h_), s(s_), on(h_->profiling && !capturing(s_)) {
     if (on) { r.a = pool_event(h); r.b = pool_event(h); r.kind = kind; cudaEventRecord(r.a, s); }
   }
   ~LaunchGuard() {
@@ -574,6 +579,14 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
         int ns_steps, const float* coeffs, float eps, float wd, int nesterov, int scale_mode,
         int ns_only, cudaStream_t stream) {
   if (cudaSetDevice(h->device) != cudaSuccess) return fail(h, DMUON_ERR_CUDA, "cudaSetDevice");
+  // Under stream capture nothing may allocate, upload or synchronise: the
+  // plan, the update scales and the pointer set must already exist from an
+  // earlier call with the same shapes, options and buffers.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return fail(h, DMUON_ERR_CUDA, "cudaStreamIsCapturing");
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
+  if (capturing && !same_shapes(h, shapes, n))
+    return fail(h, DMUON_ERR_ARG, "stream capture: call once with these shapes before capturing");
   int rc = build_plan(h, shapes, n);
   if (rc) return rc;
 
@@ -586,6 +599,8 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
       const float s = scale_of(ch.L.mats[i], scale_mode);
       if (ch.L.mats[i].scale != s) { ch.L.mats[i].scale = s; dirty = true; }
     }
+    if (dirty && capturing)
+      return fail(h, DMUON_ERR_ARG, "stream capture: call once with this scale_mode before capturing");
     if (dirty) {
       e = cudaStreamSynchronize(stream);
       if (e == cudaSuccess) e = cudaMemcpy(ch.d_mats, ch.L.mats.data(), sizeof(MatDesc) * ch.n, cudaMemcpyHostToDevice);
@@ -605,6 +620,8 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
       same = sp[i].W == ptrs[i].W && sp[i].G == ptrs[i].G && sp[i].M == ptrs[i].M;
     if (same) slot = k;
   }
+  if (slot < 0 && capturing)
+    return fail(h, DMUON_ERR_ARG, "stream capture: call once with these buffers before capturing");
   if (slot < 0) {
     slot = 0;
     for (int k = 1; k < kPtrSlots; ++k)

@@ -219,6 +219,43 @@ def test_chunking_is_bitwise_neutral(handle):
         assert torch.equal(a, b)
 
 
+def test_step_recorded_in_cuda_graph(handle):
+    """Three eager steps equal one eager step plus two replays of a graph
+    that recorded the step, bitwise; capturing before the buffers were seen
+    is refused with DMUON_ERR_ARG and records nothing."""
+    w = workloads.get("tinymlp_d128")
+    n = len(w.shapes)
+    Ws = [workloads.weight(w, i) for i in range(n)]
+    Gs = [workloads.grad(w, i) for i in range(n)]
+    Ms = [workloads.momentum(w, i) for i in range(n)]
+    Wa, Ga, Ma = _to_dev(Ws), _to_dev(Gs), _to_dev(Ms)
+    for _ in range(3):
+        handle.step(Wa, Ga, Ma)
+    torch.cuda.synchronize()
+    with dm.Handle(0) as h2:
+        Wb, Gb, Mb = _to_dev(Ws), _to_dev(Gs), _to_dev(Ms)
+        Wc, Gc, Mc = _to_dev(Ws), _to_dev(Gs), _to_dev(Ms)
+        h2.step(Wb, Gb, Mb)            # plans and caches these buffers
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            h2.step(Wb, Gb, Mb)
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2):
+            rc = dm.dmuon_step_ptrs(h2.h, [t.data_ptr() for t in Wc], [t.data_ptr() for t in Gc],
+                                    [t.data_ptr() for t in Mc], [tuple(t.shape) for t in Wc],
+                                    0.02, 0.95, 5, check=False)
+        assert rc == -1 and "capture" in dm.dmuon_last_error(h2.h)
+        g.replay()
+        g.replay()
+        torch.cuda.synchronize()
+        assert h2.status()[0] == 0
+        for a, b in zip(Wa + Ma, Wb + Mb):
+            assert torch.equal(a, b)
+        for a, b in zip(Wc, Ws):
+            assert torch.equal(a.cpu(), b)   # the refused capture changed nothing
+
+
 def test_alternating_pointer_sets(handle):
     """Per-group calls (same shapes, different buffers) reuse cached pointer
     slots: 70 groups cycle through the 64 slots twice, so slots are evicted
