@@ -252,6 +252,15 @@ int dmuon_set_tile_mode(dmuon_handle_t h, int mode);
  * result does not depend on the chunking. */
 int dmuon_set_chunk_elements(dmuon_handle_t h, int64_t elems);
 
+/* Overlap of later plans with two or more chunks (default off): chunk c+1's
+ * momentum/normalisation pass runs on an internal stream while chunk c's
+ * tensor-core phases run on the caller's stream; chunks then alternate
+ * between two workspaces (twice the workspace memory).  The call stays
+ * ordered on the caller's stream (fork and join through events).  The
+ * result does not depend on the setting.  On a power-capped GB300 running
+ * the Llama-3-8B set it measured the same step time either way. */
+int dmuon_set_overlap(dmuon_handle_t h, int on);
+
 /* Kernel launches issued by this handle since creation (a counter). */
 int64_t dmuon_launch_count(dmuon_handle_t h);
 

@@ -96,6 +96,8 @@ def load(path=None):
     L.dmuon_get_status.restype = i32
     L.dmuon_last_error.argtypes = [vp]
     L.dmuon_last_error.restype = ctypes.c_char_p
+    L.dmuon_set_overlap.argtypes = [vp, i32]
+    L.dmuon_set_overlap.restype = i32
     L.dmuon_set_chunk_elements.argtypes = [vp, i64]
     L.dmuon_set_chunk_elements.restype = i32
     L.dmuon_set_tile_mode.argtypes = [vp, i32]
@@ -322,6 +324,11 @@ def dmuon_get_status(h, n_flags=0):
     flags = (ctypes.c_int * max(1, n_flags))()
     rc = load().dmuon_get_status(h, flags, int(n_flags))
     return rc, [flags[i] for i in range(n_flags)]
+
+
+def dmuon_set_overlap(h, on=True):  # default off in the library
+    """Overlap the next chunk's momentum pass with the current chunk's products."""
+    _check(load().dmuon_set_overlap(h, 1 if on else 0), "dmuon_set_overlap")
 
 
 def dmuon_set_chunk_elements(h, elems):

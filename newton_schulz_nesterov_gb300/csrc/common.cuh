@@ -45,9 +45,10 @@ struct MatPtrs {
 // Momentum/normalisation tile: 64 x 64 fp32 elements of W's shape.
 constexpr int kMomTile = 64;
 
-// Work item of a tensor-core phase: {matrix, 128-row tile, 256-col tile,
-// number of 64-wide K blocks}.
-// Tensor-core tile: 128 rows (UMMA M) x 256 cols (UMMA N), K step 64.
+// Work item of a tensor-core phase: {matrix, row tile, 256-col tile, number
+// of 64-wide K blocks}; the row tile is 128 rows for single CTAs and 256 rows
+// for CTA pairs.
+// Single-CTA tile: 128 rows (UMMA M) x 256 cols (UMMA N), K step 64.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
@@ -69,11 +70,8 @@ constexpr int kGemmSmem =
 constexpr int kPairStages = 6;
 constexpr int kPairHalfBytes = 128 * kBK * 2;            // 16 KB
 constexpr int kPairStageBytes = 2 * kPairHalfBytes;      // 32 KB per CTA
-// The 16 KB guard after the stages keeps any operand read that overruns a
-// stage inside this CTA's shared memory.
-constexpr int kPairGuardBytes = 16384;
-constexpr int kPairSmem = 1024 /*align slack*/ + kPairStages * kPairStageBytes + kPairGuardBytes +
-                          4 * kEpiWords * 4 + 256;
+constexpr int kPairSmem =
+    1024 /*align slack*/ + kPairStages * kPairStageBytes + 4 * kEpiWords * 4 + 256;
 
 enum Phase : int { kPhaseGram = 0, kPhaseGram2 = 1, kPhaseApply = 2 };
 enum FinalMode : int { kWriteX = 0, kUpdateW = 1, kWriteO = 2 };

@@ -196,6 +196,13 @@ struct dmuon_ctx {
   int64_t chunk_elems = 0;                  // requested chunk size (0: default)
   bool plan_pair = false;                   // tile kind of the current plan
   int64_t plan_chunk_elems = 0;             // chunk size of the current plan
+  // Overlap of chunk c+1's momentum pass with chunk c's tensor-core phases:
+  // a side stream, two alternating chunk workspaces and fork/join events.
+  bool overlap = false;                     // requested (off: measured neutral at the power cap)
+  bool plan_overlap = false;                // in the current plan (needs >= 2 chunks)
+  size_t ws_chunk = 0;                      // bytes of one chunk workspace
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_norm[2] = {}, ev_gemm[2] = {};
   // AdamW / clipping: descriptor buffer (device), pinned staging, results
   void* aux_dev = nullptr;
   size_t aux_dev_cap = 0;
@@ -258,7 +265,7 @@ int64_t chunk_limit(const dmuon_ctx* h) { return h->chunk_elems > 0 ? h->chunk_e
 
 bool same_shapes(const dmuon_ctx* h, const dmuon_shape_t* s, int n) {
   if ((int)h->shapes.size() != n || !h->small || h->plan_pair != use_pairs(h, s, n) ||
-      h->plan_chunk_elems != chunk_limit(h))
+      h->plan_chunk_elems != chunk_limit(h) || h->plan_overlap != (h->overlap && h->chunks.size() > 1))
     return false;
   for (int i = 0; i < n; ++i)
     if (h->shapes[i].rows != s[i].rows || h->shapes[i].cols != s[i].cols) return false;
@@ -323,6 +330,9 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
     h->ws_bytes = std::max(h->ws_bytes, ch.L.ws_bytes);
     h->small_bytes += chunk_small_bytes(ch.L, ch.n);
   }
+  h->ws_chunk = h->ws_bytes;
+  h->plan_overlap = h->overlap && h->chunks.size() > 1;
+  if (h->plan_overlap) h->ws_bytes = 2 * h->ws_chunk;  // chunks alternate between two
   cudaError_t e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) { h->ws = nullptr; cudaGetLastError(); free_plan(h); return fail(h, DMUON_ERR_OOM, "workspace cudaMalloc", e); }
   e = cudaMalloc(&h->small, h->small_bytes);
@@ -332,8 +342,9 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
   h->d_ptrs = (MatPtrs*)carve(sizeof(MatPtrs) * n * kPtrSlots);
   h->d_flags = (int*)carve(4 * n);
   h->d_err = (int*)carve(256);
-  uint8_t* ws = (uint8_t*)h->ws;
-  for (Chunk& ch : h->chunks) {
+  for (size_t c = 0; c < h->chunks.size(); ++c) {
+    Chunk& ch = h->chunks[c];
+    uint8_t* ws = (uint8_t*)h->ws + (h->plan_overlap ? (c & 1) * h->ws_chunk : 0);
     Layout& L = ch.L;
     const int cn = ch.n;
     ch.d_mats = (MatDesc*)carve(sizeof(MatDesc) * cn);
@@ -515,8 +526,9 @@ bool is_vec4(const void* p, int64_t numel) { return (((uintptr_t)p & 15u) == 0) 
 
 // The launch sequence of one chunk: momentum/normalise, norm, then
 // ns_steps x (Gram, Gram2, Apply), the last Apply writing W (or O).
-int run_chunk(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, float mu, int ns_steps,
-              const float* coeffs, float eps, float wd, int nesterov, int ns_only, cudaStream_t stream) {
+// Momentum, Nesterov input, bf16 iterate and the per-matrix norm of a chunk.
+int run_chunk_norm(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float mu, float eps,
+                   int nesterov, int ns_only, cudaStream_t stream) {
   const Layout& L = ch.L;
   const int n = ch.n;
   const int64_t nt = L.tile_prefix[n];
@@ -532,6 +544,16 @@ int run_chunk(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, flo
     LaunchGuard g(h, stream, DMUON_KIND_FINALIZE);
     if ((e = launch_finalize(a, stream)) != cudaSuccess) return fail(h, cuda_err(e), "finalize launch", e);
   }
+  return DMUON_OK;
+}
+
+// Newton-Schulz iterations and the update of a chunk.
+int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, int ns_steps,
+                 const float* coeffs, float wd, int ns_only, cudaStream_t stream) {
+  const Layout& L = ch.L;
+  const int n = ch.n;
+  const int64_t nt = L.tile_prefix[n];
+  cudaError_t e;
   const float decay = 1.f - lr * wd;
   if (ns_steps == 0) {
     Update0Args a{ch.d_mats, dptrs, ch.d_prefix, n, nt, ch.d_svec, lr, decay, ns_only};
@@ -640,10 +662,36 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
   const MatPtrs* dptrs = h->d_ptrs + (size_t)slot * n;
   h->last_stream = stream;
 
-  for (const Chunk& ch : h->chunks) {
-    rc = run_chunk(h, ch, dptrs + ch.i0, lr, mu, ns_steps, coeffs, eps, wd, nesterov, ns_only, stream);
-    if (rc) return rc;
+  if (!h->plan_overlap) {
+    for (const Chunk& ch : h->chunks) {
+      if ((rc = run_chunk_norm(h, ch, dptrs + ch.i0, mu, eps, nesterov, ns_only, stream))) return rc;
+      if ((rc = run_chunk_ns(h, ch, dptrs + ch.i0, lr, ns_steps, coeffs, wd, ns_only, stream))) return rc;
+    }
+    return DMUON_OK;
   }
+  // Chunk c's momentum pass runs on the side stream into workspace c % 2
+  // once chunk c-2's tensor-core phases (same workspace) are done; chunk c's
+  // phases run on the caller's stream once its norm is ready.  Enqueued
+  // chunk by chunk so every event is recorded before it is waited on.
+  if ((e = cudaEventRecord(h->ev_fork, stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(h->side, h->ev_fork, 0)) != cudaSuccess)
+    return fail(h, cuda_err(e), "overlap fork", e);
+  for (size_t c = 0; c < h->chunks.size(); ++c) {
+    const Chunk& ch = h->chunks[c];
+    const int b = (int)(c & 1);
+    if (c >= 2 && (e = cudaStreamWaitEvent(h->side, h->ev_gemm[b], 0)) != cudaSuccess)
+      return fail(h, cuda_err(e), "overlap wait", e);
+    if ((rc = run_chunk_norm(h, ch, dptrs + ch.i0, mu, eps, nesterov, ns_only, h->side))) return rc;
+    if ((e = cudaEventRecord(h->ev_norm[b], h->side)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, h->ev_norm[b], 0)) != cudaSuccess)
+      return fail(h, cuda_err(e), "overlap hand-off", e);
+    if ((rc = run_chunk_ns(h, ch, dptrs + ch.i0, lr, ns_steps, coeffs, wd, ns_only, stream))) return rc;
+    if ((e = cudaEventRecord(h->ev_gemm[b], stream)) != cudaSuccess)
+      return fail(h, cuda_err(e), "overlap record", e);
+  }
+  if ((e = cudaEventRecord(h->ev_join, h->side)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(stream, h->ev_join, 0)) != cudaSuccess)
+    return fail(h, cuda_err(e), "overlap join", e);
   return DMUON_OK;
 }
 
@@ -700,6 +748,17 @@ int dmuon_create(dmuon_handle_t* out, int device) {
     delete h;
     return DMUON_ERR_CUDA;
   }
+  bool ok = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) == cudaSuccess;
+  for (int b = 0; b < 2; ++b) {
+    ok = ok && cudaEventCreateWithFlags(&h->ev_norm[b], cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&h->ev_gemm[b], cudaEventDisableTiming) == cudaSuccess;
+  }
+  if (!ok) {
+    dmuon_destroy(h);
+    return DMUON_ERR_CUDA;
+  }
   *out = h;
   return DMUON_OK;
 }
@@ -712,6 +771,9 @@ void dmuon_destroy(dmuon_handle_t h) {
   for (int k = 0; k < kPtrSlots; ++k)
     if (h->slot_ev[k]) cudaEventDestroy(h->slot_ev[k]);
   if (h->aux_ev) cudaEventDestroy(h->aux_ev);
+  for (cudaEvent_t ev : {h->ev_fork, h->ev_join, h->ev_norm[0], h->ev_norm[1], h->ev_gemm[0], h->ev_gemm[1]})
+    if (ev) cudaEventDestroy(ev);
+  if (h->side) cudaStreamDestroy(h->side);
   if (h->aux_dev) cudaFree(h->aux_dev);
   if (h->aux_host) cudaFreeHost(h->aux_host);
   for (auto& r : h->prof) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
@@ -941,6 +1003,12 @@ int dmuon_set_wait_timeout(dmuon_handle_t h, uint64_t ns) {
 int dmuon_set_chunk_elements(dmuon_handle_t h, int64_t elems) {
   if (!h || elems < 0) return DMUON_ERR_ARG;
   h->chunk_elems = elems;
+  return DMUON_OK;
+}
+
+int dmuon_set_overlap(dmuon_handle_t h, int on) {
+  if (!h) return DMUON_ERR_ARG;
+  h->overlap = on != 0;
   return DMUON_OK;
 }
 

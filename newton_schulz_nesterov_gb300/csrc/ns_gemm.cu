@@ -433,7 +433,7 @@ __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
   const uint32_t a = ptx::smem_addr(raw);
   uint8_t* base = raw + ((1024u - (a & 1023u)) & 1023u);
   s.stages = base;
-  uint8_t* after = base + kPairStages * kPairStageBytes + kPairGuardBytes;
+  uint8_t* after = base + kPairStages * kPairStageBytes;
   s.scratch = reinterpret_cast<uint32_t*>(after);
   s.bars = reinterpret_cast<uint64_t*>(after + 4 * kEpiWords * 4);
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + 2 * kPairStages + 5);

@@ -194,18 +194,20 @@ def test_deterministic_bitwise(handle):
 
 
 def test_chunking_is_bitwise_neutral(handle):
-    """The same list stepped as one chunk and as many small chunks gives
-    bitwise identical weights and momenta (each matrix's arithmetic does not
-    depend on its neighbours); each chunk issues its own 2 + 3*ns launches."""
+    """The same list stepped as one chunk and as many small chunks, with the
+    next chunk's momentum pass overlapped or not, gives bitwise identical
+    weights and momenta (each matrix's arithmetic does not depend on its
+    neighbours); each chunk issues its own 2 + 3*ns launches."""
     gen = torch.Generator().manual_seed(29)
     shapes = [(300, 500), (500, 300), (257, 257), (64, 640), (640, 64), (130, 900)]
     Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
     Gs = [torch.randn(s, generator=gen) for s in shapes]
     Ms = [torch.randn(s, generator=gen) for s in shapes]
     res = {}
-    for elems in (1 << 29, 160_000):
+    for elems, overlap in ((1 << 29, True), (160_000, True), (160_001, False)):
         with dm.Handle(0) as h2:
             dm.dmuon_set_chunk_elements(h2.h, elems)
+            dm.dmuon_set_overlap(h2.h, overlap)
             Wd, Gd, Md = _to_dev(Ws), _to_dev(Gs), _to_dev(Ms)
             before = dm.dmuon_launch_count(h2.h)
             h2.step(Wd, Gd, Md)
@@ -215,8 +217,9 @@ def test_chunking_is_bitwise_neutral(handle):
             res[elems] = ([x.cpu() for x in Wd], [x.cpu() for x in Md], launches, summary)
     assert res[1 << 29][2] == 17 and "chunks 1 " in res[1 << 29][3]
     assert res[160_000][2] > 17 and res[160_000][2] % 17 == 0
-    for a, b in zip(res[1 << 29][0] + res[1 << 29][1], res[160_000][0] + res[160_000][1]):
-        assert torch.equal(a, b)
+    for key in (160_000, 160_001):   # overlapped and serial chunk schedules
+        for a, b in zip(res[1 << 29][0] + res[1 << 29][1], res[key][0] + res[key][1]):
+            assert torch.equal(a, b)
 
 
 def test_step_recorded_in_cuda_graph(handle):
