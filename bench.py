@@ -24,7 +24,6 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +32,6 @@ sys.path.insert(0, ROOT)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
-L2_BYTES = 129 * 1024 * 1024
 
 
 def parse_args():

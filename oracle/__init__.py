@@ -32,6 +32,10 @@ rank-1 cases, and hand-computed momentum/update values.  Two readings are
 (``scale_mode``) and the coefficient rows used beyond the fifth step.
 """
 
+# oracle.aux_steps holds the fp64 AdamW and segmented-clipping oracle (the
+# other parts of Muon.step built here); it is pinned in
+# tests/test_oracle_aux_pins.py against hand values and PyTorch's routines.
+from . import aux_steps  # noqa: F401
 from .step import (  # noqa: F401
     YOU_COEFFICIENTS,
     coefficient_rows,

@@ -413,5 +413,6 @@ def test_full_spiked_4096_sampled(handle):
 
 
 @pytest.mark.slow
-def test_full_tp_70b_mixed_small_sampled(handle):
-    _full_size_sampled(handle, "tp_70b_mixed", [1, 2, 256, 512])
+def test_full_tp_70b_mixed_sampled(handle):
+    # the 28672x8192 matrix (transposed, short side 8192) and four 64x256 ones
+    _full_size_sampled(handle, "tp_70b_mixed", [0, 1, 2, 256, 512])

@@ -12,7 +12,6 @@ a fresh process and after the rest of the suite.
 """
 import ctypes
 
-import numpy as np
 import pytest
 
 torch = pytest.importorskip("torch")
