@@ -261,6 +261,19 @@ int dmuon_set_chunk_elements(dmuon_handle_t h, int64_t elems);
  * the Llama-3-8B set it measured the same step time either way. */
 int dmuon_set_overlap(dmuon_handle_t h, int on);
 
+/* Small-matrix kernel for later plans (default on): every matrix whose
+ * oriented shape has m = min(rows, cols) <= 128 and n = max(rows, cols) <= 512
+ * (the TinyMLP projections of DMuon "Quick Start" at small widths; the
+ * small parameters that "API Reference", section "Muon", packs together
+ * under pack_small_params; 64x256 tensor-parallel shards) runs its whole step -- momentum, Nesterov input, norm, the ns_steps
+ * iterations and the update -- in one CTA, with the iterate in shared memory
+ * and the products in tensor memory; all such matrices share one launch.
+ * Off: they run through the chunked tensor-core path like the others.  Same
+ * maths and bf16 roundings either way (the summation order inside a product
+ * differs, so results agree to rounding, not bitwise).  Returns
+ * DMUON_ERR_UNSUPPORTED if it cannot be enabled on this device. */
+int dmuon_set_small_path(dmuon_handle_t h, int on);
+
 /* Kernel launches issued by this handle since creation (a counter). */
 int64_t dmuon_launch_count(dmuon_handle_t h);
 
@@ -282,7 +295,8 @@ int64_t dmuon_launch_count(dmuon_handle_t h);
 #define DMUON_KIND_UPDATE0  5
 #define DMUON_KIND_ADAMW    6
 #define DMUON_KIND_CLIP     7
-#define DMUON_NUM_KINDS     8
+#define DMUON_KIND_SMALL    8
+#define DMUON_NUM_KINDS     9
 int dmuon_profile_enable(dmuon_handle_t h, int on);
 int dmuon_profile_read(dmuon_handle_t h, double* ms, int64_t* count,
                        int n_kinds);

@@ -32,7 +32,7 @@ STATUS = {
     -4: "DMUON_ERR_CUDA", -5: "DMUON_ERR_NONFINITE", -6: "DMUON_ERR_TIMEOUT",
     -7: "DMUON_ERR_UNSUPPORTED",
 }
-KIND_NAMES = ("momentum", "finalize", "gram", "gram2", "apply", "update0", "adamw", "clip")
+KIND_NAMES = ("momentum", "finalize", "gram", "gram2", "apply", "update0", "adamw", "clip", "small")
 
 
 class DmuonError(RuntimeError):
@@ -98,6 +98,8 @@ def load(path=None):
     L.dmuon_last_error.restype = ctypes.c_char_p
     L.dmuon_set_overlap.argtypes = [vp, i32]
     L.dmuon_set_overlap.restype = i32
+    L.dmuon_set_small_path.argtypes = [vp, i32]
+    L.dmuon_set_small_path.restype = i32
     L.dmuon_set_chunk_elements.argtypes = [vp, i64]
     L.dmuon_set_chunk_elements.restype = i32
     L.dmuon_set_tile_mode.argtypes = [vp, i32]
@@ -334,6 +336,12 @@ def dmuon_set_overlap(h, on=True):  # default off in the library
 def dmuon_set_chunk_elements(h, elems):
     """Chunk size of later plans in matrix elements (0 = default 2^29)."""
     _check(load().dmuon_set_chunk_elements(h, int(elems)), "dmuon_set_chunk_elements")
+
+
+def dmuon_set_small_path(h, on=True):  # default on in the library
+    """Route small matrices (oriented m <= 128, n <= 512) through the fused
+    one-CTA-per-matrix kernel (on) or through the chunked GEMM path (off)."""
+    _check(load().dmuon_set_small_path(h, 1 if on else 0), "dmuon_set_small_path")
 
 
 def dmuon_set_tile_mode(h, mode):

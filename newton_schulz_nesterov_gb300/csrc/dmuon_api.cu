@@ -3,10 +3,17 @@
 // per-call pointer upload and the launch sequence of one step.
 //
 // Launch sequence of one step (all on the caller's stream, no host sync):
+//   ns_small    every small matrix (oriented m <= 128, n <= 512) in one
+//               launch, one CTA per matrix running its whole step
+//   then, per chunk of the other matrices:
 //   mom_norm    M <- mu*M + G, U, X0 = bf16(U or U^T), tile sums of U^2
 //   finalize    s = 1/(||U||_F + eps) per matrix
 //   ns_steps x [ Gram (A = X X^T) -> Gram2 (B = bA + cAA) -> Apply (X' = aX + BX) ]
 //   the last Apply updates W in place (or writes O for the standalone NS)
+//
+// Plan order: the large matrices (in the caller's order, chunked), then the
+// small ones.  Device pointer sets and flags are kept in plan order; the
+// caller's order is restored when flags are read.
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
@@ -20,6 +27,7 @@
 #include "../../include/dmuon.h"
 #include "aux.cuh"
 #include "common.cuh"
+#include "small.cuh"
 
 using namespace dmuon;
 
@@ -40,6 +48,11 @@ const char* kVersion = "dmuon-gb300 0.1.0 (sm_103a, tcgen05/TMA)";
 constexpr int kPtrSlots = 64;
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Shapes the fused small-matrix kernel takes (oriented m <= 128, n <= 512).
+inline bool is_small(const dmuon_shape_t& s) {
+  return std::min(s.rows, s.cols) <= kSmallMaxM && std::max(s.rows, s.cols) <= kSmallMaxN;
+}
 inline int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -169,7 +182,14 @@ struct dmuon_ctx {
   int device = 0;
   int num_sms = 0;
   // plan
-  std::vector<dmuon_shape_t> shapes;
+  std::vector<dmuon_shape_t> shapes;   // caller order
+  std::vector<int> order;              // plan position -> caller index
+  int n_large = 0;                     // plan positions [0, n_large) are chunked
+  std::vector<SmallDesc> small_descs;  // plan positions [n_large, n)
+  SmallDesc* d_small = nullptr;
+  bool small_path = true;              // requested
+  bool small_ok = false;               // small kernel configured on this device
+  bool plan_small = false;             // small kernel used by the current plan
   std::vector<Chunk> chunks;
   size_t ws_bytes = 0, small_bytes = 0;
   void* ws = nullptr;
@@ -239,6 +259,10 @@ void free_plan(dmuon_ctx* h) {
   if (h->small) cudaFree(h->small);
   h->ws = h->small = nullptr;
   h->shapes.clear();
+  h->order.clear();
+  h->small_descs.clear();
+  h->d_small = nullptr;
+  h->n_large = 0;
   h->chunks.clear();
   for (int k = 0; k < kPtrSlots; ++k) {
     if (h->slot_pending[k]) cudaEventSynchronize(h->slot_ev[k]);
@@ -265,6 +289,7 @@ int64_t chunk_limit(const dmuon_ctx* h) { return h->chunk_elems > 0 ? h->chunk_e
 
 bool same_shapes(const dmuon_ctx* h, const dmuon_shape_t* s, int n) {
   if ((int)h->shapes.size() != n || !h->small || h->plan_pair != use_pairs(h, s, n) ||
+      h->plan_small != (h->small_path && h->small_ok) ||
       h->plan_chunk_elems != chunk_limit(h) || h->plan_overlap != (h->overlap && h->chunks.size() > 1))
     return false;
   for (int i = 0; i < n; ++i)
@@ -299,14 +324,32 @@ size_t chunk_small_bytes(const Layout& L, int n) {
          rup(16 * L.items[0].size(), 256) + rup(16 * L.items[1].size(), 256) + rup(16 * L.items[2].size(), 256);
 }
 
+// Plan order: positions [0, n_large) hold the matrices run by the chunked
+// tensor-core path (caller order), the rest the small ones (caller order).
+int plan_order(const dmuon_shape_t* shapes, int n, bool small_path, std::vector<int>& order) {
+  order.clear();
+  for (int i = 0; i < n; ++i)
+    if (!(small_path && is_small(shapes[i]))) order.push_back(i);
+  const int n_large = (int)order.size();
+  for (int i = 0; i < n; ++i)
+    if (small_path && is_small(shapes[i])) order.push_back(i);
+  return n_large;
+}
+
 // Host-side plan sizes (no device work): workspace of the largest chunk and
 // all device arrays.
-void plan_sizes(const dmuon_shape_t* shapes, int n, bool pair, int64_t limit, size_t* ws, size_t* small) {
+void plan_sizes(const dmuon_shape_t* shapes, int n, bool pair, int64_t limit, bool small_path, size_t* ws,
+                size_t* small) {
+  std::vector<int> order;
+  const int n_large = plan_order(shapes, n, small_path, order);
+  std::vector<dmuon_shape_t> ps(n);
+  for (int k = 0; k < n; ++k) ps[k] = shapes[order[k]];
   *ws = 256;
-  *small = rup(sizeof(MatPtrs) * n * kPtrSlots, 256) + rup(4 * n, 256) + 256;
-  for (const auto& c : split_chunks(shapes, n, limit)) {
+  *small = rup(sizeof(MatPtrs) * n * kPtrSlots, 256) + rup(4 * n, 256) + 256 +
+           rup(sizeof(SmallDesc) * (n - n_large), 256);
+  for (const auto& c : split_chunks(ps.data(), n_large, limit)) {
     Layout L;
-    make_layout(shapes + c.first, c.second, L, pair);
+    make_layout(ps.data() + c.first, c.second, L, pair);
     *ws = std::max(*ws, L.ws_bytes);
     *small += chunk_small_bytes(L, c.second);
   }
@@ -318,15 +361,24 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
   if (!get_encoder()) return fail(h, DMUON_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
   h->plan_pair = use_pairs(h, shapes, n);
   h->plan_chunk_elems = chunk_limit(h);
-  const auto parts = split_chunks(shapes, n, h->plan_chunk_elems);
+  h->plan_small = h->small_path && h->small_ok;
+  h->n_large = plan_order(shapes, n, h->plan_small, h->order);
+  std::vector<dmuon_shape_t> ps(n);
+  for (int k = 0; k < n; ++k) ps[k] = shapes[h->order[k]];
+  const int n_small = n - h->n_large;
+  h->small_descs.resize(n_small);
+  for (int k = 0; k < n_small; ++k)
+    h->small_descs[k] = SmallDesc{ps[h->n_large + k].rows, ps[h->n_large + k].cols, h->n_large + k, 1.f};
+  const auto parts = split_chunks(ps.data(), h->n_large, h->plan_chunk_elems);
   h->chunks.resize(parts.size());
   h->ws_bytes = 256;
-  h->small_bytes = rup(sizeof(MatPtrs) * n * kPtrSlots, 256) + rup(4 * n, 256) + 256;
+  h->small_bytes = rup(sizeof(MatPtrs) * n * kPtrSlots, 256) + rup(4 * n, 256) + 256 +
+                   rup(sizeof(SmallDesc) * n_small, 256);
   for (size_t c = 0; c < parts.size(); ++c) {
     Chunk& ch = h->chunks[c];
     ch.i0 = parts[c].first;
     ch.n = parts[c].second;
-    make_layout(shapes + ch.i0, ch.n, ch.L, h->plan_pair);
+    make_layout(ps.data() + ch.i0, ch.n, ch.L, h->plan_pair);
     h->ws_bytes = std::max(h->ws_bytes, ch.L.ws_bytes);
     h->small_bytes += chunk_small_bytes(ch.L, ch.n);
   }
@@ -342,6 +394,11 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
   h->d_ptrs = (MatPtrs*)carve(sizeof(MatPtrs) * n * kPtrSlots);
   h->d_flags = (int*)carve(4 * n);
   h->d_err = (int*)carve(256);
+  h->d_small = (SmallDesc*)carve(sizeof(SmallDesc) * n_small);
+  if (n_small > 0) {
+    e = cudaMemcpy(h->d_small, h->small_descs.data(), sizeof(SmallDesc) * n_small, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) { free_plan(h); return fail(h, cuda_err(e), "plan upload", e); }
+  }
   for (size_t c = 0; c < h->chunks.size(); ++c) {
     Chunk& ch = h->chunks[c];
     uint8_t* ws = (uint8_t*)h->ws + (h->plan_overlap ? (c & 1) * h->ws_chunk : 0);
@@ -367,7 +424,8 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
                 encode_map(&maps[kMapsPerMat * i + 3], d.B, d.m, d.m, d.lda);
       if (!ok) {
         char what[160];
-        std::snprintf(what, sizeof what, "cuTensorMapEncodeTiled failed for matrix %d (%lld x %lld)", ch.i0 + i,
+        std::snprintf(what, sizeof what, "cuTensorMapEncodeTiled failed for matrix %d (%lld x %lld)",
+                      h->order[ch.i0 + i],
                       (long long)d.rows, (long long)d.cols);
         free_plan(h);
         return fail(h, DMUON_ERR_CUDA, what);
@@ -629,6 +687,25 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
       if (e != cudaSuccess) return fail(h, cuda_err(e), "descriptor refresh", e);
     }
   }
+  {
+    bool dirty = false;
+    for (SmallDesc& d : h->small_descs) {
+      MatDesc md{};
+      md.rows = d.rows;
+      md.cols = d.cols;
+      const float s = scale_of(md, scale_mode);
+      if (d.scale != s) { d.scale = s; dirty = true; }
+    }
+    if (dirty && capturing)
+      return fail(h, DMUON_ERR_ARG, "stream capture: call once with this scale_mode before capturing");
+    if (dirty) {
+      e = cudaStreamSynchronize(stream);
+      if (e == cudaSuccess)
+        e = cudaMemcpy(h->d_small, h->small_descs.data(), sizeof(SmallDesc) * h->small_descs.size(),
+                       cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) return fail(h, cuda_err(e), "descriptor refresh", e);
+    }
+  }
 
   // Caller pointer sets are cached in kPtrSlots device slots (least recently
   // used is replaced), so alternating between a few lists of buffers -- e.g.
@@ -651,7 +728,7 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
     // The slot's pinned staging may still feed an earlier copy.
     if (h->slot_pending[slot]) { cudaEventSynchronize(h->slot_ev[slot]); h->slot_pending[slot] = false; }
     MatPtrs* stage = h->h_stage + (size_t)slot * n;
-    std::memcpy(stage, ptrs, sizeof(MatPtrs) * n);
+    for (int k = 0; k < n; ++k) stage[k] = ptrs[h->order[k]];  // plan order
     e = cudaMemcpyAsync(h->d_ptrs + (size_t)slot * n, stage, sizeof(MatPtrs) * n, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess) e = cudaEventRecord(h->slot_ev[slot], stream);
     if (e != cudaSuccess) return fail(h, cuda_err(e), "pointer upload", e);
@@ -661,6 +738,29 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
   h->slot_use[slot] = ++h->use_clock;
   const MatPtrs* dptrs = h->d_ptrs + (size_t)slot * n;
   h->last_stream = stream;
+
+  if (!h->small_descs.empty()) {
+    SmallArgs a{};
+    a.descs = h->d_small;
+    a.ptrs = dptrs;
+    a.flags = h->d_flags;
+    a.err = h->d_err;
+    a.timeout_ns = h->wait_timeout_ns;
+    a.ns_steps = ns_steps;
+    a.ns_only = ns_only;
+    a.nesterov = nesterov;
+    a.mu = mu;
+    a.eps = eps;
+    a.lr = lr;
+    a.decay = 1.f - lr * wd;
+    for (int k = 0; k < ns_steps; ++k) {
+      const float* row = coeffs ? coeffs + 3 * k : kYouCoefficients[std::min(k, 4)];
+      for (int q = 0; q < 3; ++q) a.coeffs[k][q] = row[q];
+    }
+    LaunchGuard g(h, stream, DMUON_KIND_SMALL);
+    if ((e = launch_small(a, (int)h->small_descs.size(), stream)) != cudaSuccess)
+      return fail(h, cuda_err(e), "ns_small launch", e);
+  }
 
   if (!h->plan_overlap) {
     for (const Chunk& ch : h->chunks) {
@@ -727,6 +827,8 @@ int dmuon_create(dmuon_handle_t* out, int device) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (major != 10 || minor != 3) return DMUON_ERR_UNSUPPORTED;
   if (gemm_configure() != cudaSuccess) return DMUON_ERR_CUDA;
+  const bool small_ok = small_configure() == cudaSuccess;
+  if (!small_ok) cudaGetLastError();
   int clusters = 0;
   if (gemm_pair_configure(&clusters) != cudaSuccess) {
     cudaGetLastError();
@@ -736,6 +838,7 @@ int dmuon_create(dmuon_handle_t* out, int device) {
   h->device = device;
   h->num_sms = sms;
   h->max_clusters = clusters;
+  h->small_ok = small_ok;
   for (int k = 0; k < kPtrSlots; ++k) {
     if (cudaEventCreateWithFlags(&h->slot_ev[k], cudaEventDisableTiming) != cudaSuccess) {
       for (int j = 0; j < k; ++j) cudaEventDestroy(h->slot_ev[j]);
@@ -786,10 +889,16 @@ int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats, size_t* out_b
   *out_bytes = 0;
   if (n_mats == 0) return DMUON_OK;
   if (int rc = check_shapes(shapes, n_mats)) return rc;
-  size_t ws1, sm1, ws2, sm2;
-  plan_sizes(shapes, n_mats, false, kDefaultChunkElems, &ws1, &sm1);
-  plan_sizes(shapes, n_mats, true, kDefaultChunkElems, &ws2, &sm2);
-  *out_bytes = std::max(ws1 + sm1, ws2 + sm2);
+  // The largest plan over tile kinds, with and without the small-matrix
+  // kernel (which needs no workspace).
+  size_t most = 0;
+  for (int pair = 0; pair < 2; ++pair)
+    for (int sp = 0; sp < 2; ++sp) {
+      size_t ws, sm;
+      plan_sizes(shapes, n_mats, pair != 0, kDefaultChunkElems, sp != 0, &ws, &sm);
+      most = std::max(most, ws + sm);
+    }
+  *out_bytes = most;
   return DMUON_OK;
 }
 
@@ -974,7 +1083,9 @@ int dmuon_get_status(dmuon_handle_t h, int* flags, int n_flags) {
   const int n = (int)h->shapes.size();
   std::vector<int> f(n, 0);
   int err = 0;
-  e = cudaMemcpy(f.data(), h->d_flags, 4 * n, cudaMemcpyDeviceToHost);
+  std::vector<int> fp(n, 0);
+  e = cudaMemcpy(fp.data(), h->d_flags, 4 * n, cudaMemcpyDeviceToHost);
+  for (int k = 0; k < n; ++k) f[h->order[k]] = fp[k];  // plan order -> caller order
   if (e == cudaSuccess) e = cudaMemcpy(&err, h->d_err, 4, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(h->d_flags, 0, 4 * n);
   if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, 4);
@@ -1012,6 +1123,13 @@ int dmuon_set_overlap(dmuon_handle_t h, int on) {
   return DMUON_OK;
 }
 
+int dmuon_set_small_path(dmuon_handle_t h, int on) {
+  if (!h) return DMUON_ERR_ARG;
+  if (on && !h->small_ok) return DMUON_ERR_UNSUPPORTED;
+  h->small_path = on != 0;
+  return DMUON_OK;
+}
+
 int dmuon_set_tile_mode(dmuon_handle_t h, int mode) {
   if (!h || mode < 0 || mode > 2) return DMUON_ERR_ARG;
   if (mode == 2 && h->max_clusters <= 0) return DMUON_ERR_UNSUPPORTED;
@@ -1043,7 +1161,7 @@ int dmuon_profile_read(dmuon_handle_t h, double* ms, int64_t* count, int n_kinds
 int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len) {
   if (!h) return DMUON_ERR_ARG;
   std::string s;
-  char line[256];
+  char line[384];
   const int n = (int)h->shapes.size();
   std::snprintf(line, sizeof line, "device %d, %d SMs, %d 2-CTA clusters; matrices %d; tiles %s; ", h->device,
                 h->num_sms, h->max_clusters, n, h->plan_pair ? "256x256 CTA pairs" : "128x256 single CTAs");
@@ -1056,10 +1174,10 @@ int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len) {
       for (int q = 0; q < 3; ++q) it[q] += ch.L.items[q].size();
     }
     std::snprintf(line, sizeof line,
-                  "chunks %zu (<= %lld elements); momentum tiles %lld; items gram %zu gram2 %zu apply %zu; "
-                  "workspace %.3f GB + %.3f MB",
-                  h->chunks.size(), (long long)h->plan_chunk_elems, (long long)tiles, it[0], it[1], it[2],
-                  h->ws_bytes / 1e9, h->small_bytes / 1e6);
+                  "small-matrix kernel %zu; chunks %zu (<= %lld elements); momentum tiles %lld; "
+                  "items gram %zu gram2 %zu apply %zu; workspace %.3f GB + %.3f MB",
+                  h->small_descs.size(), h->chunks.size(), (long long)h->plan_chunk_elems, (long long)tiles,
+                  it[0], it[1], it[2], h->ws_bytes / 1e9, h->small_bytes / 1e6);
     s += line;
   } else {
     s += "no plan";

@@ -124,12 +124,14 @@ def test_newton_schulz_ragged_shapes(handle):
 @pytest.mark.parametrize("mode", [1, 2])
 def test_tile_modes_match_oracle(handle, mode):
     """Single-CTA 128x256 tiles (mode 1) and CTA-pair 256x256 tiles (mode 2)
-    both meet the bar on ragged shapes and a full step."""
+    both meet the bar on ragged shapes and a full step (the small-matrix
+    kernel off, so that the small shapes run through these tiles too)."""
     gen = torch.Generator().manual_seed(23)
     ins = [torch.randn(s, generator=gen) for s in RAGGED]
     outs = [torch.empty(s, device="cuda") for s in RAGGED]
     with dm.Handle(0) as h2:
         dm.dmuon_set_tile_mode(h2.h, mode)
+        dm.dmuon_set_small_path(h2.h, False)
         h2.newton_schulz(_to_dev(ins), outs)
         assert h2.status()[0] == 0
         assert (("pairs" in dm.dmuon_plan_summary(h2.h)) == (mode == 2))
