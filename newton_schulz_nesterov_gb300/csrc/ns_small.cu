@@ -18,9 +18,12 @@
 // K-major operand of X X^T (rows of X, K along columns) and the MN-major B
 // operand of B X (K along rows, N along columns); A and B are K-major.
 //
-// 128 threads: thread i owns row i (TMEM lane i) in every epilogue; thread 0
-// issues the MMAs (M = 128, fp32 accumulate, bf16 operands).  Every product
-// completes on one mbarrier with a bounded wait.
+// 256 threads (8 warps).  Streaming phases (momentum pass, update) use all
+// of them with several 16-byte loads in flight per thread.  In the
+// epilogues warp w reads TMEM lanes 32*(w%4).. (its rows) and takes half of
+// the columns (w/4).  Thread 0 issues the MMAs (M = 128, fp32 accumulate,
+// bf16 operands); every product completes on one mbarrier with a bounded
+// wait.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "small.cuh"
@@ -29,6 +32,9 @@ namespace dmuon {
 
 namespace {
 
+constexpr int kThreads = kSmallThreads;
+constexpr int kWarps = kThreads / 32;
+constexpr int kInFlight = 8;                          // 16-byte loads per array per thread
 constexpr uint64_t kSmallTimeoutNs = 4000000000ull;  // default product wait limit
 constexpr uint64_t kSmallDrainNs = 4000000000ull;    // drain after a timed-out wait
 
@@ -43,9 +49,22 @@ __device__ __forceinline__ uint32_t bf16_bits(float f) {
   return *reinterpret_cast<const uint16_t*>(&b);
 }
 
-__device__ __forceinline__ float bf16_at(const uint8_t* base, int row, int col) {
-  const uint16_t h = *reinterpret_cast<const uint16_t*>(base + swz(row, col));
-  return __uint_as_float((uint32_t)h << 16);
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) { return bf16_bits(lo) | (bf16_bits(hi) << 16); }
+
+// Eight consecutive bf16 of one row (col % 8 == 0): one 16-byte chunk.
+__device__ __forceinline__ void load8(const uint8_t* base, int row, int col, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(base + swz(row, col));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    f[2 * k] = __uint_as_float(w[k] << 16);
+    f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ void store8(uint8_t* base, int row, int col, const float (&f)[8]) {
+  *reinterpret_cast<uint4*>(base + swz(row, col)) =
+      make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
 }
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -130,29 +149,221 @@ __device__ bool run_product(const Product& p, uint32_t tmem, uint32_t bar, uint3
   return ok;
 }
 
-// Momentum, Nesterov input and sum of squares of one element; writes the
-// element of X0 = bf16(U) (or of U^T).
-struct MomCtx {
-  uint8_t* X;
-  int cols;
-  bool tr, ns_only, nesterov;
-  float mu;
-};
-
-__device__ __forceinline__ float mom_elem(const MomCtx& c, int e, float g, float m_old, float& m_new) {
-  float u;
-  if (c.ns_only) {
-    u = g;
-  } else {
-    m_new = fmaf(c.mu, m_old, g);
-    u = c.nesterov ? fmaf(c.mu, m_new, g) : m_new;
-  }
-  const int r = e / c.cols, col = e - r * c.cols;
-  *reinterpret_cast<uint16_t*>(c.X + (c.tr ? swz(col, r) : swz(r, col))) = (uint16_t)bf16_bits(u);
-  return u;
+// Momentum and Nesterov input of one element: returns U, writes the new
+// momentum to m_new (unless ns_only).
+__device__ __forceinline__ float mom_u(const SmallArgs& a, float g, float m_old, float& m_new) {
+  if (a.ns_only) return g;
+  m_new = fmaf(a.mu, m_old, g);
+  return a.nesterov ? fmaf(a.mu, m_new, g) : m_new;
 }
 
-__global__ void __launch_bounds__(128, 1) ns_small_kernel(const __grid_constant__ SmallArgs a) {
+// Momentum pass: M <- mu*M + G, U, X0 = bf16(U) (or U^T) into shared
+// memory.  Returns this thread's sum of U^2 (fixed order).  Rows of 4k
+// floats go as float4 (G, M, W are 16-byte aligned); (row, column) advance
+// incrementally, no division per element.
+__device__ float momentum_pass(const SmallArgs& a, const MatPtrs& p, uint8_t* X, int rows, int cols, bool tr) {
+  const int tid = threadIdx.x;
+  float ss = 0.f;
+  if ((cols & 3) == 0) {
+    const int c4n = cols >> 2, total4 = rows * c4n;
+    const int dr = kThreads / c4n, dc = kThreads % c4n;
+    int r = tid / c4n, c = tid % c4n;
+    const float4* G4 = reinterpret_cast<const float4*>(p.G);
+    float4* M4 = reinterpret_cast<float4*>(p.M);
+    for (int v0 = tid; v0 < total4; v0 += kInFlight * kThreads) {
+      float4 g[kInFlight], mo[kInFlight];
+      int rr[kInFlight], cc[kInFlight];
+#pragma unroll
+      for (int k = 0; k < kInFlight; ++k) {
+        const int v = v0 + k * kThreads;
+        rr[k] = r;
+        cc[k] = c;
+        g[k] = mo[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (v < total4) {
+          g[k] = G4[v];
+          if (!a.ns_only) mo[k] = M4[v];
+        }
+        r += dr;
+        c += dc;
+        if (c >= c4n) { c -= c4n; ++r; }
+      }
+#pragma unroll
+      for (int k = 0; k < kInFlight; ++k) {
+        const int v = v0 + k * kThreads;
+        if (v < total4) {
+          float4 mn = make_float4(0.f, 0.f, 0.f, 0.f);
+          const float u0 = mom_u(a, g[k].x, mo[k].x, mn.x);
+          const float u1 = mom_u(a, g[k].y, mo[k].y, mn.y);
+          const float u2 = mom_u(a, g[k].z, mo[k].z, mn.z);
+          const float u3 = mom_u(a, g[k].w, mo[k].w, mn.w);
+          if (!a.ns_only) M4[v] = mn;
+          ss = fmaf(u0, u0, ss);
+          ss = fmaf(u1, u1, ss);
+          ss = fmaf(u2, u2, ss);
+          ss = fmaf(u3, u3, ss);
+          const int col = 4 * cc[k];
+          if (!tr) {
+            *reinterpret_cast<uint2*>(X + swz(rr[k], col)) = make_uint2(pack_bf16(u0, u1), pack_bf16(u2, u3));
+          } else {
+            *reinterpret_cast<uint16_t*>(X + swz(col + 0, rr[k])) = (uint16_t)bf16_bits(u0);
+            *reinterpret_cast<uint16_t*>(X + swz(col + 1, rr[k])) = (uint16_t)bf16_bits(u1);
+            *reinterpret_cast<uint16_t*>(X + swz(col + 2, rr[k])) = (uint16_t)bf16_bits(u2);
+            *reinterpret_cast<uint16_t*>(X + swz(col + 3, rr[k])) = (uint16_t)bf16_bits(u3);
+          }
+        }
+      }
+    }
+  } else {
+    const int total = rows * cols;
+    const int dr = kThreads / cols, dc = kThreads % cols;
+    int r = tid / cols, c = tid % cols;
+    for (int e0 = tid; e0 < total; e0 += kInFlight * kThreads) {
+      float g[kInFlight], mo[kInFlight];
+      int rr[kInFlight], cc[kInFlight];
+#pragma unroll
+      for (int k = 0; k < kInFlight; ++k) {
+        const int e = e0 + k * kThreads;
+        rr[k] = r;
+        cc[k] = c;
+        g[k] = mo[k] = 0.f;
+        if (e < total) {
+          g[k] = p.G[e];
+          if (!a.ns_only) mo[k] = p.M[e];
+        }
+        r += dr;
+        c += dc;
+        if (c >= cols) { c -= cols; ++r; }
+      }
+#pragma unroll
+      for (int k = 0; k < kInFlight; ++k) {
+        const int e = e0 + k * kThreads;
+        if (e < total) {
+          float mn = 0.f;
+          const float u = mom_u(a, g[k], mo[k], mn);
+          if (!a.ns_only) p.M[e] = mn;
+          ss = fmaf(u, u, ss);
+          *reinterpret_cast<uint16_t*>(X + (tr ? swz(cc[k], rr[k]) : swz(rr[k], cc[k]))) = (uint16_t)bf16_bits(u);
+        }
+      }
+    }
+  }
+  return ss;
+}
+
+struct FinalCtx {
+  float ca, alpha, coef, decay;
+  int m, n, cols;
+  bool ns_only;
+};
+
+// Last iteration, transposed matrix (W is n x m): row `row` of O is column
+// `row` of W, so the lanes of a warp write neighbouring addresses.  Columns
+// [c_lo, c_hi) of this thread's half, 32 per TMEM load, W loads issued
+// before the stores.
+__device__ __forceinline__ void final_transposed(const FinalCtx& f, const uint8_t* X, float* W, uint32_t tq,
+                                                 int row, int c_lo, int c_hi) {
+  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+    uint32_t v[32];
+    ptx::tmem_ld32(tq + c0, v);
+    if (row < f.m) {
+      float w[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        w[j] = (!f.ns_only && c0 + j < f.n) ? W[(int64_t)(c0 + j) * f.cols + row] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        float x[8];
+        load8(X, row, c0 + j, x);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int cj = c0 + j + t;
+          if (cj < f.n) {
+            const float o = f.alpha * fmaf(f.ca, x[t], __uint_as_float(v[j + t]));
+            W[(int64_t)cj * f.cols + row] = f.ns_only ? o : fmaf(f.decay, w[j + t], -f.coef * o);
+          }
+        }
+      }
+    }
+  }
+}
+
+// Last iteration, row-major matrix: O goes through a 128 x 128 fp32 staging
+// tile (the A and B regions, free after the last product) with 16-byte
+// chunks swizzled by row, then whole rows of W are updated by one warp each
+// (coalesced 512-byte rows, 16 rows' loads in flight per warp).
+__device__ __forceinline__ void final_rows(const FinalCtx& f, const uint8_t* X, float* W, uint32_t tq, float* stg,
+                                           int row, int h, int n_pad) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool vec = (f.cols & 3) == 0;
+  for (int p0 = 0; p0 < n_pad; p0 += 128) {
+#pragma unroll
+    for (int hc = 0; hc < 64; hc += 32) {
+      const int c0 = p0 + 64 * h + hc;
+      if (c0 < n_pad) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tq + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          float x[8], o[8];
+          load8(X, row, c0 + j, x);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) o[t] = f.alpha * fmaf(f.ca, x[t], __uint_as_float(v[j + t]));
+          const int ch = (c0 - p0 + j) >> 2;
+          *reinterpret_cast<float4*>(stg + row * 128 + ((ch ^ (row & 31)) << 2)) = make_float4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<float4*>(stg + row * 128 + (((ch + 1) ^ (row & 31)) << 2)) =
+              make_float4(o[4], o[5], o[6], o[7]);
+        }
+      }
+    }
+    __syncthreads();
+    const int cl = p0 + 4 * lane;
+    float4 w[128 / kWarps];
+#pragma unroll
+    for (int k = 0; k < 128 / kWarps; ++k) {
+      const int r = warp + kWarps * k;
+      w[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!f.ns_only && r < f.m && cl < f.n) {
+        const float* src = W + (int64_t)r * f.cols + cl;
+        if (vec) {
+          w[k] = *reinterpret_cast<const float4*>(src);
+        } else {
+          w[k].x = src[0];
+          if (cl + 1 < f.n) w[k].y = src[1];
+          if (cl + 2 < f.n) w[k].z = src[2];
+          if (cl + 3 < f.n) w[k].w = src[3];
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 128 / kWarps; ++k) {
+      const int r = warp + kWarps * k;
+      if (r < f.m && cl < f.n) {
+        const float4 o = *reinterpret_cast<const float4*>(stg + r * 128 + ((lane ^ (r & 31)) << 2));
+        float4 u;
+        if (f.ns_only) {
+          u = o;
+        } else {
+          u.x = fmaf(f.decay, w[k].x, -f.coef * o.x);
+          u.y = fmaf(f.decay, w[k].y, -f.coef * o.y);
+          u.z = fmaf(f.decay, w[k].z, -f.coef * o.z);
+          u.w = fmaf(f.decay, w[k].w, -f.coef * o.w);
+        }
+        float* dst = W + (int64_t)r * f.cols + cl;
+        if (vec) {
+          *reinterpret_cast<float4*>(dst) = u;
+        } else {
+          dst[0] = u.x;
+          if (cl + 1 < f.n) dst[1] = u.y;
+          if (cl + 2 < f.n) dst[2] = u.z;
+          if (cl + 3 < f.n) dst[3] = u.w;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_constant__ SmallArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -161,90 +372,55 @@ __global__ void __launch_bounds__(128, 1) ns_small_kernel(const __grid_constant_
   uint8_t* B = A + 2 * kSmallBlockBytes;              // 128 x 128 bf16, 2 blocks
   uint64_t* bar = reinterpret_cast<uint64_t*>(B + 2 * kSmallBlockBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
-  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // 4 floats
+  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // kWarps floats
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = warp >> 2;                 // column half in the epilogues
+  const int row = 32 * (warp & 3) + lane;  // TMEM lane = row of X, A, B
   const SmallDesc d = a.descs[blockIdx.x];
   const MatPtrs p = a.ptrs[d.idx];
-  const int64_t rows = d.rows, cols = d.cols;
+  const int rows = (int)d.rows, cols = (int)d.cols;
   const bool tr = rows > cols;
-  const int m = (int)(tr ? cols : rows), n = (int)(tr ? rows : cols);
+  const int m = tr ? cols : rows, n = tr ? rows : cols;
   const int n_pad = (n + 63) & ~63;
+  const uint32_t tcols = n_pad <= 128 ? 128u : (n_pad <= 256 ? 256u : 512u);
 
   if (tid == 0) {
     ptx::mbar_init(ptx::smem_addr(bar), 1);
     ptx::fence_mbar_init();
   }
-  if (tid < 32) {
-    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), tcols);
     ptx::tmem_relinquish();
   }
-  // Zero X (padding rows/columns must read as zero), A and B.
-  for (int off = tid * 16; off < 12 * kSmallBlockBytes; off += 128 * 16)
+  // Zero the X blocks in use (padding rows/columns must read as zero); A and
+  // B are written whole by their epilogues before they are read.
+  for (int off = tid * 16; off < (n_pad >> 6) * kSmallBlockBytes; off += kThreads * 16)
     *reinterpret_cast<uint4*>(base + off) = make_uint4(0, 0, 0, 0);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   uint32_t phase = 0;
   bool ok = true;
 
-  // ---- momentum, Nesterov input, X0 = bf16(U or U^T), sum of squares.
-  // rows * cols <= 65536; G, M and W are 16-byte aligned (checked on the
-  // host), so the body runs on float4 with four loads of each in flight.
-  float ss = 0.f;
-  const int total = (int)(rows * cols);
-  const MomCtx mc{X, (int)cols, tr, a.ns_only != 0, a.nesterov != 0, a.mu};
-  {
-    const int nv = total >> 2;
-    const float4* G4 = reinterpret_cast<const float4*>(p.G);
-    float4* M4 = reinterpret_cast<float4*>(p.M);
-    for (int v0 = tid; v0 < nv; v0 += 4 * 128) {
-      float4 g[4], mo[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int v = v0 + q * 128;
-        if (v < nv) {
-          g[q] = G4[v];
-          mo[q] = a.ns_only ? make_float4(0.f, 0.f, 0.f, 0.f) : M4[v];
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int v = v0 + q * 128;
-        if (v < nv) {
-          float4 mn;
-          const float u0 = mom_elem(mc, 4 * v + 0, g[q].x, mo[q].x, mn.x);
-          const float u1 = mom_elem(mc, 4 * v + 1, g[q].y, mo[q].y, mn.y);
-          const float u2 = mom_elem(mc, 4 * v + 2, g[q].z, mo[q].z, mn.z);
-          const float u3 = mom_elem(mc, 4 * v + 3, g[q].w, mo[q].w, mn.w);
-          ss = fmaf(u0, u0, ss); ss = fmaf(u1, u1, ss); ss = fmaf(u2, u2, ss); ss = fmaf(u3, u3, ss);
-          if (!a.ns_only) M4[v] = mn;
-        }
-      }
-    }
-    for (int e = 4 * nv + tid; e < total; e += 128) {
-      float mn = 0.f;
-      const float u = mom_elem(mc, e, p.G[e], a.ns_only ? 0.f : p.M[e], mn);
-      ss = fmaf(u, u, ss);
-      if (!a.ns_only) p.M[e] = mn;
-    }
-  }
-  // fixed-order block sum
+  // ---- momentum, Nesterov input, X0, sum of squares (fixed order)
+  float ss = momentum_pass(a, p, X, rows, cols, tr);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  if (lane == 0) red[warp] = ss;
   fence_async_smem();
   __syncthreads();
-  const double tot = (double)red[0] + (double)red[1] + (double)red[2] + (double)red[3];
+  double tot = 0.0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) tot += (double)red[w];
   const bool finite = isfinite(tot);
   const float s = finite ? (float)(1.0 / (sqrt(tot) + (double)a.eps)) : 0.f;
   if (tid == 0 && !finite) a.flags[d.idx] |= 1;
 
   const uint32_t xs = ptx::smem_addr(X), as = ptx::smem_addr(A), bs = ptx::smem_addr(B);
   const uint32_t bar_a = ptx::smem_addr(bar);
-  const int i = tid;  // this thread's row (TMEM lane)
-  const uint32_t tq = tmem + ((uint32_t)((tid >> 5) * 32) << 16);
   const float coef = a.lr * d.scale;
   const uint64_t limit = a.timeout_ns ? a.timeout_ns : kSmallTimeoutNs;
 
@@ -252,22 +428,22 @@ __global__ void __launch_bounds__(128, 1) ns_small_kernel(const __grid_constant_
     const float ca = a.coeffs[k][0], cb = a.coeffs[k][1], cc = a.coeffs[k][2];
     const bool first = k == 0;
     const bool last = k == a.ns_steps - 1;
-    // A = X X^T (K = n_pad)
+    // A = X X^T (K = n_pad); the first iteration scales by s^2
     ok = run_product(Product{xs, xs, n_pad >> 6, false, 128}, tmem, bar_a, phase, a.err, limit);
     if (!ok) break;
     {
       const float alpha = first ? s * s : 1.f;
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+#pragma unroll
+      for (int hc = 0; hc < 64; hc += 32) {
+        const int c0 = 64 * h + hc;
         uint32_t v[32];
         ptx::tmem_ld32(tq + c0, v);
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
-          uint4 w;
-          w.x = bf16_bits(__uint_as_float(v[j]) * alpha) | (bf16_bits(__uint_as_float(v[j + 1]) * alpha) << 16);
-          w.y = bf16_bits(__uint_as_float(v[j + 2]) * alpha) | (bf16_bits(__uint_as_float(v[j + 3]) * alpha) << 16);
-          w.z = bf16_bits(__uint_as_float(v[j + 4]) * alpha) | (bf16_bits(__uint_as_float(v[j + 5]) * alpha) << 16);
-          w.w = bf16_bits(__uint_as_float(v[j + 6]) * alpha) | (bf16_bits(__uint_as_float(v[j + 7]) * alpha) << 16);
-          *reinterpret_cast<uint4*>(A + swz(i, c0 + j)) = w;
+          float o[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) o[t] = __uint_as_float(v[j + t]) * alpha;
+          store8(A, row, c0 + j, o);
         }
       }
     }
@@ -277,80 +453,48 @@ __global__ void __launch_bounds__(128, 1) ns_small_kernel(const __grid_constant_
     // B = b A + c A A (K = 128)
     ok = run_product(Product{as, as, 2, false, 128}, tmem, bar_a, phase, a.err, limit);
     if (!ok) break;
-    for (int c0 = 0; c0 < 128; c0 += 32) {
+#pragma unroll
+    for (int hc = 0; hc < 64; hc += 32) {
+      const int c0 = 64 * h + hc;
       uint32_t v[32];
       ptx::tmem_ld32(tq + c0, v);
 #pragma unroll
       for (int j = 0; j < 32; j += 8) {
-        uint32_t w[4];
+        float av[8], o[8];
+        load8(A, row, c0 + j, av);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int cj = c0 + j + 2 * q;
-          const float lo = fmaf(cc, __uint_as_float(v[j + 2 * q]), cb * bf16_at(A, i, cj));
-          const float hi = fmaf(cc, __uint_as_float(v[j + 2 * q + 1]), cb * bf16_at(A, i, cj + 1));
-          w[q] = bf16_bits(lo) | (bf16_bits(hi) << 16);
-        }
-        *reinterpret_cast<uint4*>(B + swz(i, c0 + j)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int t = 0; t < 8; ++t) o[t] = fmaf(cc, __uint_as_float(v[j + t]), cb * av[t]);
+        store8(B, row, c0 + j, o);
       }
     }
     ptx::tc_fence_before();
     fence_async_smem();
     __syncthreads();
-    // X' = a X + B X (M = 128, N = n_pad, K = 128; X as the MN-major operand)
+    // X' = a X + B X (M = 128, N = n_pad, K = 128; X as the MN-major operand);
+    // the first iteration scales by s
     ok = run_product(Product{bs, xs, 2, true, n_pad}, tmem, bar_a, phase, a.err, limit);
     if (!ok) break;
     const float alpha = first ? s : 1.f;
-    for (int c0 = 0; c0 < n_pad; c0 += 32) {
-      uint32_t v[32];
-      ptx::tmem_ld32(tq + c0, v);
-      if (!last) {
+    const int half = n_pad >> 1;
+    if (!last) {
+      for (int c0 = h * half; c0 < (h + 1) * half; c0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tq + c0, v);
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
-          uint32_t w[4];
+          float x[8];
+          load8(X, row, c0 + j, x);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int cj = c0 + j + 2 * q;
-            const float lo = alpha * fmaf(ca, bf16_at(X, i, cj), __uint_as_float(v[j + 2 * q]));
-            const float hi = alpha * fmaf(ca, bf16_at(X, i, cj + 1), __uint_as_float(v[j + 2 * q + 1]));
-            w[q] = bf16_bits(lo) | (bf16_bits(hi) << 16);
-          }
-          *reinterpret_cast<uint4*>(X + swz(i, c0 + j)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      } else if (i < m) {
-        // O = a X + B X in fp32, straight to W (or to the output).  Row i
-        // of O is row i of W (float4 read-modify-write when the row is
-        // 16-byte aligned) or column i of W (lanes write neighbours).
-        const bool vec = !tr && (cols & 3) == 0;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const int cj = c0 + j;
-          if (cj >= n) break;
-          float o[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) o[q] = alpha * fmaf(ca, bf16_at(X, i, cj + q), __uint_as_float(v[j + q]));
-          if (vec) {
-            float4* w4 = reinterpret_cast<float4*>(p.W + (int64_t)i * cols + cj);
-            float4 w = a.ns_only ? make_float4(0.f, 0.f, 0.f, 0.f) : *w4;
-            if (!a.ns_only) {
-              w.x = fmaf(a.decay, w.x, -coef * o[0]);
-              w.y = fmaf(a.decay, w.y, -coef * o[1]);
-              w.z = fmaf(a.decay, w.z, -coef * o[2]);
-              w.w = fmaf(a.decay, w.w, -coef * o[3]);
-            } else {
-              w = make_float4(o[0], o[1], o[2], o[3]);
-            }
-            *w4 = w;
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (cj + q < n) {
-                const int64_t off = tr ? (int64_t)(cj + q) * cols + i : (int64_t)i * cols + cj + q;
-                p.W[off] = a.ns_only ? o[q] : fmaf(a.decay, p.W[off], -coef * o[q]);
-              }
-            }
-          }
+          for (int t = 0; t < 8; ++t) x[t] = alpha * fmaf(ca, x[t], __uint_as_float(v[j + t]));
+          store8(X, row, c0 + j, x);
         }
       }
+    } else {
+      const FinalCtx f{ca, alpha, coef, a.decay, m, n, cols, a.ns_only != 0};
+      if (tr)
+        final_transposed(f, X, p.W, tq, row, h * half, (h + 1) * half);
+      else
+        final_rows(f, X, p.W, tq, reinterpret_cast<float*>(A), row, h, n_pad);
     }
     ptx::tc_fence_before();
     fence_async_smem();
@@ -358,19 +502,30 @@ __global__ void __launch_bounds__(128, 1) ns_small_kernel(const __grid_constant_
   }
   if (ok && a.ns_steps == 0) {
     // no iteration: O = s * U, with U recomputed in fp32 from G and the
-    // updated momentum (the same fused multiply-adds as above)
-    for (int e = tid; e < total; e += 128) {
-      const float g = p.G[e];
-      const float u = a.ns_only ? g : (a.nesterov ? fmaf(a.mu, p.M[e], g) : p.M[e]);
+    // updated momentum (the same fused multiply-adds as the momentum pass)
+    const int total = rows * cols, total4 = total >> 2;
+    const float4* G4 = reinterpret_cast<const float4*>(p.G);
+    const float4* M4 = reinterpret_cast<const float4*>(p.M);
+    float4* W4 = reinterpret_cast<float4*>(p.W);
+    auto upd = [&](float g, float mnew, float w) {
+      const float u = a.ns_only ? g : (a.nesterov ? fmaf(a.mu, mnew, g) : mnew);
       const float o = s * u;
-      p.W[e] = a.ns_only ? o : fmaf(a.decay, p.W[e], -coef * o);
+      return a.ns_only ? o : fmaf(a.decay, w, -coef * o);
+    };
+    for (int v = tid; v < total4; v += kThreads) {
+      const float4 g = G4[v];
+      const float4 mv = a.ns_only ? make_float4(0.f, 0.f, 0.f, 0.f) : M4[v];
+      const float4 w = a.ns_only ? make_float4(0.f, 0.f, 0.f, 0.f) : W4[v];
+      W4[v] = make_float4(upd(g.x, mv.x, w.x), upd(g.y, mv.y, w.y), upd(g.z, mv.z, w.z), upd(g.w, mv.w, w.w));
     }
+    for (int e = 4 * total4 + tid; e < total; e += kThreads)
+      p.W[e] = upd(p.G[e], a.ns_only ? 0.f : p.M[e], a.ns_only ? 0.f : p.W[e]);
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (tid < 32) {
+  if (warp == 0) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    ptx::tmem_dealloc(tmem, tcols);
   }
 }
 
@@ -381,7 +536,7 @@ cudaError_t small_configure() {
 }
 
 cudaError_t launch_small(const SmallArgs& a, int n_mats, cudaStream_t s) {
-  ns_small_kernel<<<n_mats, 128, kSmallSmem, s>>>(a);
+  ns_small_kernel<<<n_mats, kThreads, kSmallSmem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -12,6 +12,7 @@ namespace dmuon {
 constexpr int kSmallMaxM = 128;
 constexpr int kSmallMaxN = 512;
 constexpr int kSmallBlockBytes = 128 * 128;  // one 64-column block of 128 rows (bf16)
+constexpr int kSmallThreads = 256;
 constexpr int kSmallSmem = 1024 /*align slack*/ + 12 * kSmallBlockBytes + 256;
 
 struct SmallDesc {
