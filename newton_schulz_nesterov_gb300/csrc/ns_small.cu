@@ -7,7 +7,9 @@
 // 128 KB, A and B 32 KB each.
 //
 // DMuon "API Reference", section "direct_newton_schulz": per step
-//   A = X X^T,  B = b A + c A A,  X = a X + B X;
+//   A = X X^T,  B = b A + c A A,  X = a X + B X,
+// computed here as X = Z X with Z = a I + B stored in bf16 (the a X term
+// rides in the product; no epilogue pass over X is needed).
 // section "Muon": momentum and the Nesterov input; section
 // "gram_newton_schulz_factors": normaliser = Frobenius norm + eps under the
 // orientation rule.
@@ -104,10 +106,11 @@ __device__ __noinline__ bool small_wait(uint32_t bar, uint32_t parity, int* err,
 }
 
 // One product D[tmem] = sum over kb K blocks of A_kb * B_kb (16-wide K
-// steps), issued by thread 0.  Returns true, block-uniformly, once every
-// thread has seen it complete; false when a wait ran out, after the
-// product's MMAs have drained (bounded) so that TMEM and shared memory can
-// be released.
+// steps), issued by thread 0.  Returns true, block-uniformly, once the
+// product is complete (thread 0 saw its mbarrier phase, then a block
+// barrier and the tcgen05 after-sync fence order every thread's TMEM reads
+// after it); false when the wait ran out, after the product's MMAs have
+// drained (bounded) so that TMEM and shared memory can be released.
 struct Product {
   uint32_t a_base, b_base;   // shared addresses of the operands' block 0
   int k_blocks;              // 64-wide K blocks
@@ -117,33 +120,37 @@ struct Product {
 
 __device__ bool run_product(const Product& p, uint32_t tmem, uint32_t bar, uint32_t& phase, int* err,
                             uint64_t limit) {
+  bool ok = true;
   if (threadIdx.x == 0) {
     ptx::tc_fence_after();
+    // Descriptors are built once and advanced by their start-address field
+    // (16-byte units; every operand lies below 256 KB, so no carry leaves it).
+    const uint64_t a0 = ptx::desc_sw128(p.a_base, 16, 1024);
+    const uint64_t b0 = p.b_mn_major ? ptx::desc_sw128(p.b_base, kSmallBlockBytes, 1024)
+                                     : ptx::desc_sw128(p.b_base, 16, 1024);
     for (int n0 = 0; n0 < p.n; n0 += 256) {
       const int nn = min(256, p.n - n0);
       const uint32_t idesc = ptx::idesc_bf16(128, nn, p.b_mn_major ? 1 : 0);
+      // MN-major B (X): K rows kb*64 + kk*16 of every 64-column block from
+      // block n0/64; K-major B: rows 0..nn-1, K columns kb*64 + kk*16.
+      const uint64_t bn = b0 + (uint64_t)((n0 >> 6) * (kSmallBlockBytes >> 4));
       for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const uint64_t ak = a0 + (uint64_t)(kb * (kSmallBlockBytes >> 4));
+        const uint64_t bk = p.b_mn_major ? bn + (uint64_t)(kb * (64 * 128 >> 4))
+                                         : b0 + (uint64_t)(kb * (kSmallBlockBytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = ptx::desc_sw128(p.a_base + kb * kSmallBlockBytes + kk * 32, 16, 1024);
-          uint64_t bd;
-          if (p.b_mn_major)  // K rows kb*64 + kk*16 of every 64-column block of X
-            bd = ptx::desc_sw128(p.b_base + (n0 >> 6) * kSmallBlockBytes + (kb * 64 + kk * 16) * 128,
-                                 kSmallBlockBytes, 1024);
-          else               // rows 0..nn-1 of the B operand (K-major)
-            bd = ptx::desc_sw128(p.b_base + kb * kSmallBlockBytes + kk * 32, 16, 1024);
-          ptx::mma_bf16(tmem + n0, ad, bd, idesc, (kb | kk) != 0);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_bf16(tmem + n0, ak + 2 * kk, bk + (p.b_mn_major ? 128 * kk : 2 * kk), idesc, (kb | kk) != 0);
       }
     }
     ptx::mma_commit(bar);
+    // Only the issuing thread polls; the other warps sleep in the barrier
+    // below instead of taking issue slots.  On a timeout it drains the
+    // product's MMAs (bounded) before anyone releases TMEM.
+    ok = mbar_test(bar, phase) || small_wait(bar, phase, err, limit, true);
+    if (!ok) small_wait(bar, phase, err, kSmallDrainNs, false);
   }
-  bool ok = mbar_test(bar, phase) || small_wait(bar, phase, err, limit, true);
   ok = __syncthreads_and(ok) != 0;
-  if (!ok) {
-    if (threadIdx.x == 0) small_wait(bar, phase, err, kSmallDrainNs, false);
-    __syncthreads();
-  }
   phase ^= 1u;
   ptx::tc_fence_after();
   return ok;
@@ -251,7 +258,7 @@ __device__ float momentum_pass(const SmallArgs& a, const MatPtrs& p, uint8_t* X,
 }
 
 struct FinalCtx {
-  float ca, alpha, coef, decay;
+  float alpha, coef, decay;
   int m, n, cols;
   bool ns_only;
 };
@@ -260,8 +267,8 @@ struct FinalCtx {
 // `row` of W, so the lanes of a warp write neighbouring addresses.  Columns
 // [c_lo, c_hi) of this thread's half, 32 per TMEM load, W loads issued
 // before the stores.
-__device__ __forceinline__ void final_transposed(const FinalCtx& f, const uint8_t* X, float* W, uint32_t tq,
-                                                 int row, int c_lo, int c_hi) {
+__device__ __forceinline__ void final_transposed(const FinalCtx& f, float* W, uint32_t tq, int row, int c_lo,
+                                                 int c_hi) {
   for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
     uint32_t v[32];
     ptx::tmem_ld32(tq + c0, v);
@@ -271,16 +278,11 @@ __device__ __forceinline__ void final_transposed(const FinalCtx& f, const uint8_
       for (int j = 0; j < 32; ++j)
         w[j] = (!f.ns_only && c0 + j < f.n) ? W[(int64_t)(c0 + j) * f.cols + row] : 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        float x[8];
-        load8(X, row, c0 + j, x);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int cj = c0 + j + t;
-          if (cj < f.n) {
-            const float o = f.alpha * fmaf(f.ca, x[t], __uint_as_float(v[j + t]));
-            W[(int64_t)cj * f.cols + row] = f.ns_only ? o : fmaf(f.decay, w[j + t], -f.coef * o);
-          }
+      for (int j = 0; j < 32; ++j) {
+        const int cj = c0 + j;
+        if (cj < f.n) {
+          const float o = f.alpha * __uint_as_float(v[j]);
+          W[(int64_t)cj * f.cols + row] = f.ns_only ? o : fmaf(f.decay, w[j], -f.coef * o);
         }
       }
     }
@@ -291,8 +293,8 @@ __device__ __forceinline__ void final_transposed(const FinalCtx& f, const uint8_
 // tile (the A and B regions, free after the last product) with 16-byte
 // chunks swizzled by row, then whole rows of W are updated by one warp each
 // (coalesced 512-byte rows, 16 rows' loads in flight per warp).
-__device__ __forceinline__ void final_rows(const FinalCtx& f, const uint8_t* X, float* W, uint32_t tq, float* stg,
-                                           int row, int h, int n_pad) {
+__device__ __forceinline__ void final_rows(const FinalCtx& f, float* W, uint32_t tq, float* stg, int row, int h,
+                                           int n_pad) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool vec = (f.cols & 3) == 0;
   for (int p0 = 0; p0 < n_pad; p0 += 128) {
@@ -304,10 +306,9 @@ __device__ __forceinline__ void final_rows(const FinalCtx& f, const uint8_t* X, 
         ptx::tmem_ld32(tq + c0, v);
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
-          float x[8], o[8];
-          load8(X, row, c0 + j, x);
+          float o[8];
 #pragma unroll
-          for (int t = 0; t < 8; ++t) o[t] = f.alpha * fmaf(f.ca, x[t], __uint_as_float(v[j + t]));
+          for (int t = 0; t < 8; ++t) o[t] = f.alpha * __uint_as_float(v[j + t]);
           const int ch = (c0 - p0 + j) >> 2;
           *reinterpret_cast<float4*>(stg + row * 128 + ((ch ^ (row & 31)) << 2)) = make_float4(o[0], o[1], o[2], o[3]);
           *reinterpret_cast<float4*>(stg + row * 128 + (((ch + 1) ^ (row & 31)) << 2)) =
@@ -383,6 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
   const bool tr = rows > cols;
   const int m = tr ? cols : rows, n = tr ? rows : cols;
   const int n_pad = (n + 63) & ~63;
+  // m x m products are m_pad wide (64 or 128); their epilogues write all 128
+  // rows of columns < m_pad and nothing reads a column >= m_pad
+  const int m_pad = (m + 63) & ~63, hw = m_pad >> 1;
   const uint32_t tcols = n_pad <= 128 ? 128u : (n_pad <= 256 ? 256u : 512u);
 
   if (tid == 0) {
@@ -428,14 +432,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
     const float ca = a.coeffs[k][0], cb = a.coeffs[k][1], cc = a.coeffs[k][2];
     const bool first = k == 0;
     const bool last = k == a.ns_steps - 1;
-    // A = X X^T (K = n_pad); the first iteration scales by s^2
-    ok = run_product(Product{xs, xs, n_pad >> 6, false, 128}, tmem, bar_a, phase, a.err, limit);
+    // A = X X^T (N = m_pad, K = n_pad); the first iteration scales by s^2
+    ok = run_product(Product{xs, xs, n_pad >> 6, false, m_pad}, tmem, bar_a, phase, a.err, limit);
     if (!ok) break;
     {
       const float alpha = first ? s * s : 1.f;
-#pragma unroll
-      for (int hc = 0; hc < 64; hc += 32) {
-        const int c0 = 64 * h + hc;
+      for (int c0 = h * hw; c0 < (h + 1) * hw; c0 += 32) {
         uint32_t v[32];
         ptx::tmem_ld32(tq + c0, v);
 #pragma unroll
@@ -450,12 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
     ptx::tc_fence_before();
     fence_async_smem();
     __syncthreads();
-    // B = b A + c A A (K = 128)
-    ok = run_product(Product{as, as, 2, false, 128}, tmem, bar_a, phase, a.err, limit);
+    // Z = a I + b A + c A A (N = K = m_pad), stored where B lives
+    ok = run_product(Product{as, as, m_pad >> 6, false, m_pad}, tmem, bar_a, phase, a.err, limit);
     if (!ok) break;
-#pragma unroll
-    for (int hc = 0; hc < 64; hc += 32) {
-      const int c0 = 64 * h + hc;
+    for (int c0 = h * hw; c0 < (h + 1) * hw; c0 += 32) {
       uint32_t v[32];
       ptx::tmem_ld32(tq + c0, v);
 #pragma unroll
@@ -463,16 +463,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
         float av[8], o[8];
         load8(A, row, c0 + j, av);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) o[t] = fmaf(cc, __uint_as_float(v[j + t]), cb * av[t]);
+        for (int t = 0; t < 8; ++t)
+          o[t] = fmaf(cc, __uint_as_float(v[j + t]), cb * av[t]) + (c0 + j + t == row ? ca : 0.f);
         store8(B, row, c0 + j, o);
       }
     }
     ptx::tc_fence_before();
     fence_async_smem();
     __syncthreads();
-    // X' = a X + B X (M = 128, N = n_pad, K = 128; X as the MN-major operand);
+    // X' = Z X (M = 128, N = n_pad, K = m_pad; X as the MN-major operand);
     // the first iteration scales by s
-    ok = run_product(Product{bs, xs, 2, true, n_pad}, tmem, bar_a, phase, a.err, limit);
+    ok = run_product(Product{bs, xs, m_pad >> 6, true, n_pad}, tmem, bar_a, phase, a.err, limit);
     if (!ok) break;
     const float alpha = first ? s : 1.f;
     const int half = n_pad >> 1;
@@ -483,18 +484,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
           float x[8];
-          load8(X, row, c0 + j, x);
 #pragma unroll
-          for (int t = 0; t < 8; ++t) x[t] = alpha * fmaf(ca, x[t], __uint_as_float(v[j + t]));
+          for (int t = 0; t < 8; ++t) x[t] = alpha * __uint_as_float(v[j + t]);
           store8(X, row, c0 + j, x);
         }
       }
     } else {
-      const FinalCtx f{ca, alpha, coef, a.decay, m, n, cols, a.ns_only != 0};
+      const FinalCtx f{alpha, coef, a.decay, m, n, cols, a.ns_only != 0};
       if (tr)
-        final_transposed(f, X, p.W, tq, row, h * half, (h + 1) * half);
+        final_transposed(f, p.W, tq, row, h * half, (h + 1) * half);
       else
-        final_rows(f, X, p.W, tq, reinterpret_cast<float*>(A), row, h, n_pad);
+        final_rows(f, p.W, tq, reinterpret_cast<float*>(A), row, h, n_pad);
     }
     ptx::tc_fence_before();
     fence_async_smem();
