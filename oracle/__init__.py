@@ -35,7 +35,11 @@ rank-1 cases, and hand-computed momentum/update values.  Two readings are
 # oracle.aux_steps holds the fp64 AdamW and segmented-clipping oracle (the
 # other parts of Muon.step built here); it is pinned in
 # tests/test_oracle_aux_pins.py against hand values and PyTorch's routines.
+# oracle.gram holds the Gram-space Newton-Schulz backend with restarts,
+# pinned in tests/test_oracle_gram_pins.py to the direct oracle, the SVD
+# closed form and the structure of its factors.
 from . import aux_steps  # noqa: F401
+from . import gram  # noqa: F401
 from .step import (  # noqa: F401
     YOU_COEFFICIENTS,
     coefficient_rows,
