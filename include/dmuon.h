@@ -67,7 +67,22 @@ typedef struct {
     int64_t cols;
 } dmuon_shape_t;
 
-/* Options of a step; dmuon_default_opts() fills the pages' defaults. */
+/* Newton-Schulz backends (DMuon "API Reference", section "NewtonSchulz",
+ * argument backend).  DIRECT iterates on the m x n matrix (section
+ * "direct_newton_schulz"); GRAM iterates on its m x m Gram matrix with
+ * restarts (section "gram_newton_schulz"): per restart window
+ * R = X X^T, then per step Z = a I + b R + c R^2, Q <- Z Q, R <- Z R Z, and
+ * X <- Q X at each restart and at the end.  Same function in exact
+ * arithmetic; GRAM needs 3 m^2 n + 7 m^3 multiply-adds for five steps with
+ * one restart against 7.5 m^2 n + 2.5 m^3 for DIRECT (symmetric products
+ * count half), so it is cheaper whenever n > m.  GRAM keeps R and R Z in
+ * fp16 scaled by a power of two near m (at most 1024), Z and Q in fp16
+ * (bf16 for the Q X product); matrices taken by the small-matrix kernel
+ * (dmuon_set_small_path) run the direct iteration either way. */
+#define DMUON_BACKEND_DIRECT 0
+#define DMUON_BACKEND_GRAM   1
+
+/* Options of a step; dmuon_default_opts() fills the defaults. */
 typedef struct {
     float weight_decay;   /* Muon weight decay; default 0.0                */
     float eps;            /* normalisation epsilon; default 1e-7           */
@@ -77,13 +92,21 @@ typedef struct {
     const float* coeffs;  /* NULL: the YOU_COEFFICIENTS rows, last row
                            * repeated past five steps; else host memory of
                            * ns_steps rows of (a, b, c), row-major          */
+    int   backend;        /* DMUON_BACKEND_DIRECT (default) or _GRAM       */
+    const int* restarts;  /* GRAM: restart positions (host), a position k
+                           * starting a new window before step k (0-based);
+                           * positions outside (0, ns_steps) are ignored.
+                           * NULL = the pages' default {2}                  */
+    int   n_restarts;     /* entries of restarts (0..DMUON_MAX_NS_STEPS)   */
 } dmuon_opts_t;
 
 /* Opaque handle: owns the workspace, the plan cache and the status flags. */
 typedef struct dmuon_ctx* dmuon_handle_t;
 
 /* Fill *opts with the defaults (weight_decay 0, eps 1e-7, nesterov 1,
- * scale_mode 0, coeffs NULL).  No-op on NULL. */
+ * scale_mode 0, coeffs NULL, backend DIRECT, restarts NULL).  No-op on
+ * NULL.  The pages' own default backend is GRAM; DIRECT is the default
+ * here because it is the iteration the step is specified by. */
 void dmuon_default_opts(dmuon_opts_t* opts);
 
 /* Create a handle on CUDA device `device` (which becomes current for the
@@ -101,6 +124,11 @@ void dmuon_destroy(dmuon_handle_t h);
 int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats,
                           size_t* out_bytes);
 
+/* As dmuon_workspace_bytes for a backend: DMUON_BACKEND_GRAM plans hold
+ * X ping/pong plus seven m x m 16-bit buffers per matrix of the largest
+ * chunk.  DMUON_ERR_ARG for an unknown backend.  Host only. */
+int dmuon_workspace_bytes_ex(const dmuon_shape_t* shapes, int n_mats, int backend, size_t* out_bytes);
+
 /*
  * One owner-side Muon step over n_mats matrices (see the top of this file).
  *
@@ -111,7 +139,10 @@ int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats,
  *   params, grads, momentum, shapes: host arrays of n_mats entries.
  *   lr, mu      Muon learning rate and momentum coefficient.
  *   ns_steps    number of Newton-Schulz iterations, 0..DMUON_MAX_NS_STEPS.
- *   opts        NULL = defaults.
+ *   opts        NULL = defaults.  backend DMUON_BACKEND_GRAM selects the
+ *               Gram-space iteration (DMUON_ERR_ARG for coefficient rows
+ *               outside its fp16 range, see dmuon_gram_newton_schulz;
+ *               DMUON_ERR_UNSUPPORTED without 2-CTA clusters).
  *   stream      a cudaStream_t (NULL = legacy default stream).
  *
  * The caller owns all matrix memory; pointers must be 16-byte aligned and
@@ -143,6 +174,20 @@ int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs,
                         float* const* outputs, const dmuon_shape_t* shapes,
                         int n_mats, int ns_steps, const float* coeffs,
                         float eps, void* stream);
+
+/*
+ * Standalone Newton-Schulz with the Gram-space backend (DMuon "API
+ * Reference", section "gram_newton_schulz"): as dmuon_newton_schulz, with
+ * restart positions `restarts` (host, n_restarts entries; NULL = {2}).
+ * DMUON_ERR_ARG if a coefficient row has |a| + 2|b| + 4|c| > 40 or a
+ * restart window's gain prod |a| exceeds 8192 (the fp16 range of the
+ * Gram-space buffers); DMUON_ERR_UNSUPPORTED without 2-CTA clusters.
+ */
+int dmuon_gram_newton_schulz(dmuon_handle_t h, const float* const* inputs,
+                             float* const* outputs, const dmuon_shape_t* shapes,
+                             int n_mats, int ns_steps, const float* coeffs,
+                             const int* restarts, int n_restarts, float eps,
+                             void* stream);
 
 /*
  * AdamW on a list of flat fp32 tensors, in place (the non-Muon half of
@@ -296,7 +341,9 @@ int64_t dmuon_launch_count(dmuon_handle_t h);
 #define DMUON_KIND_ADAMW    6
 #define DMUON_KIND_CLIP     7
 #define DMUON_KIND_SMALL    8
-#define DMUON_NUM_KINDS     9
+#define DMUON_KIND_GS_GRAM  9   /* Gram backend: R = kappa s^2 X X^T        */
+#define DMUON_KIND_GS_PROD  10  /* Gram backend: m x m window products     */
+#define DMUON_NUM_KINDS     11
 int dmuon_profile_enable(dmuon_handle_t h, int on);
 int dmuon_profile_read(dmuon_handle_t h, double* ms, int64_t* count,
                        int n_kinds);

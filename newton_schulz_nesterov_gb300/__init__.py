@@ -16,6 +16,7 @@ __all__ = [
     "DmuonError", "load", "lib_path", "dmuon_create", "dmuon_destroy",
     "dmuon_step", "dmuon_step_ptrs", "dmuon_newton_schulz",
     "dmuon_newton_schulz_ptrs", "dmuon_newton_schulz_noalloc", "dmuon_get_status",
+    "dmuon_gram_newton_schulz", "dmuon_gram_newton_schulz_ptrs", "BACKENDS",
     "dmuon_adamw_step", "dmuon_adamw_step_ptrs", "dmuon_clip_grad_norm", "dmuon_clip_grad_norm_ptrs",
     "dmuon_workspace_bytes",
     "dmuon_launch_count", "dmuon_last_error", "dmuon_profile_enable", "dmuon_profile_read",
@@ -32,7 +33,8 @@ STATUS = {
     -4: "DMUON_ERR_CUDA", -5: "DMUON_ERR_NONFINITE", -6: "DMUON_ERR_TIMEOUT",
     -7: "DMUON_ERR_UNSUPPORTED",
 }
-KIND_NAMES = ("momentum", "finalize", "gram", "gram2", "apply", "update0", "adamw", "clip", "small")
+KIND_NAMES = ("momentum", "finalize", "gram", "gram2", "apply", "update0", "adamw", "clip", "small",
+              "gs_gram", "gs_prod")
 
 
 class DmuonError(RuntimeError):
@@ -51,7 +53,11 @@ class Shape(ctypes.Structure):
 class Opts(ctypes.Structure):
     _fields_ = [("weight_decay", ctypes.c_float), ("eps", ctypes.c_float),
                 ("nesterov", ctypes.c_int), ("scale_mode", ctypes.c_int),
-                ("coeffs", ctypes.POINTER(ctypes.c_float))]
+                ("coeffs", ctypes.POINTER(ctypes.c_float)), ("backend", ctypes.c_int),
+                ("restarts", ctypes.POINTER(ctypes.c_int)), ("n_restarts", ctypes.c_int)]
+
+
+BACKENDS = {"direct": 0, "gram": 1}
 
 
 def lib_path():
@@ -77,6 +83,12 @@ def load(path=None):
     L.dmuon_destroy.restype = None
     L.dmuon_workspace_bytes.argtypes = [ctypes.POINTER(Shape), i32, ctypes.POINTER(ctypes.c_size_t)]
     L.dmuon_workspace_bytes.restype = i32
+    L.dmuon_workspace_bytes_ex.argtypes = [ctypes.POINTER(Shape), i32, i32, ctypes.POINTER(ctypes.c_size_t)]
+    L.dmuon_workspace_bytes_ex.restype = i32
+    L.dmuon_gram_newton_schulz.argtypes = [vp, pp, pp, ctypes.POINTER(Shape), i32, i32,
+                                           ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int),
+                                           i32, f32, vp]
+    L.dmuon_gram_newton_schulz.restype = i32
     L.dmuon_step.argtypes = [vp, pp, pp, pp, ctypes.POINTER(Shape), i32, f32, f32, i32,
                              ctypes.POINTER(Opts), vp]
     L.dmuon_step.restype = i32
@@ -191,17 +203,27 @@ def dmuon_destroy(h):
         load().dmuon_destroy(h)
 
 
-def dmuon_workspace_bytes(shapes):
+def dmuon_workspace_bytes(shapes, backend="direct"):
     out = ctypes.c_size_t(0)
-    _check(load().dmuon_workspace_bytes(_shape_array(shapes), len(shapes), ctypes.byref(out)),
-           "dmuon_workspace_bytes")
+    _check(load().dmuon_workspace_bytes_ex(_shape_array(shapes), len(shapes), BACKENDS[backend],
+                                           ctypes.byref(out)), "dmuon_workspace_bytes")
     return out.value
+
+
+def _restart_array(restarts):
+    """None -> NULL (the default {2}); a sequence -> (int array, count)."""
+    if restarts is None:
+        return None, 0
+    rs = [int(k) for k in restarts]
+    return (ctypes.c_int * max(1, len(rs)))(*rs), len(rs)
 
 
 def dmuon_step_ptrs(h, w_ptrs, g_ptrs, m_ptrs, shapes, lr, mu, ns_steps=5,
                     weight_decay=0.0, eps=1e-7, nesterov=True, scale_mode=0,
-                    coeffs=None, stream=None, check=True):
-    """dmuon_step on raw device pointers; returns the status code."""
+                    coeffs=None, stream=None, check=True, backend="direct", restarts=None):
+    """dmuon_step on raw device pointers; returns the status code.
+    backend "gram" selects the Gram-space iteration with restart positions
+    `restarts` (None = the default [2])."""
     L = load()
     opts = Opts()
     L.dmuon_default_opts(ctypes.byref(opts))
@@ -209,6 +231,11 @@ def dmuon_step_ptrs(h, w_ptrs, g_ptrs, m_ptrs, shapes, lr, mu, ns_steps=5,
     opts.eps = float(eps)
     opts.nesterov = 1 if nesterov else 0
     opts.scale_mode = int(scale_mode)
+    opts.backend = BACKENDS[backend]
+    rarr, nr = _restart_array(restarts)
+    if rarr is not None:
+        opts.restarts = ctypes.cast(rarr, ctypes.POINTER(ctypes.c_int))
+        opts.n_restarts = nr
     carr = _coeff_array(coeffs)
     if carr is not None:
         opts.coeffs = ctypes.cast(carr, ctypes.POINTER(ctypes.c_float))
@@ -249,6 +276,31 @@ def dmuon_newton_schulz(h, inputs, outputs, ns_steps=5, coeffs=None, eps=1e-7, s
     if is_ != os_:
         raise ValueError("inputs and outputs must have matching shapes")
     return dmuon_newton_schulz_ptrs(h, ip, op, is_, ns_steps, coeffs, eps, stream)
+
+
+def dmuon_gram_newton_schulz_ptrs(h, in_ptrs, out_ptrs, shapes, ns_steps=5, coeffs=None, restarts=None,
+                                  eps=1e-7, stream=None, check=True):
+    L = load()
+    carr = _coeff_array(coeffs)
+    rarr, nr = _restart_array(restarts)
+    rc = L.dmuon_gram_newton_schulz(
+        h, _ptr_array(in_ptrs), _ptr_array(out_ptrs), _shape_array(shapes), len(shapes), int(ns_steps),
+        None if carr is None else ctypes.cast(carr, ctypes.POINTER(ctypes.c_float)),
+        None if rarr is None else ctypes.cast(rarr, ctypes.POINTER(ctypes.c_int)), nr, float(eps),
+        ctypes.c_void_p(_stream_handle(stream)))
+    if check:
+        _check(rc, "dmuon_gram_newton_schulz", h)
+    return rc
+
+
+def dmuon_gram_newton_schulz(h, inputs, outputs, ns_steps=5, coeffs=None, restarts=None, eps=1e-7,
+                             stream=None):
+    """Standalone Newton-Schulz with the Gram-space backend."""
+    ip, is_ = _tensor_args(inputs, "inputs")
+    op, os_ = _tensor_args(outputs, "outputs")
+    if is_ != os_:
+        raise ValueError("inputs and outputs must have matching shapes")
+    return dmuon_gram_newton_schulz_ptrs(h, ip, op, is_, ns_steps, coeffs, restarts, eps, stream)
 
 
 def dmuon_newton_schulz_noalloc(input_ptr, output_ptr, rows, cols, ns_steps=5, coeffs=None,
@@ -410,6 +462,10 @@ class Handle:
 
     def newton_schulz(self, inputs, outputs, ns_steps=5, coeffs=None, eps=1e-7, stream=None):
         return dmuon_newton_schulz(self.h, inputs, outputs, ns_steps, coeffs, eps, stream)
+
+    def gram_newton_schulz(self, inputs, outputs, ns_steps=5, coeffs=None, restarts=None, eps=1e-7,
+                           stream=None):
+        return dmuon_gram_newton_schulz(self.h, inputs, outputs, ns_steps, coeffs, restarts, eps, stream)
 
     def status(self, n_flags=0):
         return dmuon_get_status(self.h, n_flags)

@@ -27,6 +27,7 @@
 #include "../../include/dmuon.h"
 #include "aux.cuh"
 #include "common.cuh"
+#include "gram.cuh"
 #include "small.cuh"
 
 using namespace dmuon;
@@ -70,14 +71,16 @@ bool get_encoder() {
   return g_encode != nullptr;
 }
 
-// bf16 row-major rows x cols with leading dimension ld (elements): 64x64
-// boxes, 128-byte swizzle, zero fill outside the matrix.
-bool encode_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld) {
+// 16-bit (bf16 by default, else fp16) row-major rows x cols with leading
+// dimension ld (elements): 64x64 boxes, 128-byte swizzle, zero fill outside
+// the matrix.
+bool encode_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld, bool fp16 = false) {
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
   cuuint32_t box[2] = {(cuuint32_t)kBox, (cuuint32_t)kBox};
   cuuint32_t estr[2] = {1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+  return g_encode(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                  strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -85,15 +88,20 @@ bool encode_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_
 struct Layout {
   std::vector<MatDesc> mats;       // device pointers filled in once allocated
   std::vector<int64_t> xoff, aoff, boff;  // workspace byte offsets
+  std::vector<int64_t> goff;       // Gram-space buffers: kGramBufs per matrix (gram plans)
   std::vector<int64_t> tile_prefix;
   size_t ws_bytes = 0;             // big bf16 workspace
   size_t small_bytes = 0;          // descriptors, maps, lists, partials
   std::vector<int4> items[3];
 };
 
-void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair) {
+// Workspace of a chunk.  Direct plans: X[0], X[1] (m x n bf16), A, B
+// (m x m bf16) per matrix.  Gram plans: X[0], X[1] and the kGramBufs m x m
+// buffers of the Gram-space window (R[2], B, T, Q[2] fp16; Q bf16).
+void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair, bool gram = false) {
   L.mats.assign(n, MatDesc{});
   L.xoff.resize(n); L.aoff.resize(n); L.boff.resize(n);
+  L.goff.assign(gram ? (size_t)n * kGramBufs : 0, 0);
   L.tile_prefix.assign(n + 1, 0);
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off += (size_t)rup((int64_t)bytes, 256); return (int64_t)o; };
@@ -107,8 +115,13 @@ void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair) {
     d.ldx = rup(d.n, 8);
     d.lda = rup(d.m, 8);
     L.xoff[i] = take((size_t)(2 * d.m * d.ldx * 2));  // X[0] and X[1] back to back
-    L.aoff[i] = take((size_t)(d.m * d.lda * 2));
-    L.boff[i] = take((size_t)(d.m * d.lda * 2));
+    if (gram) {
+      for (int b = 0; b < kGramBufs; ++b) L.goff[(size_t)i * kGramBufs + b] = take((size_t)(d.m * d.lda * 2));
+      L.aoff[i] = L.boff[i] = L.goff[(size_t)i * kGramBufs + kGbQb];
+    } else {
+      L.aoff[i] = take((size_t)(d.m * d.lda * 2));
+      L.boff[i] = take((size_t)(d.m * d.lda * 2));
+    }
     d.tiles_c = (int32_t)cdiv(d.cols, kMomTile);
     d.tile0 = L.tile_prefix[i];
     L.tile_prefix[i + 1] = L.tile_prefix[i] + cdiv(d.rows, kMomTile) * d.tiles_c;
@@ -176,6 +189,8 @@ struct Chunk {
   float* d_partials = nullptr;
   float* d_svec = nullptr;
   int4* d_items[3] = {nullptr, nullptr, nullptr};
+  GramDesc* d_gd = nullptr;       // gram plans: per-matrix Gram-space buffers
+  CUtensorMap* d_gmaps = nullptr; // gram plans: kGramBufs maps per matrix
 };
 
 struct dmuon_ctx {
@@ -190,6 +205,8 @@ struct dmuon_ctx {
   bool small_path = true;              // requested
   bool small_ok = false;               // small kernel configured on this device
   bool plan_small = false;             // small kernel used by the current plan
+  bool plan_gram = false;              // chunks laid out for the Gram-space backend
+  bool gram_ok = false;                // Gram-space kernels configured on this device
   std::vector<Chunk> chunks;
   size_t ws_bytes = 0, small_bytes = 0;
   void* ws = nullptr;
@@ -277,8 +294,10 @@ void free_plan(dmuon_ctx* h) {
 // CTA pairs unless single CTAs are requested, pairs are unavailable, or (in
 // automatic mode) every short side fits one 128-row tile, where a pair's
 // second CTA would only compute padding.
-bool use_pairs(const dmuon_ctx* h, const dmuon_shape_t* s, int n) {
-  if (h->max_clusters <= 0 || h->tile_mode == 1) return false;
+bool use_pairs(const dmuon_ctx* h, const dmuon_shape_t* s, int n, bool gram = false) {
+  if (h->max_clusters <= 0) return false;
+  if (gram) return true;  // the Gram-space kernels exist for CTA pairs only
+  if (h->tile_mode == 1) return false;
   if (h->tile_mode == 2) return true;
   for (int i = 0; i < n; ++i)
     if (std::min(s[i].rows, s[i].cols) > kBM) return true;
@@ -287,8 +306,9 @@ bool use_pairs(const dmuon_ctx* h, const dmuon_shape_t* s, int n) {
 
 int64_t chunk_limit(const dmuon_ctx* h) { return h->chunk_elems > 0 ? h->chunk_elems : kDefaultChunkElems; }
 
-bool same_shapes(const dmuon_ctx* h, const dmuon_shape_t* s, int n) {
-  if ((int)h->shapes.size() != n || !h->small || h->plan_pair != use_pairs(h, s, n) ||
+bool same_shapes(const dmuon_ctx* h, const dmuon_shape_t* s, int n, bool gram = false) {
+  if ((int)h->shapes.size() != n || !h->small || h->plan_pair != use_pairs(h, s, n, gram) ||
+      h->plan_gram != gram ||
       h->plan_small != (h->small_path && h->small_ok) ||
       h->plan_chunk_elems != chunk_limit(h) || h->plan_overlap != (h->overlap && h->chunks.size() > 1))
     return false;
@@ -319,9 +339,20 @@ std::vector<std::pair<int, int>> split_chunks(const dmuon_shape_t* shapes, int n
 // Bytes of one chunk's device arrays (descriptors, maps, prefix, partials,
 // scale vector, work lists).
 size_t chunk_small_bytes(const Layout& L, int n) {
+  const bool gram = !L.goff.empty();
   return rup(sizeof(MatDesc) * n, 256) + rup(sizeof(CUtensorMap) * kMapsPerMat * n, 256) +
          rup(8 * (n + 1), 256) + rup(4 * L.tile_prefix[n], 256) + rup(4 * n, 256) +
-         rup(16 * L.items[0].size(), 256) + rup(16 * L.items[1].size(), 256) + rup(16 * L.items[2].size(), 256);
+         rup(16 * L.items[0].size(), 256) + rup(16 * L.items[1].size(), 256) + rup(16 * L.items[2].size(), 256) +
+         (gram ? rup(sizeof(GramDesc) * n, 256) + rup(sizeof(CUtensorMap) * kGramBufs * n, 256) : 0);
+}
+
+// Power-of-two scale of the Gram-space R and R Z of an m x m window: near m
+// (entries of R are ~1/m), at most 1024 so that kappa * |R Z| stays well
+// inside fp16 for coefficient rows with |a| + 2|b| + 4|c| <= 40.
+float gram_kappa(int64_t m) {
+  float k = 1.f;
+  while (k * 2.f <= (float)std::min<int64_t>(m, 1024)) k *= 2.f;
+  return k;
 }
 
 // Plan order: positions [0, n_large) hold the matrices run by the chunked
@@ -339,7 +370,7 @@ int plan_order(const dmuon_shape_t* shapes, int n, bool small_path, std::vector<
 // Host-side plan sizes (no device work): workspace of the largest chunk and
 // all device arrays.
 void plan_sizes(const dmuon_shape_t* shapes, int n, bool pair, int64_t limit, bool small_path, size_t* ws,
-                size_t* small) {
+                size_t* small, bool gram = false) {
   std::vector<int> order;
   const int n_large = plan_order(shapes, n, small_path, order);
   std::vector<dmuon_shape_t> ps(n);
@@ -349,17 +380,20 @@ void plan_sizes(const dmuon_shape_t* shapes, int n, bool pair, int64_t limit, bo
            rup(sizeof(SmallDesc) * (n - n_large), 256);
   for (const auto& c : split_chunks(ps.data(), n_large, limit)) {
     Layout L;
-    make_layout(ps.data() + c.first, c.second, L, pair);
+    make_layout(ps.data() + c.first, c.second, L, pair, gram);
     *ws = std::max(*ws, L.ws_bytes);
     *small += chunk_small_bytes(L, c.second);
   }
 }
 
-int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
-  if (same_shapes(h, shapes, n)) return DMUON_OK;
+int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
+  if (same_shapes(h, shapes, n, gram)) return DMUON_OK;
   free_plan(h);
   if (!get_encoder()) return fail(h, DMUON_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
-  h->plan_pair = use_pairs(h, shapes, n);
+  if (gram && (h->max_clusters <= 0 || !h->gram_ok))
+    return fail(h, DMUON_ERR_UNSUPPORTED, "Gram-space backend needs 2-CTA clusters, unavailable on this device");
+  h->plan_gram = gram;
+  h->plan_pair = use_pairs(h, shapes, n, gram);
   h->plan_chunk_elems = chunk_limit(h);
   h->plan_small = h->small_path && h->small_ok;
   h->n_large = plan_order(shapes, n, h->plan_small, h->order);
@@ -378,7 +412,7 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
     Chunk& ch = h->chunks[c];
     ch.i0 = parts[c].first;
     ch.n = parts[c].second;
-    make_layout(ps.data() + ch.i0, ch.n, ch.L, h->plan_pair);
+    make_layout(ps.data() + ch.i0, ch.n, ch.L, h->plan_pair, gram);
     h->ws_bytes = std::max(h->ws_bytes, ch.L.ws_bytes);
     h->small_bytes += chunk_small_bytes(ch.L, ch.n);
   }
@@ -410,7 +444,13 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
     ch.d_partials = (float*)carve(4 * L.tile_prefix[cn]);
     ch.d_svec = (float*)carve(4 * cn);
     for (int q = 0; q < 3; ++q) ch.d_items[q] = (int4*)carve(16 * L.items[q].size());
+    if (gram) {
+      ch.d_gd = (GramDesc*)carve(sizeof(GramDesc) * cn);
+      ch.d_gmaps = (CUtensorMap*)carve(sizeof(CUtensorMap) * kGramBufs * cn);
+    }
     std::vector<CUtensorMap> maps(kMapsPerMat * (size_t)cn);
+    std::vector<CUtensorMap> gmaps(gram ? kGramBufs * (size_t)cn : 0);
+    std::vector<GramDesc> gds(gram ? cn : 0);
     for (int i = 0; i < cn; ++i) {
       MatDesc& d = L.mats[i];
       d.X[0] = (__nv_bfloat16*)(ws + L.xoff[i]);
@@ -422,6 +462,19 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
                 encode_map(&maps[kMapsPerMat * i + 1], d.X[1], d.m, d.n, d.ldx) &&
                 encode_map(&maps[kMapsPerMat * i + 2], d.A, d.m, d.m, d.lda) &&
                 encode_map(&maps[kMapsPerMat * i + 3], d.B, d.m, d.m, d.lda);
+      if (gram) {
+        // Gram plans: A and B above both name the bf16 Q buffer, so the
+        // direct Apply kernel computes Q X.
+        GramDesc& gd = gds[i];
+        gd.m = d.m;
+        gd.ld = d.lda;
+        gd.kappa = gram_kappa(d.m);
+        gd.inv_kappa = 1.f / gd.kappa;
+        for (int b = 0; b < kGramBufs && ok; ++b) {
+          gd.buf[b] = (uint16_t*)(ws + L.goff[(size_t)i * kGramBufs + b]);
+          ok = encode_map(&gmaps[kGramBufs * i + b], gd.buf[b], d.m, d.m, d.lda, b != kGbQb);
+        }
+      }
       if (!ok) {
         char what[160];
         std::snprintf(what, sizeof what, "cuTensorMapEncodeTiled failed for matrix %d (%lld x %lld)",
@@ -434,6 +487,9 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n) {
     e = cudaMemcpy(ch.d_mats, L.mats.data(), sizeof(MatDesc) * cn, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(ch.d_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(ch.d_prefix, L.tile_prefix.data(), 8 * (cn + 1), cudaMemcpyHostToDevice);
+    if (gram && e == cudaSuccess) e = cudaMemcpy(ch.d_gd, gds.data(), sizeof(GramDesc) * cn, cudaMemcpyHostToDevice);
+    if (gram && e == cudaSuccess)
+      e = cudaMemcpy(ch.d_gmaps, gmaps.data(), sizeof(CUtensorMap) * gmaps.size(), cudaMemcpyHostToDevice);
     for (int q = 0; q < 3 && e == cudaSuccess; ++q)
       if (!L.items[q].empty()) e = cudaMemcpy(ch.d_items[q], L.items[q].data(), 16 * L.items[q].size(), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) { free_plan(h); return fail(h, cuda_err(e), "plan upload", e); }
@@ -654,10 +710,155 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
   return DMUON_OK;
 }
 
+// Restart windows [start, end) of ns_steps steps: positions outside
+// (0, ns_steps) start no window; duplicates collapse.
+std::vector<std::pair<int, int>> restart_windows(int ns_steps, const std::vector<int>& restarts) {
+  std::vector<int> cuts;
+  for (int k : restarts)
+    if (k > 0 && k < ns_steps) cuts.push_back(k);
+  std::sort(cuts.begin(), cuts.end());
+  cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
+  std::vector<std::pair<int, int>> w;
+  int start = 0;
+  for (int k : cuts) { w.push_back({start, k}); start = k; }
+  if (ns_steps > start) w.push_back({start, ns_steps});
+  return w;
+}
+
+// Newton-Schulz of a chunk with the Gram-space backend and the update.
+// Per window: R~ = kappa s^2 X X^T, then per step Z (copied to Q at the
+// window's first step), Q' = Z Q (later steps), W~ = R~ Z and R~' = Z W~
+// (all but the window's last step); between windows and at the end the
+// direct Apply kernel forms Q X (a = 0), the last one updating W (or
+// writing O).
+int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, int ns_steps,
+                   const float* coeffs, float wd, int ns_only, const std::vector<int>& restarts,
+                   cudaStream_t stream) {
+  const Layout& L = ch.L;
+  const int n = ch.n;
+  const int64_t nt = L.tile_prefix[n];
+  cudaError_t e;
+  const float decay = 1.f - lr * wd;
+  if (ns_steps == 0) {
+    Update0Args a{ch.d_mats, dptrs, ch.d_prefix, n, nt, ch.d_svec, lr, decay, ns_only};
+    const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
+    LaunchGuard g(h, stream, DMUON_KIND_UPDATE0);
+    if ((e = launch_update0(a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "update0 launch", e);
+    return DMUON_OK;
+  }
+  const int n_gram = (int)L.items[kPhaseGram].size(), n_prod = (int)L.items[kPhaseGram2].size();
+  auto prod = [&](GramArgs a, bool x_operand, int kind) -> int {
+    a.gd = ch.d_gd;
+    a.mats = ch.d_mats;
+    a.xmaps = ch.d_maps;
+    a.gmaps = ch.d_gmaps;
+    a.x_operand = x_operand ? 1 : 0;
+    a.items = ch.d_items[x_operand ? kPhaseGram : kPhaseGram2];
+    a.n_items = x_operand ? n_gram : n_prod;
+    a.svec = ch.d_svec;
+    a.err = h->d_err;
+    a.timeout_ns = h->wait_timeout_ns;
+    if (a.n_items <= 0) return DMUON_OK;
+    LaunchGuard g(h, stream, kind);
+    const cudaError_t ee = launch_gram_pair(a, std::min(a.n_items, h->max_clusters), stream);
+    return ee == cudaSuccess ? DMUON_OK : fail(h, cuda_err(ee), "ns_gram_pair launch", ee);
+  };
+  auto apply = [&](int src, bool first, int mode) -> int {
+    GemmArgs a{};
+    a.mats = ch.d_mats;
+    a.ptrs = dptrs;
+    a.tmaps = ch.d_maps;
+    a.items = ch.d_items[kPhaseApply];
+    a.n_items = (int)L.items[kPhaseApply].size();
+    a.src = src;
+    a.ca = 0.f;          // X' = Q X
+    a.first = first;     // the first window's X is U unnormalised: times s
+    a.final_mode = mode;
+    a.lr = lr;
+    a.decay = decay;
+    a.svec = ch.d_svec;
+    a.err = h->d_err;
+    a.timeout_ns = h->wait_timeout_ns;
+    if (a.n_items <= 0) return DMUON_OK;
+    LaunchGuard g(h, stream, DMUON_KIND_APPLY);
+    const cudaError_t ee = launch_gemm_pair(kPhaseApply, a, std::min(a.n_items, h->max_clusters), stream);
+    return ee == cudaSuccess ? DMUON_OK : fail(h, cuda_err(ee), "ns_gemm_pair launch", ee);
+  };
+  auto blank = []() {
+    GramArgs a{};
+    a.out2 = a.add1 = -1;
+    a.g0 = 1.f;
+    return a;
+  };
+  const auto windows = restart_windows(ns_steps, restarts);
+  int src = 0;
+  bool first = true;
+  int rc;
+  for (size_t wi = 0; wi < windows.size(); ++wi) {
+    if (wi > 0) {  // restart: X <- Q X, then a new window from the explicit iterate
+      if ((rc = apply(src, first, kWriteX))) return rc;
+      src ^= 1;
+      first = false;
+    }
+    {  // R~ = kappa s^2 X X^T (s only while X is still unnormalised)
+      GramArgs a = blank();
+      a.src = src;
+      a.out = kGbR0;
+      a.gpow = 1;
+      a.use_s2 = first ? 1 : 0;
+      if ((rc = prod(a, true, DMUON_KIND_GS_GRAM))) return rc;
+    }
+    int rc_ = kGbR0, qc = kGbQ0;
+    for (int k = windows[wi].first; k < windows[wi].second; ++k) {
+      const float* row = coeffs ? coeffs + 3 * k : kYouCoefficients[std::min(k, 4)];
+      const bool wfirst = k == windows[wi].first, wlast = k == windows[wi].second - 1;
+      {  // Z = a I + (b/kappa) R~ + (c/kappa^2) R~ R~; at the window's first step also Q = Z
+        GramArgs a = blank();
+        a.opA = a.opB = rc_;
+        a.out = kGbZ;
+        a.g0 = row[2];
+        a.gpow = -2;
+        a.add1 = rc_;
+        a.c1 = row[1];
+        a.p1pow = -1;
+        a.diag = row[0];
+        if (wfirst) {
+          a.out2 = wlast ? kGbQb : qc;
+          a.out2_bf16 = wlast ? 1 : 0;
+        }
+        if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
+      }
+      if (!wfirst) {  // Q' = Z Q
+        GramArgs a = blank();
+        a.opA = kGbZ;
+        a.opB = qc;
+        a.out = wlast ? kGbQb : (qc ^ kGbQ0 ^ kGbQ1);
+        a.out_bf16 = wlast ? 1 : 0;
+        if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
+        if (!wlast) qc ^= kGbQ0 ^ kGbQ1;
+      }
+      if (!wlast) {
+        GramArgs a = blank();  // W~ = R~ Z
+        a.opA = rc_;
+        a.opB = kGbZ;
+        a.out = kGbW;
+        if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
+        GramArgs r = blank();  // R~' = Z W~
+        r.opA = kGbZ;
+        r.opB = kGbW;
+        r.out = rc_ ^ kGbR0 ^ kGbR1;
+        if ((rc = prod(r, false, DMUON_KIND_GS_PROD))) return rc;
+        rc_ ^= kGbR0 ^ kGbR1;
+      }
+    }
+  }
+  return apply(src, first, ns_only ? kWriteO : kUpdateW);
+}
+
 // Shared by dmuon_step (ns_only = 0) and dmuon_newton_schulz (ns_only = 1).
 int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, float lr, float mu,
         int ns_steps, const float* coeffs, float eps, float wd, int nesterov, int scale_mode,
-        int ns_only, cudaStream_t stream) {
+        int ns_only, cudaStream_t stream, bool gram = false, const std::vector<int>& restarts = {}) {
   if (cudaSetDevice(h->device) != cudaSuccess) return fail(h, DMUON_ERR_CUDA, "cudaSetDevice");
   // Under stream capture nothing may allocate, upload or synchronise: the
   // plan, the update scales and the pointer set must already exist from an
@@ -665,9 +866,9 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return fail(h, DMUON_ERR_CUDA, "cudaStreamIsCapturing");
   const bool capturing = cap != cudaStreamCaptureStatusNone;
-  if (capturing && !same_shapes(h, shapes, n))
+  if (capturing && !same_shapes(h, shapes, n, gram))
     return fail(h, DMUON_ERR_ARG, "stream capture: call once with these shapes before capturing");
-  int rc = build_plan(h, shapes, n);
+  int rc = build_plan(h, shapes, n, gram);
   if (rc) return rc;
 
   // Per-matrix update scale depends on the mode: refresh descriptors when
@@ -762,10 +963,14 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
       return fail(h, cuda_err(e), "ns_small launch", e);
   }
 
+  auto chunk_ns = [&](const Chunk& ch, cudaStream_t st) {
+    return h->plan_gram ? run_chunk_gram(h, ch, dptrs + ch.i0, lr, ns_steps, coeffs, wd, ns_only, restarts, st)
+                        : run_chunk_ns(h, ch, dptrs + ch.i0, lr, ns_steps, coeffs, wd, ns_only, st);
+  };
   if (!h->plan_overlap) {
     for (const Chunk& ch : h->chunks) {
       if ((rc = run_chunk_norm(h, ch, dptrs + ch.i0, mu, eps, nesterov, ns_only, stream))) return rc;
-      if ((rc = run_chunk_ns(h, ch, dptrs + ch.i0, lr, ns_steps, coeffs, wd, ns_only, stream))) return rc;
+      if ((rc = chunk_ns(ch, stream))) return rc;
     }
     return DMUON_OK;
   }
@@ -785,7 +990,7 @@ int run(dmuon_ctx* h, const MatPtrs* ptrs, const dmuon_shape_t* shapes, int n, f
     if ((e = cudaEventRecord(h->ev_norm[b], h->side)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(stream, h->ev_norm[b], 0)) != cudaSuccess)
       return fail(h, cuda_err(e), "overlap hand-off", e);
-    if ((rc = run_chunk_ns(h, ch, dptrs + ch.i0, lr, ns_steps, coeffs, wd, ns_only, stream))) return rc;
+    if ((rc = chunk_ns(ch, stream))) return rc;
     if ((e = cudaEventRecord(h->ev_gemm[b], stream)) != cudaSuccess)
       return fail(h, cuda_err(e), "overlap record", e);
   }
@@ -801,6 +1006,34 @@ bool finite3(const float* c, int rows) {
   return true;
 }
 
+// Gram-space backend: restart positions (NULL = the pages' default {2}) and
+// the fp16 range check of the coefficient table: |a| + 2|b| + 4|c| <= 40
+// per step (bounds |Z| on Gram eigenvalues up to 1.5, so kappa |R Z| <=
+// 1024 * 1.5 * 40 stays below the fp16 maximum) and a
+// window gain prod |a| <= 8192 (Q holds q(R), whose entries reach it).
+int gram_options(dmuon_ctx* h, int ns_steps, const float* coeffs, const int* restarts, int n_restarts,
+                 std::vector<int>* out) {
+  out->clear();
+  if (!restarts) {
+    out->push_back(2);
+  } else {
+    if (n_restarts < 0 || n_restarts > DMUON_MAX_NS_STEPS) return fail(h, DMUON_ERR_ARG, "n_restarts out of range");
+    out->assign(restarts, restarts + n_restarts);
+  }
+  for (const auto& w : restart_windows(ns_steps, *out)) {
+    double gain = 1.0;
+    for (int k = w.first; k < w.second; ++k) {
+      const float* row = coeffs ? coeffs + 3 * k : kYouCoefficients[std::min(k, 4)];
+      if (std::fabs(row[0]) + 2.f * std::fabs(row[1]) + 4.f * std::fabs(row[2]) > 40.f)
+        return fail(h, DMUON_ERR_ARG, "Gram-space backend: |a| + 2|b| + 4|c| above 40 in a coefficient row");
+      gain *= std::max(1.0, (double)std::fabs(row[0]));
+    }
+    if (gain > 8192.0)
+      return fail(h, DMUON_ERR_ARG, "Gram-space backend: a restart window's gain prod |a| exceeds 8192; add restarts");
+  }
+  return DMUON_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -812,6 +1045,9 @@ void dmuon_default_opts(dmuon_opts_t* o) {
   o->nesterov = 1;
   o->scale_mode = 0;
   o->coeffs = nullptr;
+  o->backend = DMUON_BACKEND_DIRECT;
+  o->restarts = nullptr;
+  o->n_restarts = 0;
 }
 
 int dmuon_create(dmuon_handle_t* out, int device) {
@@ -834,11 +1070,14 @@ int dmuon_create(dmuon_handle_t* out, int device) {
     cudaGetLastError();
     clusters = 0;
   }
+  const bool gram_ok = clusters > 0 && gram_configure() == cudaSuccess;
+  if (!gram_ok) cudaGetLastError();
   dmuon_ctx* h = new dmuon_ctx();
   h->device = device;
   h->num_sms = sms;
   h->max_clusters = clusters;
   h->small_ok = small_ok;
+  h->gram_ok = gram_ok;
   for (int k = 0; k < kPtrSlots; ++k) {
     if (cudaEventCreateWithFlags(&h->slot_ev[k], cudaEventDisableTiming) != cudaSuccess) {
       for (int j = 0; j < k; ++j) cudaEventDestroy(h->slot_ev[j]);
@@ -902,6 +1141,22 @@ int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats, size_t* out_b
   return DMUON_OK;
 }
 
+int dmuon_workspace_bytes_ex(const dmuon_shape_t* shapes, int n_mats, int backend, size_t* out_bytes) {
+  if (backend == DMUON_BACKEND_DIRECT) return dmuon_workspace_bytes(shapes, n_mats, out_bytes);
+  if (backend != DMUON_BACKEND_GRAM || !out_bytes || n_mats < 0 || (n_mats > 0 && !shapes)) return DMUON_ERR_ARG;
+  *out_bytes = 0;
+  if (n_mats == 0) return DMUON_OK;
+  if (int rc = check_shapes(shapes, n_mats)) return rc;
+  size_t most = 0;
+  for (int sp = 0; sp < 2; ++sp) {
+    size_t ws, sm;
+    plan_sizes(shapes, n_mats, true, kDefaultChunkElems, sp != 0, &ws, &sm, true);
+    most = std::max(most, ws + sm);
+  }
+  *out_bytes = most;
+  return DMUON_OK;
+}
+
 int dmuon_step(dmuon_handle_t h, float* const* params, const float* const* grads,
                float* const* momentum, const dmuon_shape_t* shapes, int n_mats, float lr,
                float mu, int ns_steps, const dmuon_opts_t* opts, void* stream) {
@@ -916,7 +1171,11 @@ int dmuon_step(dmuon_handle_t h, float* const* params, const float* const* grads
   if (!std::isfinite(o.weight_decay) || !std::isfinite(o.eps) || o.eps < 0.f) return DMUON_ERR_ARG;
   if (o.scale_mode < 0 || o.scale_mode > 2) return DMUON_ERR_ARG;
   if (o.coeffs && !finite3(o.coeffs, ns_steps)) return DMUON_ERR_ARG;
+  if (o.backend != DMUON_BACKEND_DIRECT && o.backend != DMUON_BACKEND_GRAM) return DMUON_ERR_ARG;
   if (int rc = check_shapes(shapes, n_mats)) return rc;
+  std::vector<int> restarts;
+  if (o.backend == DMUON_BACKEND_GRAM)
+    if (int rc = gram_options(h, ns_steps, o.coeffs, o.restarts, o.n_restarts, &restarts)) return rc;
   std::vector<MatPtrs> ptrs(n_mats);
   for (int i = 0; i < n_mats; ++i) {
     int rc;
@@ -927,7 +1186,7 @@ int dmuon_step(dmuon_handle_t h, float* const* params, const float* const* grads
     ptrs[i] = MatPtrs{params[i], grads[i], momentum[i], nullptr};
   }
   return run(h, ptrs.data(), shapes, n_mats, lr, mu, ns_steps, o.coeffs, o.eps, o.weight_decay,
-             o.nesterov ? 1 : 0, o.scale_mode, 0, (cudaStream_t)stream);
+             o.nesterov ? 1 : 0, o.scale_mode, 0, (cudaStream_t)stream, o.backend == DMUON_BACKEND_GRAM, restarts);
 }
 
 int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs, float* const* outputs,
@@ -950,6 +1209,30 @@ int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs, float* con
   }
   return run(h, ptrs.data(), shapes, n_mats, 0.f, 0.f, ns_steps, coeffs, eps, 0.f, 0, 1, 1,
              (cudaStream_t)stream);
+}
+
+int dmuon_gram_newton_schulz(dmuon_handle_t h, const float* const* inputs, float* const* outputs,
+                             const dmuon_shape_t* shapes, int n_mats, int ns_steps, const float* coeffs,
+                             const int* restarts, int n_restarts, float eps, void* stream) {
+  if (!h || n_mats < 0) return DMUON_ERR_ARG;
+  if (n_mats == 0) return DMUON_OK;
+  if (!inputs || !outputs || !shapes) return DMUON_ERR_ARG;
+  if (ns_steps < 0 || ns_steps > DMUON_MAX_NS_STEPS) return DMUON_ERR_ARG;
+  if (!std::isfinite(eps)) return DMUON_ERR_ARG;
+  if (eps <= 0.f) eps = 1e-7f;
+  if (coeffs && !finite3(coeffs, ns_steps)) return DMUON_ERR_ARG;
+  if (int rc = check_shapes(shapes, n_mats)) return rc;
+  std::vector<int> rs;
+  if (int rc = gram_options(h, ns_steps, coeffs, restarts, n_restarts, &rs)) return rc;
+  std::vector<MatPtrs> ptrs(n_mats);
+  for (int i = 0; i < n_mats; ++i) {
+    int rc;
+    if ((rc = check_ptr(inputs[i])) || (rc = check_ptr(outputs[i]))) return rc;
+    if ((const void*)inputs[i] == (const void*)outputs[i]) return DMUON_ERR_ARG;
+    ptrs[i] = MatPtrs{outputs[i], inputs[i], nullptr, nullptr};
+  }
+  return run(h, ptrs.data(), shapes, n_mats, 0.f, 0.f, ns_steps, coeffs, eps, 0.f, 0, 1, 1,
+             (cudaStream_t)stream, true, rs);
 }
 
 int dmuon_adamw_step(dmuon_handle_t h, float* const* params, const float* const* grads,
@@ -1163,8 +1446,9 @@ int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len) {
   std::string s;
   char line[384];
   const int n = (int)h->shapes.size();
-  std::snprintf(line, sizeof line, "device %d, %d SMs, %d 2-CTA clusters; matrices %d; tiles %s; ", h->device,
-                h->num_sms, h->max_clusters, n, h->plan_pair ? "256x256 CTA pairs" : "128x256 single CTAs");
+  std::snprintf(line, sizeof line, "device %d, %d SMs, %d 2-CTA clusters; matrices %d; backend %s; tiles %s; ",
+                h->device, h->num_sms, h->max_clusters, n, h->plan_gram ? "gram" : "direct",
+                h->plan_pair ? "256x256 CTA pairs" : "128x256 single CTAs");
   s += line;
   if (h->small) {
     int64_t tiles = 0;

@@ -1,0 +1,219 @@
+"""GPU parity of the Gram-space Newton-Schulz backend (CTA-pair fp16
+Gram-window kernels + the direct Apply kernel for Q X) against the fp64 Gram
+oracle (``oracle/gram.py``, itself pinned to the direct oracle and the SVD
+closed form).
+
+Bars as in the direct parity tests: NS output and weight update within 3e-2
+relative Frobenius error per matrix, momentum within 1e-6.  The small-matrix
+kernel (which always runs the direct iteration) is switched off on the
+handles here so that small shapes exercise the Gram kernels too.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import newton_schulz_nesterov_gb300 as dm  # noqa: E402
+from newton_schulz_nesterov_gb300 import _build, workloads  # noqa: E402
+import oracle  # noqa: E402
+from oracle import gram as og  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+MOM_TOL = 1e-6
+NS_TOL = 3e-2
+F32 = lambda x: float(np.float32(x))  # noqa: E731
+
+RAGGED = [(1, 1), (1, 37), (37, 1), (3, 5), (64, 256), (256, 64), (128, 512), (129, 257), (300, 700),
+          (700, 300), (200, 200), (513, 1000), (1000, 513), (255, 2050), (8, 4100), (384, 384), (640, 96)]
+
+
+def rel_fro(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    nr = np.linalg.norm(ref)
+    return np.linalg.norm(got - ref) / nr if nr > 0 else np.linalg.norm(got - ref)
+
+
+@pytest.fixture(scope="module")
+def handle():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _build.build()
+    h = dm.Handle(0)
+    dm.dmuon_set_small_path(h.h, False)
+    yield h
+    h.close()
+
+
+def _dev(ts):
+    return [t.clone().cuda() for t in ts]
+
+
+def _inputs(shapes, seed):
+    gen = torch.Generator().manual_seed(seed)
+    return ([torch.rand(s, generator=gen) - 0.5 for s in shapes], [torch.randn(s, generator=gen) for s in shapes],
+            [torch.randn(s, generator=gen) for s in shapes])
+
+
+def test_gram_newton_schulz_ragged(handle):
+    gen = torch.Generator().manual_seed(201)
+    ins = [torch.randn(s, generator=gen) for s in RAGGED]
+    outs = [torch.empty(s, device="cuda") for s in RAGGED]
+    handle.gram_newton_schulz(_dev(ins), outs)
+    assert handle.status()[0] == 0
+    assert "backend gram" in dm.dmuon_plan_summary(handle.h)
+    for x, o, s in zip(ins, outs, RAGGED):
+        e = rel_fro(o.cpu().numpy(), og.gram_newton_schulz(x.numpy()))
+        assert e <= NS_TOL, (s, e)
+
+
+@pytest.mark.parametrize("ns_steps,restarts,coeffs", [
+    (5, (), None), (5, (1,), None), (5, (1, 3), None), (5, (1, 2, 3, 4), None), (1, (2,), None),
+    (3, (2,), [(3.0, -3.2, 1.2), (2.5, -2.0, 0.5), (1.875, -1.25, 0.375)]), (7, (2, 4), None), (0, (2,), None),
+])
+def test_gram_restart_sets(handle, ns_steps, restarts, coeffs):
+    gen = torch.Generator().manual_seed(203)
+    shapes = [(300, 900), (900, 300), (256, 256), (100, 2000)]
+    ins = [torch.randn(s, generator=gen) for s in shapes]
+    outs = [torch.empty(s, device="cuda") for s in shapes]
+    handle.gram_newton_schulz(_dev(ins), outs, ns_steps=ns_steps, coeffs=coeffs, restarts=restarts)
+    assert handle.status()[0] == 0
+    for x, o, s in zip(ins, outs, shapes):
+        ref = og.gram_newton_schulz(x.numpy(), ns_steps, coeffs=coeffs, restarts=restarts)
+        e = rel_fro(o.cpu().numpy(), ref)
+        assert e <= NS_TOL, (s, ns_steps, restarts, e)
+
+
+def test_gram_scaled_inputs(handle):
+    gen = torch.Generator().manual_seed(205)
+    base = torch.randn((300, 520), generator=gen)
+    for scale in (1e-6, 1e-3, 1.0, 1e3):
+        x = (base * scale).cuda()
+        o = torch.empty_like(x)
+        handle.gram_newton_schulz([x], [o])
+        assert rel_fro(o.cpu().numpy(), og.gram_newton_schulz(x.cpu().numpy())) <= NS_TOL, scale
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(nesterov=False), dict(wd=0.1), dict(scale_mode=2),
+                                dict(ns_steps=3, restarts=(1,))])
+def test_gram_step(handle, kw):
+    shapes = [(384, 1000), (1000, 384), (520, 520), (64, 1500)]
+    Ws, Gs, Ms = _inputs(shapes, 207)
+    Wd, Gd, Md = _dev(Ws), _dev(Gs), _dev(Ms)
+    kw = dict(kw)
+    ns = kw.pop("ns_steps", 5)
+    rs = kw.pop("restarts", None)
+    wd = kw.pop("wd", 0.0)
+    handle.step(Wd, Gd, Md, lr=0.05, mu=0.9, ns_steps=ns, weight_decay=wd, backend="gram", restarts=rs, **kw)
+    rc, flags = handle.status(len(shapes))
+    assert rc == 0 and not any(flags)
+    for i, s in enumerate(shapes):
+        ref = og.muon_step_gram(Ws[i].numpy(), Gs[i].numpy(), Ms[i].numpy(), lr=F32(0.05), mu=F32(0.9),
+                                wd=F32(wd), ns_steps=ns, restarts=(2,) if rs is None else rs, **kw)
+        W0 = Ws[i].numpy().astype(np.float64)
+        assert rel_fro(Md[i].cpu().numpy(), ref["M"]) <= MOM_TOL
+        e = rel_fro(Wd[i].cpu().numpy().astype(np.float64) - W0, ref["W"] - W0)
+        assert e <= NS_TOL, (s, kw, e)
+
+
+def test_gram_and_direct_backends_agree(handle):
+    """Same step with both backends on one handle (the plan switches): both
+    meet the bar and agree with each other."""
+    shapes = [(512, 1536), (1536, 512)]
+    Ws, Gs, Ms = _inputs(shapes, 209)
+    res = {}
+    for backend in ("direct", "gram", "direct"):
+        Wd, Gd, Md = _dev(Ws), _dev(Gs), _dev(Ms)
+        handle.step(Wd, Gd, Md, backend=backend)
+        assert handle.status()[0] == 0
+        res.setdefault(backend, []).append([w.cpu() for w in Wd])
+    for a, b in zip(res["direct"][0], res["direct"][1]):
+        assert torch.equal(a, b)   # switching the plan back gives the same bits
+    for a, b, w0 in zip(res["gram"][0], res["direct"][0], Ws):
+        assert rel_fro((a - w0).numpy(), (b - w0).numpy()) <= 2 * NS_TOL
+
+
+def test_gram_deterministic_and_launch_count(handle):
+    shapes = [(300, 900), (700, 300)]
+    Ws, Gs, Ms = _inputs(shapes, 211)
+    Gd = _dev(Gs)
+    outs = []
+    for _ in range(2):
+        Wd, Md = _dev(Ws), _dev(Ms)
+        before = dm.dmuon_launch_count(handle.h)
+        handle.step(Wd, Gd, Md, backend="gram")
+        torch.cuda.synchronize()
+        # 2 (momentum, norm) + window 1: R, 3 + 2 products; restart Q X;
+        # window 2: R, 3 + 4 + 2 products; final Q X
+        assert dm.dmuon_launch_count(handle.h) - before == 20
+        outs.append([t.cpu() for t in Wd + Md])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    assert handle.status()[0] == 0
+
+
+def test_gram_argument_errors(handle):
+    x = torch.randn((300, 900), device="cuda")
+    o = torch.empty_like(x)
+    p = [x.data_ptr()], [o.data_ptr()], [(300, 900)]
+    before = dm.dmuon_launch_count(handle.h)
+    # a window of 8 steps without restart: gain prod |a| ~ 1.1e4 > 8192
+    assert dm.dmuon_gram_newton_schulz_ptrs(handle.h, *p, ns_steps=8, restarts=(), check=False) == -1
+    assert "gain" in dm.dmuon_last_error(handle.h)
+    assert dm.dmuon_gram_newton_schulz_ptrs(handle.h, *p, ns_steps=1, coeffs=[(1.0, 25.0, 0.0)],
+                                            check=False) == -1
+    assert dm.dmuon_launch_count(handle.h) == before
+    # with restarts the same 8 steps are fine
+    assert dm.dmuon_gram_newton_schulz_ptrs(handle.h, *p, ns_steps=8, restarts=(3, 6), check=False) == 0
+    assert handle.status()[0] == 0
+    ref = og.gram_newton_schulz(x.cpu().numpy(), 8, restarts=(3, 6))
+    assert rel_fro(o.cpu().numpy(), ref) <= NS_TOL
+
+
+def test_gram_step_in_cuda_graph(handle):
+    shapes = [(384, 1000), (600, 300)]
+    Ws, Gs, Ms = _inputs(shapes, 213)
+    Wa, Ga, Ma = _dev(Ws), _dev(Gs), _dev(Ms)
+    for _ in range(3):
+        handle.step(Wa, Ga, Ma, backend="gram")
+    torch.cuda.synchronize()
+    with dm.Handle(0) as h2:
+        Wb, Gb, Mb = _dev(Ws), _dev(Gs), _dev(Ms)
+        h2.step(Wb, Gb, Mb, backend="gram")
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            h2.step(Wb, Gb, Mb, backend="gram")
+        g.replay()
+        g.replay()
+        torch.cuda.synchronize()
+        assert h2.status()[0] == 0
+        for a, b in zip(Wa + Ma, Wb + Mb):
+            assert torch.equal(a, b)
+
+
+@pytest.mark.slow
+def test_gram_full_llama3_8b_sampled(handle):
+    """All 224 Llama-3-8B matrices with the Gram backend (bench launch
+    configuration); sampled matrices against the Gram oracle."""
+    w = workloads.get("llama3_8b")
+    n = len(w.shapes)
+    dev = "cuda"
+    Wd = [workloads.weight(w, i, dev) for i in range(n)]
+    Md = [workloads.momentum(w, i, dev) for i in range(n)]
+    Gd = [workloads.grad(w, i, 0, dev) for i in range(n)]
+    sample = [0, 1, 4, 6, 218]
+    W0 = {i: Wd[i].cpu() for i in sample}
+    M0 = {i: Md[i].cpu() for i in sample}
+    with dm.Handle(0) as h2:
+        h2.step(Wd, Gd, Md, backend="gram")
+        assert h2.status()[0] == 0
+    for i in sample:
+        ref = og.muon_step_gram(W0[i].numpy(), Gd[i].cpu().numpy(), M0[i].numpy(), lr=F32(0.02), mu=F32(0.95))
+        w0 = W0[i].numpy().astype(np.float64)
+        assert rel_fro(Md[i].cpu().numpy(), ref["M"]) <= MOM_TOL
+        e = rel_fro(Wd[i].cpu().numpy().astype(np.float64) - w0, ref["W"] - w0)
+        assert e <= NS_TOL, (i, w.shapes[i], e)
+    del Wd, Md, Gd
+    torch.cuda.empty_cache()
