@@ -45,6 +45,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-aux", action="store_true")
+    p.add_argument("--no-gram", action="store_true")
     return p.parse_args()
 
 
@@ -345,6 +346,11 @@ def run_ours(args, rank, world, local_rank):
     if args.workload == "llama3_8b" and not args.no_aux:
         aux = run_aux(args, h, Gs, stream, hbm_peak)
 
+    # ---- the Gram-space backend on the same workload (own handle and plan)
+    gram = None
+    if not args.no_gram:
+        gram = run_gram(args, Ws, Gs, Ms, shapes, stream, world, ms / args.steps, local_rank)
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
@@ -367,6 +373,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
         "aux": aux,
+        "gram_backend": gram,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         idx, desc = oracle_sample(args.workload)
@@ -377,6 +384,60 @@ def run_ours(args, rank, world, local_rank):
     h.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_gram(args, Ws, Gs, Ms, shapes, stream, world, direct_ms, device):
+    """The same step with the Gram-space Newton-Schulz backend (restart
+    before the third step), timed like the headline (CUDA events, warm-up
+    first) on a handle of its own.  Reports its step time, matrices/s, its
+    own algorithmic flop rate, the direct-iteration-equivalent rate (the
+    headline's flop count over this time) and the speed-up over the direct
+    backend measured just before."""
+    import torch
+    import newton_schulz_nesterov_gb300 as dm
+    from newton_schulz_nesterov_gb300 import flops
+    wp = [t.data_ptr() for t in Ws]
+    gp = [t.data_ptr() for t in Gs]
+    mp = [t.data_ptr() for t in Ms]
+    h = dm.Handle(device)
+
+    def one_step():
+        dm.dmuon_step_ptrs(h.h, wp, gp, mp, shapes, 0.02, 0.95, 5, stream=stream, backend="gram")
+
+    for _ in range(max(args.warmup, 3)):
+        one_step()
+    if h.status()[0] != 0:
+        raise RuntimeError("gram warm-up status")
+    dm.dmuon_profile_read(h.h)
+    dm.dmuon_profile_enable(h.h, True)
+    torch.cuda.synchronize()
+    l0 = dm.dmuon_launch_count(h.h)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = dm.dmuon_launch_count(h.h) - l0
+    dm.dmuon_profile_enable(h.h, False)
+    prof = dm.dmuon_profile_read(h.h)
+    rc = h.status()[0]
+    h.close()
+    if rc != 0:
+        raise RuntimeError("gram timed status %d" % rc)
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    gfl = flops.gram_flops(shapes, 5, (2,))
+    return {
+        "restarts": [2], "ms_per_step": ms,
+        "matrices_per_s": len(shapes) * world / (ms / 1e3),
+        "algorithmic_tflops": gfl * world / (ms / 1e3) / 1e12,
+        "direct_equivalent_tflops": flops.algorithmic_flops(shapes) * world / (ms / 1e3) / 1e12,
+        "speedup_vs_direct": direct_ms / ms,
+        "gpu_launches": launches,
+        "phases": {k: {"ms_per_step": v[0] / args.steps, "launches": v[1]} for k, v in prof.items() if v[1]},
+        "parity": "tests/test_gpu_gram.py (fp64 Gram oracle, 3e-2 per matrix)",
+    }
 
 
 def run_aux(args, h, Gs, stream, hbm_peak):

@@ -33,3 +33,27 @@ def elementwise_bytes(shapes):
     """Algorithmic HBM bytes of the momentum/normalise pass: read G and M,
     write M (fp32) and the bf16 iterate: 14 bytes per element."""
     return sum(14 * r * c for r, c in shapes)
+
+
+def gram_flops(shapes, ns_steps=5, restarts=(2,)):
+    """Algorithmic flops of the Gram-space backend.  Per restart window:
+    X X^T (one triangle, m^2 n), per step Z from R R (m^3), Q' = Z Q on all
+    but the window's first step (m^3), R Z and Z (R Z) on all but its last
+    (2 m^3), all symmetric products as one triangle, and the closing Q X
+    (2 m^2 n, dense).  Five steps with a restart before the third:
+    6 m^2 n + 14 m^3."""
+    cuts = sorted({int(k) for k in restarts if 0 < int(k) < ns_steps})
+    bounds = [0] + cuts + [ns_steps]
+    windows = [(bounds[i], bounds[i + 1]) for i in range(len(bounds) - 1) if bounds[i + 1] > bounds[i]]
+    tot = 0
+    for r, c in shapes:
+        m, n = min(r, c), max(r, c)
+        for start, end in windows:
+            tot += 3 * m * m * n
+            for k in range(start, end):
+                tot += m ** 3
+                if k > start:
+                    tot += m ** 3
+                if k < end - 1:
+                    tot += 2 * m ** 3
+    return tot

@@ -152,6 +152,34 @@ def test_workload_shapes_and_flop_totals():
     assert round(flops.algorithmic_flops(w5) / 1e12, 1) == 31.6
 
 
+def test_gram_flop_count():
+    """Gram backend: per window X X^T (m^2 n), per step Z (m^3), Q' (m^3, not
+    on the window's first step), R Z and Z (R Z) (2 m^3, not on its last),
+    closing Q X (2 m^2 n)."""
+    m, n = 96, 300
+    assert flops.gram_flops([(m, n)]) == 6 * m * m * n + 14 * m ** 3          # restart before step 2
+    assert flops.gram_flops([(n, m)], 5, ()) == 3 * m * m * n + (5 + 4 + 2 * 4) * m ** 3     # one window
+    assert flops.gram_flops([(m, n)], 1, (2,)) == 3 * m * m * n + m ** 3      # one window, one step
+    assert flops.gram_flops([(m, n)], 3, (1, 2)) == 3 * (3 * m * m * n + m ** 3)
+    assert flops.gram_flops([(m, n)], 0) == 0
+    # cheaper than the direct iteration when n > m, equal for square matrices
+    assert flops.gram_flops([(1024, 4096)]) < flops.algorithmic_flops([(1024, 4096)])
+    assert flops.gram_flops([(1024, 1024)]) == flops.algorithmic_flops([(1024, 1024)])  # break-even at n = m
+
+
+def test_gram_workspace_bytes(lib):
+    shapes = list(workloads.get("llama3_8b").shapes)
+    direct = dm.dmuon_workspace_bytes(shapes)
+    gram = dm.dmuon_workspace_bytes(shapes, "gram")
+    # the largest chunk gains seven m x m 16-bit buffers per matrix in place of A and B
+    assert direct < gram < direct + 7 * 2 * 16 * 4096 * 4096
+    out = ctypes.c_size_t()
+    arr = (dm.Shape * 1)(dm.Shape(64, 64))
+    assert lib.dmuon_workspace_bytes_ex(arr, 1, 7, ctypes.byref(out)) == -1
+    assert lib.dmuon_workspace_bytes_ex(arr, 1, 0, ctypes.byref(out)) == 0
+    assert lib.dmuon_workspace_bytes_ex(arr, 1, 1, ctypes.byref(out)) == 0 and out.value > 0
+
+
 def test_inputs_are_seeded_and_shaped():
     torch = pytest.importorskip("torch")
     w = workloads.get("tinymlp_d128")
