@@ -46,6 +46,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-aux", action="store_true")
     p.add_argument("--no-gram", action="store_true")
+    p.add_argument("--tile-mode", type=int, default=0, choices=[0, 1, 2],
+                   help="direct backend tiles: 0 automatic, 1 single CTAs (128x256), 2 CTA pairs (256x256)")
     return p.parse_args()
 
 
@@ -254,6 +256,8 @@ def run_ours(args, rank, world, local_rank):
     Ws = [workloads.weight(w, i, dev) for i in range(n)]
     Ms = [workloads.momentum(w, i, dev) for i in range(n)]
     h = dm.Handle(local_rank)
+    if args.tile_mode:
+        dm.dmuon_set_tile_mode(h.h, args.tile_mode)
     for step in range(w.warm_steps):
         Gw = [workloads.grad(w, i, step, dev) for i in range(n)]
         h.step(Ws, Gw, Ms, lr=lr, mu=mu)
@@ -333,13 +337,15 @@ def run_ours(args, rank, world, local_rank):
     phase = {k: {"ms_per_launch": (v[0] / v[1]) if v[1] else None, "launches": v[1],
                  "ms_per_step": v[0] / args.steps}
              for k, v in prof.items() if v[1]}
-    mom_ms_step = prof["momentum"][0] / args.steps
     hbm_peak = FALLBACK_HBM_GBS
     pk, _ = measured_peaks()
     if pk and pk.get("hbm_gbs"):
         hbm_peak = float(pk["hbm_gbs"])
-    phase["momentum"]["achieved_gbs"] = flops.elementwise_bytes(shapes) / (mom_ms_step / 1e3) / 1e9
-    phase["momentum"]["frac_of_hbm"] = phase["momentum"]["achieved_gbs"] / hbm_peak
+    if "momentum" in phase:   # absent when every matrix runs on the small-matrix kernel
+        big = [s_ for s_ in shapes if not (min(s_) <= 128 and max(s_) <= 512)]
+        mom_ms_step = prof["momentum"][0] / args.steps
+        phase["momentum"]["achieved_gbs"] = flops.elementwise_bytes(big) / (mom_ms_step / 1e3) / 1e9
+        phase["momentum"]["frac_of_hbm"] = phase["momentum"]["achieved_gbs"] / hbm_peak
 
     # ---- the rest of Muon.step: AdamW and clipping rooflines (HBM-bound)
     aux = None
