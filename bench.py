@@ -371,7 +371,9 @@ def run_ours(args, rank, world, local_rank):
         "dense_equiv_tflops": flops.dense_flops(shapes) * args.steps * world / sec / 1e12,
         "config": {"workload": args.workload, "matrices": n, "ns_steps": 5,
                    "resident_bytes": resident,
-                   "l2": "inputs larger than L2 (%.1f GB resident W/G/M)" % (resident / 1e9),
+                   "l2": ("inputs larger than L2 (%.1f GB resident W/G/M), no flush needed" % (resident / 1e9)
+                          if resident > 129e6 else
+                          "inputs fit in L2 (%.1f MB resident W/G/M; a latency case, not flushed)" % (resident / 1e6)),
                    "parallelism": "replicas x%d" % world if world > 1 else "single GPU"},
         "gpu_launches": launches,
         "roofline": roofline,
