@@ -217,3 +217,39 @@ def test_gram_full_llama3_8b_sampled(handle):
         assert e <= NS_TOL, (i, w.shapes[i], e)
     del Wd, Md, Gd
     torch.cuda.empty_cache()
+
+
+def test_gram_nonfinite_flags_in_caller_order(handle):
+    shapes = [(300, 500), (700, 300), (260, 900)]
+    Ws = [torch.zeros(s, device="cuda") for s in shapes]
+    Gs = [torch.randn(s, device="cuda") for s in shapes]
+    Ms = [torch.zeros(s, device="cuda") for s in shapes]
+    Gs[1][5, 7] = float("nan")
+    handle.step(Ws, Gs, Ms, backend="gram")
+    rc, flags = handle.status(3)
+    assert rc == -5 and flags == [0, 1, 0]
+    assert handle.status(3) == (0, [0, 0, 0])
+
+
+def test_gram_wait_timeout_is_reported_and_context_recovers(handle):
+    """A 1 ns wait limit makes the Gram-space (and Apply) kernels give up at
+    their first non-immediate wait, drain their own copies and MMAs, free
+    TMEM and return; the host reads DMUON_ERR_TIMEOUT, and with the default
+    limit restored the next step meets the bar again."""
+    shapes = [(384, 1000), (600, 300)]
+    Ws, Gs, Ms = _inputs(shapes, 215)
+    dm.dmuon_set_wait_timeout(handle.h, 1)
+    try:
+        handle.step(_dev(Ws), _dev(Gs), _dev(Ms), backend="gram")
+        rc, _ = handle.status(2)
+    finally:
+        dm.dmuon_set_wait_timeout(handle.h, 0)
+    assert rc == -6
+    assert handle.status(2)[0] == 0
+    Wd, Gd, Md = _dev(Ws), _dev(Gs), _dev(Ms)
+    handle.step(Wd, Gd, Md, backend="gram")
+    assert handle.status(2)[0] == 0
+    for i in range(2):
+        ref = og.muon_step_gram(Ws[i].numpy(), Gs[i].numpy(), Ms[i].numpy(), lr=F32(0.02), mu=F32(0.95))
+        W0 = Ws[i].numpy().astype(np.float64)
+        assert rel_fro(Wd[i].cpu().numpy().astype(np.float64) - W0, ref["W"] - W0) <= NS_TOL
