@@ -253,3 +253,43 @@ def test_gram_wait_timeout_is_reported_and_context_recovers(handle):
         ref = og.muon_step_gram(Ws[i].numpy(), Gs[i].numpy(), Ms[i].numpy(), lr=F32(0.02), mu=F32(0.95))
         W0 = Ws[i].numpy().astype(np.float64)
         assert rel_fro(Wd[i].cpu().numpy().astype(np.float64) - W0, ref["W"] - W0) <= NS_TOL
+
+
+def _gram_full_size_sampled(name, sample):
+    w = workloads.get(name)
+    n = len(w.shapes)
+    dev = "cuda"
+    Wd = [workloads.weight(w, i, dev) for i in range(n)]
+    Md = [workloads.momentum(w, i, dev) for i in range(n)]
+    with dm.Handle(0) as h2:
+        for step in range(w.warm_steps):
+            Gw = [workloads.grad(w, i, step, dev) for i in range(n)]
+            h2.step(Wd, Gw, Md, backend="gram")
+            del Gw
+        Gd = [workloads.grad(w, i, w.warm_steps, dev) for i in range(n)]
+        W0 = {i: Wd[i].cpu() for i in sample}
+        M0 = {i: Md[i].cpu() for i in sample}
+        h2.step(Wd, Gd, Md, backend="gram")
+        assert h2.status()[0] == 0
+    for i in sample:
+        ref = og.muon_step_gram(W0[i].numpy(), Gd[i].cpu().numpy(), M0[i].numpy(), lr=F32(0.02), mu=F32(0.95))
+        w0 = W0[i].numpy().astype(np.float64)
+        assert rel_fro(Md[i].cpu().numpy(), ref["M"]) <= MOM_TOL
+        e = rel_fro(Wd[i].cpu().numpy().astype(np.float64) - w0, ref["W"] - w0)
+        assert e <= NS_TOL, (name, i, w.shapes[i], e)
+    del Wd, Md, Gd
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_gram_full_spiked_4096_sampled(handle):
+    """Singular values spread over 1e-3..1e2 (rank-16 spike): the widest
+    spectrum of the workloads, through the fp16 Gram window."""
+    _gram_full_size_sampled("spiked_4096", [0, 63])
+
+
+@pytest.mark.slow
+def test_gram_full_tp_70b_mixed_sampled(handle):
+    """The 28672x8192 matrix (m = 8192, the largest Gram window) and packed
+    64x256 matrices (small-matrix kernel) in one call."""
+    _gram_full_size_sampled("tp_70b_mixed", [0, 1, 300, 512])
