@@ -418,3 +418,49 @@ def test_full_spiked_4096_sampled(handle):
 def test_full_tp_70b_mixed_sampled(handle):
     # the 28672x8192 matrix (transposed, short side 8192) and four 64x256 ones
     _full_size_sampled(handle, "tp_70b_mixed", [0, 1, 2, 256, 512])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape", [(32768, 32768), (65536, 32768)])
+@pytest.mark.parametrize("backend", ["direct", "gram"])
+def test_max_short_side_signed_permutation(handle, shape, backend):
+    """Short side at the limit (DMUON_MAX_SHORT_SIDE = 32768): G = alpha * P
+    with P a signed permutation (one +-1 per column of the oriented matrix)
+    and alpha a power of two, so every bf16 rounding of the input is exact.
+    All singular values of the normalised input equal
+    sigma = alpha / (alpha sqrt(m) + eps), hence O = p(sigma) P with p the
+    composed scalar quintic, taken from the oracle's direct iteration on
+    the 1x1 matrix [sigma]."""
+    r, c = shape
+    m = min(r, c)
+    alpha = 2.0 ** -10
+    gen = torch.Generator(device="cuda").manual_seed(77)
+    perm = torch.randperm(max(r, c), generator=gen, device="cuda")[:m]
+    sign = torch.randint(0, 2, (m,), generator=gen, device="cuda").float() * 2 - 1
+    G = torch.zeros(shape, device="cuda")
+    idx = torch.arange(m, device="cuda")
+    if r <= c:
+        G[idx, perm] = alpha * sign
+    else:
+        G[perm, idx] = alpha * sign
+    O = torch.empty_like(G)
+    with dm.Handle(0) as h2:
+        if backend == "gram":
+            h2.gram_newton_schulz([G], [O])
+        else:
+            h2.newton_schulz([G], [O])
+        assert h2.status()[0] == 0
+        assert "backend %s" % backend in dm.dmuon_plan_summary(h2.h)
+    sigma = alpha / (alpha * np.sqrt(m) + 1e-7)
+    p_sigma = float(oracle.newton_schulz_direct(np.array([[sigma]]), oracle.coefficient_rows(5))[0, 0])
+    expect_vals = p_sigma * sign
+    got_vals = O[idx, perm] if r <= c else O[perm, idx]
+    # the nonzero pattern: everything off the permutation is (close to) zero
+    tot = float((O * O).sum(dtype=torch.float64))
+    on = float((got_vals * got_vals).sum(dtype=torch.float64))
+    assert tot - on <= 1e-4 * tot, (tot, on)
+    diff = got_vals - expect_vals
+    err = float(torch.sqrt((diff * diff).sum(dtype=torch.float64) / (expect_vals * expect_vals).sum(dtype=torch.float64)))
+    assert err <= NS_TOL, (shape, backend, p_sigma, err)
+    del G, O
+    torch.cuda.empty_cache()
