@@ -293,3 +293,28 @@ def test_gram_full_tp_70b_mixed_sampled(handle):
     """The 28672x8192 matrix (m = 8192, the largest Gram window) and packed
     64x256 matrices (small-matrix kernel) in one call."""
     _gram_full_size_sampled("tp_70b_mixed", [0, 1, 300, 512])
+
+
+def test_gram_chunking_is_bitwise_neutral(handle):
+    """One chunk, many chunks, and many chunks with the next chunk's
+    momentum pass overlapped (chunks alternating between two workspaces
+    that hold their Gram-window buffers) give the same bits."""
+    gen = torch.Generator().manual_seed(217)
+    shapes = [(300, 500), (500, 300), (257, 257), (200, 900), (900, 200), (130, 900)]
+    Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
+    Gs = [torch.randn(s, generator=gen) for s in shapes]
+    Ms = [torch.randn(s, generator=gen) for s in shapes]
+    res = {}
+    for elems, overlap in ((1 << 29, False), (200_000, True), (200_001, False)):
+        with dm.Handle(0) as h2:
+            dm.dmuon_set_chunk_elements(h2.h, elems)
+            dm.dmuon_set_overlap(h2.h, overlap)
+            Wd, Gd, Md = _dev(Ws), _dev(Gs), _dev(Ms)
+            h2.step(Wd, Gd, Md, backend="gram")
+            assert h2.status()[0] == 0
+            summary = dm.dmuon_plan_summary(h2.h)
+            res[elems] = ([x.cpu() for x in Wd + Md], summary)
+    assert "chunks 1 " in res[1 << 29][1] and "chunks 1 " not in res[200_000][1]
+    for key in (200_000, 200_001):
+        for a, b in zip(res[1 << 29][0], res[key][0]):
+            assert torch.equal(a, b)

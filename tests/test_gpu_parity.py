@@ -464,3 +464,22 @@ def test_max_short_side_signed_permutation(handle, shape, backend):
     assert err <= NS_TOL, (shape, backend, p_sigma, err)
     del G, O
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("backend", ["direct", "gram"])
+def test_max_long_side(handle, backend):
+    """Long side at DMUON_MAX_DIM = 2^20 (8 x 2^20 and its transpose): one
+    super-tile whose X X^T runs 16384 K blocks, 4096 column tiles in the
+    Apply phase; against the fp64 oracle directly."""
+    gen = torch.Generator().manual_seed(91)
+    shapes = [(8, 1 << 20), (1 << 20, 8)]
+    ins = [torch.randn(s, generator=gen) for s in shapes]
+    outs = [torch.empty(s, device="cuda") for s in shapes]
+    if backend == "gram":
+        handle.gram_newton_schulz(_to_dev(ins), outs)
+    else:
+        handle.newton_schulz(_to_dev(ins), outs)
+    assert handle.status()[0] == 0
+    for x, o, s in zip(ins, outs, shapes):
+        e = rel_fro(o.cpu().numpy(), oracle.newton_schulz(x.numpy()))
+        assert e <= NS_TOL, (s, backend, e)
