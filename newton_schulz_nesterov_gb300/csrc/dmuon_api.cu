@@ -88,7 +88,7 @@ bool encode_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_
 struct Layout {
   std::vector<MatDesc> mats;       // device pointers filled in once allocated
   std::vector<int64_t> xoff, aoff, boff;  // workspace byte offsets
-  std::vector<int64_t> goff;       // Gram-space buffers: kGramBufs per matrix (gram plans)
+  std::vector<int64_t> goff;       // Gram-space buffers: kGramBufs per matrix (gram plans; -1 unused)
   std::vector<int64_t> tile_prefix;
   size_t ws_bytes = 0;             // big bf16 workspace
   size_t small_bytes = 0;          // descriptors, maps, lists, partials
@@ -98,10 +98,12 @@ struct Layout {
 // Workspace of a chunk.  Direct plans: X[0], X[1] (m x n bf16), A, B
 // (m x m bf16) per matrix.  Gram plans: X[0], X[1] and the kGramBufs m x m
 // buffers of the Gram-space window (R[2], B, T, Q[2] fp16; Q bf16).
-void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair, bool gram = false) {
+void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair, bool gram = false,
+                 bool implicit = false) {
   L.mats.assign(n, MatDesc{});
   L.xoff.resize(n); L.aoff.resize(n); L.boff.resize(n);
-  L.goff.assign(gram ? (size_t)n * kGramBufs : 0, 0);
+  L.goff.assign(gram ? (size_t)n * kGramBufs : 0, -1);
+  const int nbuf = implicit ? kGramBufs : kGramBufsExplicit;
   L.tile_prefix.assign(n + 1, 0);
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off += (size_t)rup((int64_t)bytes, 256); return (int64_t)o; };
@@ -116,7 +118,7 @@ void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair, bool 
     d.lda = rup(d.m, 8);
     L.xoff[i] = take((size_t)(2 * d.m * d.ldx * 2));  // X[0] and X[1] back to back
     if (gram) {
-      for (int b = 0; b < kGramBufs; ++b) L.goff[(size_t)i * kGramBufs + b] = take((size_t)(d.m * d.lda * 2));
+      for (int b = 0; b < nbuf; ++b) L.goff[(size_t)i * kGramBufs + b] = take((size_t)(d.m * d.lda * 2));
       L.aoff[i] = L.boff[i] = L.goff[(size_t)i * kGramBufs + kGbQb];
     } else {
       L.aoff[i] = take((size_t)(d.m * d.lda * 2));
@@ -189,6 +191,7 @@ struct Chunk {
   float* d_partials = nullptr;
   float* d_svec = nullptr;
   int4* d_items[3] = {nullptr, nullptr, nullptr};
+  bool implicit = false;          // gram plans: restarts without forming X (n >= 2m)
   GramDesc* d_gd = nullptr;       // gram plans: per-matrix Gram-space buffers
   CUtensorMap* d_gmaps = nullptr; // gram plans: kGramBufs maps per matrix
 };
@@ -357,14 +360,39 @@ float gram_kappa(int64_t m) {
 
 // Plan order: positions [0, n_large) hold the matrices run by the chunked
 // tensor-core path (caller order), the rest the small ones (caller order).
-int plan_order(const dmuon_shape_t* shapes, int n, bool small_path, std::vector<int>& order) {
+//
+// Gram plans order the chunked matrices further: those restarting
+// explicitly (n < 2m) first, then those restarting implicitly (n >= 2m), so
+// that every chunk holds one kind; *n_explicit counts the first kind.
+inline bool gram_implicit(const dmuon_shape_t& s) {
+  return std::max(s.rows, s.cols) >= 2 * std::min(s.rows, s.cols);
+}
+
+int plan_order(const dmuon_shape_t* shapes, int n, bool small_path, std::vector<int>& order, bool gram = false,
+               int* n_explicit = nullptr) {
   order.clear();
   for (int i = 0; i < n; ++i)
-    if (!(small_path && is_small(shapes[i]))) order.push_back(i);
+    if (!(small_path && is_small(shapes[i])) && !(gram && gram_implicit(shapes[i]))) order.push_back(i);
+  const int n_expl = (int)order.size();
+  if (gram)
+    for (int i = 0; i < n; ++i)
+      if (!(small_path && is_small(shapes[i])) && gram_implicit(shapes[i])) order.push_back(i);
   const int n_large = (int)order.size();
   for (int i = 0; i < n; ++i)
     if (small_path && is_small(shapes[i])) order.push_back(i);
+  if (n_explicit) *n_explicit = n_expl;
   return n_large;
+}
+
+// Chunks of a plan: greedy runs over [0, n_expl) and over [n_expl, n_large)
+// separately (gram plans), each flagged with its restart kind.
+std::vector<std::pair<std::pair<int, int>, bool>> plan_chunks(const dmuon_shape_t* ps, int n_expl, int n_large,
+                                                              int64_t limit, bool gram) {
+  std::vector<std::pair<std::pair<int, int>, bool>> out;
+  for (const auto& c : split_chunks(ps, n_expl, limit)) out.push_back({c, false});
+  for (const auto& c : split_chunks(ps + n_expl, n_large - n_expl, limit))
+    out.push_back({{c.first + n_expl, c.second}, gram});
+  return out;
 }
 
 // Host-side plan sizes (no device work): workspace of the largest chunk and
@@ -372,15 +400,17 @@ int plan_order(const dmuon_shape_t* shapes, int n, bool small_path, std::vector<
 void plan_sizes(const dmuon_shape_t* shapes, int n, bool pair, int64_t limit, bool small_path, size_t* ws,
                 size_t* small, bool gram = false) {
   std::vector<int> order;
-  const int n_large = plan_order(shapes, n, small_path, order);
+  int n_expl = 0;
+  const int n_large = plan_order(shapes, n, small_path, order, gram, &n_expl);
   std::vector<dmuon_shape_t> ps(n);
   for (int k = 0; k < n; ++k) ps[k] = shapes[order[k]];
   *ws = 256;
   *small = rup(sizeof(MatPtrs) * n * kPtrSlots, 256) + rup(4 * n, 256) + 256 +
            rup(sizeof(SmallDesc) * (n - n_large), 256);
-  for (const auto& c : split_chunks(ps.data(), n_large, limit)) {
+  for (const auto& cc : plan_chunks(ps.data(), n_expl, n_large, limit, gram)) {
+    const auto& c = cc.first;
     Layout L;
-    make_layout(ps.data() + c.first, c.second, L, pair, gram);
+    make_layout(ps.data() + c.first, c.second, L, pair, gram, cc.second);
     *ws = std::max(*ws, L.ws_bytes);
     *small += chunk_small_bytes(L, c.second);
   }
@@ -396,23 +426,25 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
   h->plan_pair = use_pairs(h, shapes, n, gram);
   h->plan_chunk_elems = chunk_limit(h);
   h->plan_small = h->small_path && h->small_ok;
-  h->n_large = plan_order(shapes, n, h->plan_small, h->order);
+  int n_expl = 0;
+  h->n_large = plan_order(shapes, n, h->plan_small, h->order, gram, &n_expl);
   std::vector<dmuon_shape_t> ps(n);
   for (int k = 0; k < n; ++k) ps[k] = shapes[h->order[k]];
   const int n_small = n - h->n_large;
   h->small_descs.resize(n_small);
   for (int k = 0; k < n_small; ++k)
     h->small_descs[k] = SmallDesc{ps[h->n_large + k].rows, ps[h->n_large + k].cols, h->n_large + k, 1.f};
-  const auto parts = split_chunks(ps.data(), h->n_large, h->plan_chunk_elems);
+  const auto parts = plan_chunks(ps.data(), n_expl, h->n_large, h->plan_chunk_elems, gram);
   h->chunks.resize(parts.size());
   h->ws_bytes = 256;
   h->small_bytes = rup(sizeof(MatPtrs) * n * kPtrSlots, 256) + rup(4 * n, 256) + 256 +
                    rup(sizeof(SmallDesc) * n_small, 256);
   for (size_t c = 0; c < parts.size(); ++c) {
     Chunk& ch = h->chunks[c];
-    ch.i0 = parts[c].first;
-    ch.n = parts[c].second;
-    make_layout(ps.data() + ch.i0, ch.n, ch.L, h->plan_pair, gram);
+    ch.i0 = parts[c].first.first;
+    ch.n = parts[c].first.second;
+    ch.implicit = parts[c].second;
+    make_layout(ps.data() + ch.i0, ch.n, ch.L, h->plan_pair, gram, ch.implicit);
     h->ws_bytes = std::max(h->ws_bytes, ch.L.ws_bytes);
     h->small_bytes += chunk_small_bytes(ch.L, ch.n);
   }
@@ -471,8 +503,9 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
         gd.kappa = gram_kappa(d.m);
         gd.inv_kappa = 1.f / gd.kappa;
         for (int b = 0; b < kGramBufs && ok; ++b) {
-          gd.buf[b] = (uint16_t*)(ws + L.goff[(size_t)i * kGramBufs + b]);
-          ok = encode_map(&gmaps[kGramBufs * i + b], gd.buf[b], d.m, d.m, d.lda, b != kGbQb);
+          const int64_t off = L.goff[(size_t)i * kGramBufs + b];
+          gd.buf[b] = off < 0 ? nullptr : (uint16_t*)(ws + off);   // unused in explicit chunks
+          if (off >= 0) ok = encode_map(&gmaps[kGramBufs * i + b], gd.buf[b], d.m, d.m, d.lda, b != kGbQb);
         }
       }
       if (!ok) {
@@ -791,9 +824,118 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
     return a;
   };
   const auto windows = restart_windows(ns_steps, restarts);
+  int rc;
+  // One window step: Z (copied at the window's first step to `qfirst`),
+  // Q' = Z Q, and, unless it is the window's last step, W = R Z and R' = Z W.
+  // The window's final factor goes to `qlast` (bf16 when it is kGbQb).
+  auto window = [&](int k0, int k1, int qfirst, int qlast) -> int {
+    int rc_ = kGbR0, qc = qfirst;
+    for (int k = k0; k < k1; ++k) {
+      const float* row = coeffs ? coeffs + 3 * k : kYouCoefficients[std::min(k, 4)];
+      const bool wfirst = k == k0, wlast = k == k1 - 1;
+      {  // Z = a I + (b/kappa) R~ + (c/kappa^2) R~ R~
+        GramArgs a = blank();
+        a.opA = a.opB = rc_;
+        a.out = kGbZ;
+        a.g0 = row[2];
+        a.gpow = -2;
+        a.add1 = rc_;
+        a.c1 = row[1];
+        a.p1pow = -1;
+        a.diag = row[0];
+        if (wfirst) {
+          a.out2 = wlast ? qlast : qc;
+          a.out2_bf16 = a.out2 == kGbQb ? 1 : 0;
+        }
+        if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
+      }
+      if (!wfirst) {  // Q' = Z Q
+        GramArgs a = blank();
+        a.opA = kGbZ;
+        a.opB = qc;
+        a.out = wlast ? qlast : (qc ^ kGbQ0 ^ kGbQ1);
+        a.out_bf16 = a.out == kGbQb ? 1 : 0;
+        if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
+        if (!wlast) qc ^= kGbQ0 ^ kGbQ1;
+      }
+      if (!wlast) {
+        GramArgs a = blank();  // W~ = R~ Z
+        a.opA = rc_;
+        a.opB = kGbZ;
+        a.out = kGbW;
+        if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
+        GramArgs r = blank();  // R~' = Z W~
+        r.opA = kGbZ;
+        r.opB = kGbW;
+        r.out = rc_ ^ kGbR0 ^ kGbR1;
+        if ((rc = prod(r, false, DMUON_KIND_GS_PROD))) return rc;
+        rc_ ^= kGbR0 ^ kGbR1;
+      }
+    }
+    return DMUON_OK;
+  };
+  if (ch.implicit) {
+    // Restarts without forming X: R_start = R~ of the window's start (Rs);
+    // at a restart W = R_start Qh, R~ = Qh W (the Gram matrix of Qh X), and
+    // the previous window's factor Qh joins the accumulator; at the end
+    // Q_total = Qh_last * accumulator, and O = s Q_total X0.
+    const int nw = (int)windows.size();
+    {
+      GramArgs a = blank();
+      a.src = 0;
+      a.out = kGbR0;
+      a.out2 = nw > 1 ? kGbRs : -1;
+      a.gpow = 1;
+      a.use_s2 = 1;
+      if ((rc = prod(a, true, DMUON_KIND_GS_GRAM))) return rc;
+    }
+    int acc = -1, qh = -1;  // accumulated factor (A0/A1; -1 = identity), last window's factor
+    for (int wi = 0; wi < nw; ++wi) {
+      const bool final_w = wi == nw - 1;
+      if (wi > 0) {
+        GramArgs t = blank();  // W = R_start Qh
+        t.opA = kGbRs;
+        t.opB = qh;
+        t.out = kGbW;
+        if ((rc = prod(t, false, DMUON_KIND_GS_PROD))) return rc;
+        GramArgs r = blank();  // R~ = Qh W, also the next window's R_start
+        r.opA = qh;
+        r.opB = kGbW;
+        r.out = kGbR0;
+        r.out2 = final_w ? -1 : kGbRs;
+        if ((rc = prod(r, false, DMUON_KIND_GS_PROD))) return rc;
+        if (acc < 0) {
+          acc = qh;  // the first window's factor was written to A0
+        } else {
+          GramArgs q = blank();  // accumulator <- Qh * accumulator
+          q.opA = qh;
+          q.opB = acc;
+          q.out = acc ^ kGbA0 ^ kGbA1;
+          if ((rc = prod(q, false, DMUON_KIND_GS_PROD))) return rc;
+          acc ^= kGbA0 ^ kGbA1;
+        }
+      }
+      const int k0 = windows[wi].first, k1 = windows[wi].second;
+      const int len = k1 - k0;
+      int qlast;
+      if (nw == 1) qlast = kGbQb;            // the only window: straight to the bf16 factor
+      else if (wi == 0) qlast = kGbA0;       // becomes the accumulator
+      else qlast = (len == 1) ? kGbQ0 : ((len % 2 == 0) ? kGbQ1 : kGbQ0);
+      if ((rc = window(k0, k1, kGbQ0, qlast))) return rc;
+      qh = qlast;
+    }
+    if (nw > 1) {  // Q_total = Qh * accumulator, in bf16 for the product with X
+      GramArgs q = blank();
+      q.opA = qh;
+      q.opB = acc;
+      q.out = kGbQb;
+      q.out_bf16 = 1;
+      if ((rc = prod(q, false, DMUON_KIND_GS_PROD))) return rc;
+    }
+    return apply(0, true, ns_only ? kWriteO : kUpdateW);
+  }
   int src = 0;
   bool first = true;
-  int rc;
   for (size_t wi = 0; wi < windows.size(); ++wi) {
     if (wi > 0) {  // restart: X <- Q X, then a new window from the explicit iterate
       if ((rc = apply(src, first, kWriteX))) return rc;

@@ -25,8 +25,24 @@
 namespace dmuon {
 
 // m x m buffers of one matrix, in this order in the workspace and in the
-// tensor-map array.
-enum GramBuf : int { kGbR0 = 0, kGbR1 = 1, kGbZ = 2, kGbW = 3, kGbQ0 = 4, kGbQ1 = 5, kGbQb = 6, kGramBufs = 7 };
+// tensor-map array.  The first seven serve every Gram plan; Rs (the Gram
+// matrix at the start of the window) and the factor accumulators A0, A1
+// exist only in chunks that restart implicitly (below).
+enum GramBuf : int {
+  kGbR0 = 0, kGbR1 = 1, kGbZ = 2, kGbW = 3, kGbQ0 = 4, kGbQ1 = 5, kGbQb = 6,
+  kGbRs = 7, kGbA0 = 8, kGbA1 = 9, kGramBufs = 10
+};
+constexpr int kGramBufsExplicit = 7;
+
+// Restarts.  Explicit (matrices with n < 2m): X <- Q X (bf16) and R <- X X^T.
+// Implicit (n >= 2m): R <- Q R_start Q from m x m products only (Q is a
+// polynomial in R_start, so this is the Gram matrix of the iterate Q X
+// without forming it), the window factors are multiplied into an
+// accumulator, and one product with X happens at the end.  Per five steps
+// with one restart that is 1.5 m^2 n + 8.5 m^3 multiply-adds instead of
+// 3 m^2 n + 7 m^3; an emulation of the fp16/bf16 roundings gave equal or
+// smaller errors than the explicit restart for n >= 2m and larger ones for
+// square matrices, where it saves nothing.
 
 struct GramDesc {
   uint16_t* buf[kGramBufs];  // m x m, leading dimension ld; fp16 except kGbQb (bf16)

@@ -36,24 +36,32 @@ def elementwise_bytes(shapes):
 
 
 def gram_flops(shapes, ns_steps=5, restarts=(2,)):
-    """Algorithmic flops of the Gram-space backend.  Per restart window:
-    X X^T (one triangle, m^2 n), per step Z from R R (m^3), Q' = Z Q on all
+    """Algorithmic flops of the Gram-space backend, symmetric products as one
+    triangle.  Per restart window: per step Z from R R (m^3), Q' = Z Q on all
     but the window's first step (m^3), R Z and Z (R Z) on all but its last
-    (2 m^3), all symmetric products as one triangle, and the closing Q X
-    (2 m^2 n, dense).  Five steps with a restart before the third:
-    6 m^2 n + 14 m^3."""
+    (2 m^3).  Matrices with n < 2m restart explicitly: per window X X^T
+    (m^2 n) and a closing Q X (2 m^2 n); five steps with a restart before
+    the third give 6 m^2 n + 14 m^3.  Matrices with n >= 2m restart
+    implicitly: one X X^T and one final Q X (3 m^2 n), two m^3 products per
+    restart, one more per restart after the first (the factor accumulator)
+    and one for the total factor: 3 m^2 n + 17 m^3 for the same schedule."""
     cuts = sorted({int(k) for k in restarts if 0 < int(k) < ns_steps})
     bounds = [0] + cuts + [ns_steps]
     windows = [(bounds[i], bounds[i + 1]) for i in range(len(bounds) - 1) if bounds[i + 1] > bounds[i]]
     tot = 0
     for r, c in shapes:
         m, n = min(r, c), max(r, c)
+        implicit = n >= 2 * m
         for start, end in windows:
-            tot += 3 * m * m * n
+            if not implicit:
+                tot += 3 * m * m * n
             for k in range(start, end):
                 tot += m ** 3
                 if k > start:
                     tot += m ** 3
                 if k < end - 1:
                     tot += 2 * m ** 3
+        if implicit and windows:
+            nw = len(windows)
+            tot += 3 * m * m * n + 2 * m ** 3 * (nw - 1) + m ** 3 * max(0, nw - 2) + (m ** 3 if nw > 1 else 0)
     return tot

@@ -155,15 +155,21 @@ def test_workload_shapes_and_flop_totals():
 
 
 def test_gram_flop_count():
-    """Gram backend: per window X X^T (m^2 n), per step Z (m^3), Q' (m^3, not
-    on the window's first step), R Z and Z (R Z) (2 m^3, not on its last),
-    closing Q X (2 m^2 n)."""
-    m, n = 96, 300
-    assert flops.gram_flops([(m, n)]) == 6 * m * m * n + 14 * m ** 3          # restart before step 2
+    """Gram backend: per window Z (m^3 per step), Q' (m^3, not on the
+    window's first step), R Z and Z (R Z) (2 m^3, not on its last).
+    n < 2m (explicit restarts): per window X X^T (m^2 n) and Q X (2 m^2 n).
+    n >= 2m (implicit restarts): one X X^T and one Q X, 2 m^3 per restart,
+    m^3 per accumulation after the first restart and for the total factor."""
+    m, n = 96, 150                                                            # explicit
+    assert flops.gram_flops([(m, n)]) == 6 * m * m * n + 14 * m ** 3         # restart before step 2
     assert flops.gram_flops([(n, m)], 5, ()) == 3 * m * m * n + (5 + 4 + 2 * 4) * m ** 3     # one window
     assert flops.gram_flops([(m, n)], 1, (2,)) == 3 * m * m * n + m ** 3      # one window, one step
     assert flops.gram_flops([(m, n)], 3, (1, 2)) == 3 * (3 * m * m * n + m ** 3)
     assert flops.gram_flops([(m, n)], 0) == 0
+    m, n = 96, 300                                                            # implicit
+    assert flops.gram_flops([(m, n)]) == 3 * m * m * n + 17 * m ** 3
+    assert flops.gram_flops([(n, m)], 5, ()) == 3 * m * m * n + 17 * m ** 3  # one window: same count
+    assert flops.gram_flops([(m, n)], 3, (1, 2)) == 3 * m * m * n + (3 + 2 * 2 + 1 + 1) * m ** 3
     # cheaper than the direct iteration when n > m, equal for square matrices
     assert flops.gram_flops([(1024, 4096)]) < flops.algorithmic_flops([(1024, 4096)])
     assert flops.gram_flops([(1024, 1024)]) == flops.algorithmic_flops([(1024, 1024)])  # break-even at n = m
@@ -173,8 +179,9 @@ def test_gram_workspace_bytes(lib):
     shapes = list(workloads.get("llama3_8b").shapes)
     direct = dm.dmuon_workspace_bytes(shapes)
     gram = dm.dmuon_workspace_bytes(shapes, "gram")
-    # the largest chunk gains seven m x m 16-bit buffers per matrix in place of A and B
-    assert direct < gram < direct + 7 * 2 * 16 * 4096 * 4096
+    # chunks gain up to ten m x m 16-bit buffers per matrix in place of A and B; Gram plans group
+    # the square matrices (explicit restarts) apart from the rectangular ones (implicit restarts)
+    assert direct < gram < 4 * direct
     out = ctypes.c_size_t()
     arr = (dm.Shape * 1)(dm.Shape(64, 64))
     assert lib.dmuon_workspace_bytes_ex(arr, 1, 7, ctypes.byref(out)) == -1

@@ -134,8 +134,15 @@ def test_gram_and_direct_backends_agree(handle):
         assert rel_fro((a - w0).numpy(), (b - w0).numpy()) <= 2 * NS_TOL
 
 
-def test_gram_deterministic_and_launch_count(handle):
-    shapes = [(300, 900), (700, 300)]
+@pytest.mark.parametrize("shapes,launches", [
+    # n >= 2m: implicit restarts.  2 (momentum, norm) + X X^T + window 1 (Z, W, R', Z, Q')
+    # + restart (R_start Q, Q W) + window 2 (Z, W, R', Z, Q', W, R', Z, Q') + total factor + Q X
+    ([(300, 900), (700, 300)], 21),
+    # n < 2m: explicit restarts.  2 + window 1 (X X^T, 3 + 2 products) + restart Q X
+    # + window 2 (X X^T, 3 + 4 + 2 products) + final Q X
+    ([(300, 500), (700, 400)], 20),
+])
+def test_gram_deterministic_and_launch_count(handle, shapes, launches):
     Ws, Gs, Ms = _inputs(shapes, 211)
     Gd = _dev(Gs)
     outs = []
@@ -144,9 +151,7 @@ def test_gram_deterministic_and_launch_count(handle):
         before = dm.dmuon_launch_count(handle.h)
         handle.step(Wd, Gd, Md, backend="gram")
         torch.cuda.synchronize()
-        # 2 (momentum, norm) + window 1: R, 3 + 2 products; restart Q X;
-        # window 2: R, 3 + 4 + 2 products; final Q X
-        assert dm.dmuon_launch_count(handle.h) - before == 20
+        assert dm.dmuon_launch_count(handle.h) - before == launches
         outs.append([t.cpu() for t in Wd + Md])
     for a, b in zip(*outs):
         assert torch.equal(a, b)
@@ -296,9 +301,9 @@ def test_gram_full_tp_70b_mixed_sampled(handle):
 
 
 def test_gram_chunking_is_bitwise_neutral(handle):
-    """One chunk, many chunks, and many chunks with the next chunk's
-    momentum pass overlapped (chunks alternating between two workspaces
-    that hold their Gram-window buffers) give the same bits."""
+    """One chunk per restart kind, many chunks, and many chunks with the
+    next chunk's momentum pass overlapped (chunks alternating between two
+    workspaces that hold their Gram-window buffers) give the same bits."""
     gen = torch.Generator().manual_seed(217)
     shapes = [(300, 500), (500, 300), (257, 257), (200, 900), (900, 200), (130, 900)]
     Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
@@ -314,7 +319,10 @@ def test_gram_chunking_is_bitwise_neutral(handle):
             assert h2.status()[0] == 0
             summary = dm.dmuon_plan_summary(h2.h)
             res[elems] = ([x.cpu() for x in Wd + Md], summary)
-    assert "chunks 1 " in res[1 << 29][1] and "chunks 1 " not in res[200_000][1]
+    import re
+    n_chunks = {k: int(re.search(r"chunks (\d+) ", v[1]).group(1)) for k, v in res.items()}
+    # one chunk per restart kind (square-ish matrices restart explicitly, n >= 2m implicitly)
+    assert n_chunks[1 << 29] == 2 and n_chunks[200_000] > 2
     for key in (200_000, 200_001):
         for a, b in zip(res[1 << 29][0], res[key][0]):
             assert torch.equal(a, b)
