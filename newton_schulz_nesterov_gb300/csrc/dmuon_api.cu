@@ -825,55 +825,66 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
   };
   const auto windows = restart_windows(ns_steps, restarts);
   int rc;
-  // One window step: Z (copied at the window's first step to `qfirst`),
-  // Q' = Z Q, and, unless it is the window's last step, W = R Z and R' = Z W.
-  // The window's final factor goes to `qlast` (bf16 when it is kGbQb).
-  auto window = [&](int k0, int k1, int qfirst, int qlast) -> int {
-    int rc_ = kGbR0, qc = qfirst;
+  // One window of steps [k0, k1): per step Z (into Z0 / Z1 alternately),
+  // Q' = Z Q from the second step on (the first step's Q is its Z, read
+  // from that Z buffer), and, unless it is the window's last step, W = R Z
+  // and R' = Z W.  The window's final factor goes to `qlast` (bf16 when it
+  // is kGbQb); only a one-step window copies its Z there.  Q' products of
+  // later steps alternate between Q0 and Q1; `qlast` must differ from the
+  // buffer the last Q' reads (window_qlast below picks it).
+  auto window = [&](int k0, int k1, int qlast) -> int {
+    int rc_ = kGbR0, zc = kGbZ0, qc = -1;
     for (int k = k0; k < k1; ++k) {
       const float* row = coeffs ? coeffs + 3 * k : kYouCoefficients[std::min(k, 4)];
       const bool wfirst = k == k0, wlast = k == k1 - 1;
       {  // Z = a I + (b/kappa) R~ + (c/kappa^2) R~ R~
         GramArgs a = blank();
         a.opA = a.opB = rc_;
-        a.out = kGbZ;
+        a.out = zc;
         a.g0 = row[2];
         a.gpow = -2;
         a.add1 = rc_;
         a.c1 = row[1];
         a.p1pow = -1;
         a.diag = row[0];
-        if (wfirst) {
-          a.out2 = wlast ? qlast : qc;
-          a.out2_bf16 = a.out2 == kGbQb ? 1 : 0;
+        if (wfirst && wlast) {
+          a.out2 = qlast;
+          a.out2_bf16 = qlast == kGbQb ? 1 : 0;
         }
         if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
       }
       if (!wfirst) {  // Q' = Z Q
         GramArgs a = blank();
-        a.opA = kGbZ;
+        a.opA = zc;
         a.opB = qc;
-        a.out = wlast ? qlast : (qc ^ kGbQ0 ^ kGbQ1);
+        a.out = wlast ? qlast : (qc == kGbQ0 ? kGbQ1 : kGbQ0);
         a.out_bf16 = a.out == kGbQb ? 1 : 0;
         if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
-        if (!wlast) qc ^= kGbQ0 ^ kGbQ1;
+        qc = a.out;
+      } else {
+        qc = zc;  // Q of the first step is its Z
       }
       if (!wlast) {
         GramArgs a = blank();  // W~ = R~ Z
         a.opA = rc_;
-        a.opB = kGbZ;
+        a.opB = zc;
         a.out = kGbW;
         if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
         GramArgs r = blank();  // R~' = Z W~
-        r.opA = kGbZ;
+        r.opA = zc;
         r.opB = kGbW;
         r.out = rc_ ^ kGbR0 ^ kGbR1;
         if ((rc = prod(r, false, DMUON_KIND_GS_PROD))) return rc;
         rc_ ^= kGbR0 ^ kGbR1;
       }
+      zc = zc == kGbZ0 ? kGbZ1 : kGbZ0;
     }
     return DMUON_OK;
   };
+  // A Q buffer for a window's final factor that its last Q' does not read:
+  // that Q' reads the first step's Z (two steps), or Q0 / Q1 alternating
+  // from Q0 on the second step (three or more steps).
+  auto window_qlast = [](int len) { return (len >= 3 && len % 2 == 1) ? kGbQ1 : kGbQ0; };
   if (ch.implicit) {
     // Restarts without forming X: R_start = R~ of the window's start (Rs);
     // at a restart W = R_start Qh, R~ = Qh W (the Gram matrix of Qh X), and
@@ -920,8 +931,8 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
       int qlast;
       if (nw == 1) qlast = kGbQb;            // the only window: straight to the bf16 factor
       else if (wi == 0) qlast = kGbA0;       // becomes the accumulator
-      else qlast = (len == 1) ? kGbQ0 : ((len % 2 == 0) ? kGbQ1 : kGbQ0);
-      if ((rc = window(k0, k1, kGbQ0, qlast))) return rc;
+      else qlast = window_qlast(len);
+      if ((rc = window(k0, k1, qlast))) return rc;
       qh = qlast;
     }
     if (nw > 1) {  // Q_total = Qh * accumulator, in bf16 for the product with X
@@ -950,49 +961,8 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
       a.use_s2 = first ? 1 : 0;
       if ((rc = prod(a, true, DMUON_KIND_GS_GRAM))) return rc;
     }
-    int rc_ = kGbR0, qc = kGbQ0;
-    for (int k = windows[wi].first; k < windows[wi].second; ++k) {
-      const float* row = coeffs ? coeffs + 3 * k : kYouCoefficients[std::min(k, 4)];
-      const bool wfirst = k == windows[wi].first, wlast = k == windows[wi].second - 1;
-      {  // Z = a I + (b/kappa) R~ + (c/kappa^2) R~ R~; at the window's first step also Q = Z
-        GramArgs a = blank();
-        a.opA = a.opB = rc_;
-        a.out = kGbZ;
-        a.g0 = row[2];
-        a.gpow = -2;
-        a.add1 = rc_;
-        a.c1 = row[1];
-        a.p1pow = -1;
-        a.diag = row[0];
-        if (wfirst) {
-          a.out2 = wlast ? kGbQb : qc;
-          a.out2_bf16 = wlast ? 1 : 0;
-        }
-        if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
-      }
-      if (!wfirst) {  // Q' = Z Q
-        GramArgs a = blank();
-        a.opA = kGbZ;
-        a.opB = qc;
-        a.out = wlast ? kGbQb : (qc ^ kGbQ0 ^ kGbQ1);
-        a.out_bf16 = wlast ? 1 : 0;
-        if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
-        if (!wlast) qc ^= kGbQ0 ^ kGbQ1;
-      }
-      if (!wlast) {
-        GramArgs a = blank();  // W~ = R~ Z
-        a.opA = rc_;
-        a.opB = kGbZ;
-        a.out = kGbW;
-        if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
-        GramArgs r = blank();  // R~' = Z W~
-        r.opA = kGbZ;
-        r.opB = kGbW;
-        r.out = rc_ ^ kGbR0 ^ kGbR1;
-        if ((rc = prod(r, false, DMUON_KIND_GS_PROD))) return rc;
-        rc_ ^= kGbR0 ^ kGbR1;
-      }
-    }
+    // every explicit window ends in the bf16 factor read by the Apply kernel
+    if ((rc = window(windows[wi].first, windows[wi].second, kGbQb))) return rc;
   }
   return apply(src, first, ns_only ? kWriteO : kUpdateW);
 }

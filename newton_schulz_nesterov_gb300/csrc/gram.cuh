@@ -25,14 +25,16 @@
 namespace dmuon {
 
 // m x m buffers of one matrix, in this order in the workspace and in the
-// tensor-map array.  The first seven serve every Gram plan; Rs (the Gram
-// matrix at the start of the window) and the factor accumulators A0, A1
-// exist only in chunks that restart implicitly (below).
+// tensor-map array.  The first eight serve every Gram plan (Z alternates
+// between Z0 and Z1 from step to step, so the window's first factor Q = Z
+// is read from its Z buffer instead of being copied); Rs (the Gram matrix
+// at the start of the window) and the factor accumulators A0, A1 exist only
+// in chunks that restart implicitly (below).
 enum GramBuf : int {
-  kGbR0 = 0, kGbR1 = 1, kGbZ = 2, kGbW = 3, kGbQ0 = 4, kGbQ1 = 5, kGbQb = 6,
-  kGbRs = 7, kGbA0 = 8, kGbA1 = 9, kGramBufs = 10
+  kGbR0 = 0, kGbR1 = 1, kGbZ0 = 2, kGbW = 3, kGbQ0 = 4, kGbQ1 = 5, kGbQb = 6, kGbZ1 = 7,
+  kGbRs = 8, kGbA0 = 9, kGbA1 = 10, kGramBufs = 11
 };
-constexpr int kGramBufsExplicit = 7;
+constexpr int kGramBufsExplicit = 8;
 
 // Restarts.  Explicit (matrices with n < 2m): X <- Q X (bf16) and R <- X X^T.
 // Implicit (n >= 2m): R <- Q R_start Q from m x m products only (Q is a

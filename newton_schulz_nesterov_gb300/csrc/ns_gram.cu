@@ -4,7 +4,8 @@
 // every matrix of a chunk.
 //
 //   R~ = kappa s^2 X X^T                      (bf16 X, K = n; first of a window)
-//   Z  = a I + (b/kappa) R~ + (c/kappa^2) R~ R~   (also copied to Q at a window start)
+//   Z  = a I + (b/kappa) R~ + (c/kappa^2) R~ R~   (two buffers alternating by step;
+//                                                 a window's first Q is its Z)
 //   Q' = Z Q
 //   W~ = R~ Z
 //   R~' = Z W~
