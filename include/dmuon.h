@@ -286,7 +286,8 @@ int dmuon_set_wait_timeout(dmuon_handle_t h, uint64_t ns);
  * can co-schedule 2-CTA clusters, the default), 1 = single CTAs computing
  * 128x256 tiles, 2 = CTA pairs computing 256x256 tiles (cta_group::2).  The
  * result is the same maths with the same roundings; the choice only changes
- * speed.  DMUON_ERR_UNSUPPORTED if pairs are requested but unavailable. */
+ * speed.  It applies to the direct backend; the Gram backend always uses CTA
+ * pairs.  DMUON_ERR_UNSUPPORTED if pairs are requested but unavailable. */
 int dmuon_set_tile_mode(dmuon_handle_t h, int mode);
 
 /* Chunking of later plans: the matrix list is cut into contiguous chunks of
