@@ -25,7 +25,7 @@ only m x m products; at a restart the iterate is formed explicitly
 (``X = Q X``), its Gram matrix is recomputed and ``Q`` starts again from
 the identity.
 
-Readings (also listed in the design doc):
+Readings of points the pages leave open:
 
 * a restart position ``k`` means "before step ``k`` (0-based)"; positions
   ``<= 0`` or ``>= ns_steps`` start no new window;

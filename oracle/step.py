@@ -15,7 +15,7 @@ Every array operation is float64.  A dense ``@`` is the only library
 primitive; there is no blocking, fusion or reordering beyond the steps as
 the pages state them.
 
-Readings of points the pages leave open (each also listed in the design doc):
+Readings of points the pages leave open:
 
 1. Nesterov uses the buffer *after* this step's momentum update
    (``U = G + mu * M_new``); the pre-update reading would make Nesterov the

@@ -125,7 +125,7 @@ def test_scalar_case_exact_rational(golden_dir):
     assert out["M"][0, 0] == pytest.approx(float(m_new), rel=1e-15)
     assert out["O"][0, 0] == pytest.approx(float(x), rel=1e-13)
     assert out["W"][0, 0] == pytest.approx(float(w_new), rel=1e-14)
-    # p(1) of the printed table, a fixed point the survey of the table found
+    # p(1) of the printed table: the composed quintic at sigma = 1, evaluated exactly
     assert float(_scalar_p(Fraction(1), [tuple(map(Fraction, r)) for r in rows])) == pytest.approx(0.97835, abs=5e-6)
 
 
