@@ -483,3 +483,35 @@ def test_max_long_side(handle, backend):
     for x, o, s in zip(ins, outs, shapes):
         e = rel_fro(o.cpu().numpy(), oracle.newton_schulz(x.numpy()))
         assert e <= NS_TOL, (s, backend, e)
+
+
+@pytest.mark.parametrize("backend,chunk", [("direct", 0), ("direct", 300_000), ("gram", 0), ("gram", 300_000)])
+def test_random_shape_lists(handle, backend, chunk):
+    """40 seeded random shapes (1..700 per side) in one call: small-kernel,
+    explicit- and implicit-restart matrices interleaved in the caller's list,
+    so plan ordering, pointer permutation and chunk boundaries all take
+    part; every matrix against the fp64 oracle (direct or Gram)."""
+    from oracle import gram as og
+    rng = np.random.default_rng(20261202)
+    shapes = [tuple(int(v) for v in rng.integers(1, 701, size=2)) for _ in range(40)]
+    shapes[3] = (64, 256)
+    shapes[7] = (700, 64)   # n >= 2m
+    shapes[11] = (400, 400)
+    gen = torch.Generator().manual_seed(5)
+    Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
+    Gs = [torch.randn(s, generator=gen) for s in shapes]
+    Ms = [torch.randn(s, generator=gen) for s in shapes]
+    Wd, Gd, Md = _to_dev(Ws), _to_dev(Gs), _to_dev(Ms)
+    with dm.Handle(0) as h2:
+        if chunk:
+            dm.dmuon_set_chunk_elements(h2.h, chunk)
+        h2.step(Wd, Gd, Md, lr=0.05, mu=0.9, backend=backend)
+        rc, flags = h2.status(len(shapes))
+        assert rc == 0 and not any(flags)
+    step = og.muon_step_gram if backend == "gram" else oracle.muon_step
+    for i, s in enumerate(shapes):
+        ref = step(Ws[i].numpy(), Gs[i].numpy(), Ms[i].numpy(), lr=F32(0.05), mu=F32(0.9))
+        W0 = Ws[i].numpy().astype(np.float64)
+        assert rel_fro(Md[i].cpu().numpy(), ref["M"]) <= MOM_TOL, (i, s)
+        e = rel_fro(Wd[i].cpu().numpy().astype(np.float64) - W0, ref["W"] - W0)
+        assert e <= NS_TOL, (i, s, backend, chunk, e)
