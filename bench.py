@@ -521,6 +521,18 @@ def step_groups(shapes, target_groups=32):
     return [list(range(i, i + size)) for i in range(0, n, size)]
 
 
+def host_mem_available():
+    """Bytes of host memory available (MemAvailable of /proc/meminfo), or None."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
 def run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world):
     """The same step end to end through the public API with host buffers:
     every step copies its gradients in from pinned host memory and reads the
@@ -531,6 +543,13 @@ def run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world):
     while group g computes."""
     import torch
     import newton_schulz_nesterov_gb300 as dm
+    need = sum(g.numel() * 4 for g in Gs) + sum(x.numel() * 4 for x in Ws)
+    avail = host_mem_available()
+    if avail is not None and need * world * 1.25 > avail:
+        # every rank pins its own copies; leave the host room rather than risk its memory
+        return {"value": None, "unit": "TFLOP/s (algorithmic)",
+                "skipped": "pinned host copies need %.1f GB x %d ranks, %.1f GB available"
+                           % (need / 1e9, world, avail / 1e9)}
     try:
         Gh = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in Gs]
         Wh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in Ws]
