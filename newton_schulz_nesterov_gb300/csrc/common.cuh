@@ -88,6 +88,7 @@ struct GemmArgs {
   int src;                 // X buffer holding the current iterate
   float ca, cb, cc;        // this iteration's (a, b, c)
   int first;               // first iteration: fold the norm scale in
+  int fold;                // Gram2 adds a*I (B becomes Z = aI + B); Apply then skips its a*X term
   int final_mode;          // Apply phase: kWriteX / kUpdateW / kWriteO
   float lr, decay;         // W <- decay*W - lr*scale*O
   const float* svec;       // per-matrix 1/(||U||_F + eps)

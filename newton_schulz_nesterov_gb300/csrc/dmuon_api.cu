@@ -722,6 +722,7 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
       a.src = k & 1;
       a.ca = row[0]; a.cb = row[1]; a.cc = row[2];
       a.first = k == 0;
+      a.fold = 1;
       a.final_mode = (k == ns_steps - 1) ? (ns_only ? kWriteO : kUpdateW) : kWriteX;
       a.lr = lr;
       a.decay = decay;
@@ -805,6 +806,7 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
     a.n_items = (int)L.items[kPhaseApply].size();
     a.src = src;
     a.ca = 0.f;          // X' = Q X
+    a.fold = 1;          // no a*X term to add: skip reading X in the epilogue
     a.first = first;     // the first window's X is U unnormalised: times s
     a.final_mode = mode;
     a.lr = lr;

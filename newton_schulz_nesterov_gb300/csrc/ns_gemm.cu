@@ -182,6 +182,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
         load_row32(d.A + r * ld, c, m, row_ok, av);
 #pragma unroll
         for (int j = 0; j < 32; ++j) f[j] = fmaf(a.cc, __uint_as_float(v[j]), a.cb * av[j]);
+        if (a.fold) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (r == c + j) f[j] += a.ca;
+        }
       }
       uint32_t w[16];
 #pragma unroll
@@ -202,11 +207,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
       if (c >= n) break;  // warp-uniform
       uint32_t v[32];
       ptx::tmem_ld32(tq + ch * 32, v);
-      float xv[32];
-      load_row32(xs + r * ldx, c, n, row_ok, xv);
       float o[32];
+      if (a.fold) {  // B already holds a*I: X' = Z X
 #pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = alpha * fmaf(a.ca, xv[j], __uint_as_float(v[j]));
+        for (int j = 0; j < 32; ++j) o[j] = alpha * __uint_as_float(v[j]);
+      } else {
+        float xv[32];
+        load_row32(xs + r * ldx, c, n, row_ok, xv);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = alpha * fmaf(a.ca, xv[j], __uint_as_float(v[j]));
+      }
       if constexpr (MODE == kWriteX) {
         uint32_t w[16];
 #pragma unroll
