@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--no-gram", action="store_true")
     p.add_argument("--tile-mode", type=int, default=0, choices=[0, 1, 2],
                    help="direct backend tiles: 0 automatic, 1 single CTAs (128x256), 2 CTA pairs (256x256)")
+    p.add_argument("--dealing", default="balanced", choices=["balanced", "strided"],
+                   help="work items to persistent CTAs: longest first to the least loaded, or round-robin")
     return p.parse_args()
 
 
@@ -258,6 +260,7 @@ def run_ours(args, rank, world, local_rank):
     h = dm.Handle(local_rank)
     if args.tile_mode:
         dm.dmuon_set_tile_mode(h.h, args.tile_mode)
+    dm.dmuon_set_balanced_dealing(h.h, args.dealing == "balanced")
     for step in range(w.warm_steps):
         Gw = [workloads.grad(w, i, step, dev) for i in range(n)]
         h.step(Ws, Gw, Ms, lr=lr, mu=mu)
@@ -374,6 +377,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": ("inputs larger than L2 (%.1f GB resident W/G/M), no flush needed" % (resident / 1e9)
                           if resident > 129e6 else
                           "inputs fit in L2 (%.1f MB resident W/G/M; a latency case, not flushed)" % (resident / 1e6)),
+                   "dealing": args.dealing,
                    "parallelism": "replicas x%d" % world if world > 1 else "single GPU"},
         "gpu_launches": launches,
         "roofline": roofline,
@@ -408,6 +412,7 @@ def run_gram(args, Ws, Gs, Ms, shapes, stream, world, direct_ms, device):
     gp = [t.data_ptr() for t in Gs]
     mp = [t.data_ptr() for t in Ms]
     h = dm.Handle(device)
+    dm.dmuon_set_balanced_dealing(h.h, args.dealing == "balanced")
 
     def one_step():
         dm.dmuon_step_ptrs(h.h, wp, gp, mp, shapes, 0.02, 0.95, 5, stream=stream, backend="gram")

@@ -307,6 +307,15 @@ int dmuon_set_chunk_elements(dmuon_handle_t h, int64_t elems);
  * the Llama-3-8B set it measured the same step time either way. */
 int dmuon_set_overlap(dmuon_handle_t h, int on);
 
+/* How later plans deal each phase's work items (256 x 256 output tiles,
+ * or 128-row halves) to the persistent CTAs or CTA pairs (default on):
+ * on, longest first, each to the one with the least K-blocks so far, so a
+ * list mixing long and short products (one Llama-3-8B layer: Grams with
+ * K = 14336 and K = 4096) ends evenly; off, the sorted list round-robin.
+ * The result is bitwise the same either way (each tile's arithmetic does not
+ * depend on who computes it).  dmuon_plan_summary reports the balance. */
+int dmuon_set_balanced_dealing(dmuon_handle_t h, int on);
+
 /* Small-matrix kernel for later plans (default on): every matrix whose
  * oriented shape has m = min(rows, cols) <= 128 and n = max(rows, cols) <= 512
  * (the TinyMLP projections of DMuon "Quick Start" at small widths; the
@@ -350,8 +359,10 @@ int dmuon_profile_read(dmuon_handle_t h, double* ms, int64_t* count,
                        int n_kinds);
 
 /* Human-readable description of the current plan (matrices, work items
- * per phase, workspace bytes) into buf (NUL-terminated, truncated to len).
- * Returns the full length needed. */
+ * per phase, how evenly each phase's items are dealt to the persistent
+ * CTAs or CTA pairs -- "balance": the busiest one's K-blocks over the mean,
+ * 1 = even -- and workspace bytes) into buf (NUL-terminated, truncated to
+ * len).  Returns the full length needed. */
 int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len);
 
 /* Static string for a status code. */

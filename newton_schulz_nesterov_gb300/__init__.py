@@ -110,6 +110,8 @@ def load(path=None):
     L.dmuon_last_error.restype = ctypes.c_char_p
     L.dmuon_set_overlap.argtypes = [vp, i32]
     L.dmuon_set_overlap.restype = i32
+    L.dmuon_set_balanced_dealing.argtypes = [vp, i32]
+    L.dmuon_set_balanced_dealing.restype = i32
     L.dmuon_set_small_path.argtypes = [vp, i32]
     L.dmuon_set_small_path.restype = i32
     L.dmuon_set_chunk_elements.argtypes = [vp, i64]
@@ -388,6 +390,11 @@ def dmuon_set_overlap(h, on=True):  # default off in the library
 def dmuon_set_chunk_elements(h, elems):
     """Chunk size of later plans in matrix elements (0 = default 2^29)."""
     _check(load().dmuon_set_chunk_elements(h, int(elems)), "dmuon_set_chunk_elements")
+
+
+def dmuon_set_balanced_dealing(h, on=True):  # default on in the library
+    """Longest-first dealing of work items to the least-loaded CTA (pair) for later plans."""
+    _check(load().dmuon_set_balanced_dealing(h, 1 if on else 0), "dmuon_set_balanced_dealing")
 
 
 def dmuon_set_small_path(h, on=True):  # default on in the library

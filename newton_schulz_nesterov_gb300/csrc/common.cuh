@@ -85,6 +85,7 @@ struct GemmArgs {
   const CUtensorMap* tmaps;
   const int4* items;       // {mat, ti, tj, k_blocks}
   int n_items;
+  const int* starts;       // balanced dealing: processor c runs items [starts[c], starts[c+1]); null: c, c+P, ...
   int src;                 // X buffer holding the current iterate
   float ca, cb, cc;        // this iteration's (a, b, c)
   int first;               // first iteration: fold the norm scale in
@@ -95,6 +96,16 @@ struct GemmArgs {
   int* err;                // device error word (bit 0: wait timeout)
   unsigned long long timeout_ns;  // wait without progress before giving up (0 = 4 s)
 };
+
+// Items of one persistent processor (a CTA, or a CTA pair): its own run
+// [starts[proc], starts[proc + 1]) when the host dealt the list (the launch
+// then has exactly as many processors as starts has entries minus one), else
+// every nproc-th item from proc on.
+struct WorkRange { int w0, w1, step; };
+__device__ __forceinline__ WorkRange work_range(const int* starts, int proc, int nproc, int n_items) {
+  if (starts) return WorkRange{starts[proc], starts[proc + 1], 1};
+  return WorkRange{proc, n_items, nproc};
+}
 
 struct MomArgs {
   const MatDesc* mats;

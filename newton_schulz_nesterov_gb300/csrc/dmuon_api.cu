@@ -19,6 +19,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -91,15 +92,58 @@ struct Layout {
   std::vector<int64_t> goff;       // Gram-space buffers: kGramBufs per matrix (gram plans; -1 unused)
   std::vector<int64_t> tile_prefix;
   size_t ws_bytes = 0;             // big bf16 workspace
-  size_t small_bytes = 0;          // descriptors, maps, lists, partials
   std::vector<int4> items[3];
+  std::vector<int> starts[3];      // per processor: first item of its run (procs + 1 entries)
+  int procs[3] = {0, 0, 0};        // persistent CTAs (or CTA pairs) to launch per phase
 };
+
+// Cost of one work item for the dealing below, in K-blocks: its main loop,
+// but at least the time of a 256 x 256 epilogue (reading, writing and
+// mirroring a tile takes about as long as 30-45 K-blocks of products, so a
+// short-K tile is epilogue-bound), plus a little for the tile's start.
+constexpr int64_t kItemFloor = 32;
+constexpr int64_t kItemOverhead = 2;
+inline int64_t item_cost(const int4& it) { return std::max<int64_t>(it.w, kItemFloor) + kItemOverhead; }
+
+// Deals a work list over `procs` persistent processors, longest item first,
+// each item to the processor with the least work so far (ties: the lowest
+// index), and regroups the list so that processor c's items, in the order it
+// got them, are [starts[c], starts[c+1]).  A run of equal items falls
+// round-robin, as a plain strided dealing would; mixed lengths (gate/up/down
+// Grams of K = 14336 beside q/k/v/o ones of K = 4096) no longer leave
+// the processors that drew one long item more than the others idle at the end.
+// Unbalanced (`balanced` false): the sorted list as is, item w to processor
+// w mod procs, and `starts` left empty (the kernels then stride).
+void deal_items(std::vector<int4>& items, int procs, bool balanced, std::vector<int>& starts, int& used) {
+  const int n = (int)items.size();
+  used = std::max(0, std::min(procs, n));
+  std::stable_sort(items.begin(), items.end(), [](const int4& x, const int4& y) { return x.w > y.w; });
+  starts.clear();
+  if (used == 0 || !balanced) return;
+  starts.assign(used + 1, 0);
+  using Load = std::pair<int64_t, int>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> q;
+  for (int c = 0; c < used; ++c) q.push({0, c});
+  std::vector<std::vector<int4>> per(used);
+  for (const int4& it : items) {
+    const Load l = q.top();
+    q.pop();
+    per[l.second].push_back(it);
+    q.push({l.first + item_cost(it), l.second});
+  }
+  int k = 0;
+  for (int c = 0; c < used; ++c) {
+    starts[c] = k;
+    for (const int4& it : per[c]) items[k++] = it;
+  }
+  starts[used] = k;
+}
 
 // Workspace of a chunk.  Direct plans: X[0], X[1] (m x n bf16), A, B
 // (m x m bf16) per matrix.  Gram plans: X[0], X[1] and the kGramBufs m x m
 // buffers of the Gram-space window (R[2], B, T, Q[2] fp16; Q bf16).
-void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair, bool gram = false,
-                 bool implicit = false) {
+void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair, int procs, bool balanced,
+                 bool gram = false, bool implicit = false) {
   L.mats.assign(n, MatDesc{});
   L.xoff.resize(n); L.aoff.resize(n); L.boff.resize(n);
   L.goff.assign(gram ? (size_t)n * kGramBufs : 0, -1);
@@ -162,14 +206,7 @@ void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair, bool 
       for (int64_t ti = 0; ti < cdiv(d.m, kBM); ++ti)
         L.items[kPhaseApply].push_back(make_int4(i, (int)ti, (int)tj, km));
   }
-  for (int p = 0; p < 3; ++p)
-    std::stable_sort(L.items[p].begin(), L.items[p].end(),
-                     [](const int4& x, const int4& y) { return x.w > y.w; });
-  const int64_t nt = L.tile_prefix[n];
-  L.small_bytes = rup(sizeof(MatDesc) * n, 256) + rup(sizeof(MatPtrs) * n * kPtrSlots, 256) +
-                  rup(sizeof(CUtensorMap) * kMapsPerMat * n, 256) + rup(8 * (n + 1), 256) +
-                  rup(4 * nt, 256) + 2 * rup(4 * n, 256) + 256 + rup(16 * L.items[0].size(), 256) +
-                  rup(16 * L.items[1].size(), 256) + rup(16 * L.items[2].size(), 256);
+  for (int p = 0; p < 3; ++p) deal_items(L.items[p], procs, balanced, L.starts[p], L.procs[p]);
 }
 
 }  // namespace
@@ -191,6 +228,7 @@ struct Chunk {
   float* d_partials = nullptr;
   float* d_svec = nullptr;
   int4* d_items[3] = {nullptr, nullptr, nullptr};
+  int* d_starts[3] = {nullptr, nullptr, nullptr};
   bool implicit = false;          // gram plans: restarts without forming X (n >= 2m)
   GramDesc* d_gd = nullptr;       // gram plans: per-matrix Gram-space buffers
   CUtensorMap* d_gmaps = nullptr; // gram plans: kGramBufs maps per matrix
@@ -239,6 +277,8 @@ struct dmuon_ctx {
   // Overlap of chunk c+1's momentum pass with chunk c's tensor-core phases:
   // a side stream, two alternating chunk workspaces and fork/join events.
   bool overlap = false;                     // requested (off: measured neutral at the power cap)
+  bool balanced = true;                     // requested: work items dealt longest-first to the least loaded
+  bool plan_balanced = true;                // in the current plan
   bool plan_overlap = false;                // in the current plan (needs >= 2 chunks)
   size_t ws_chunk = 0;                      // bytes of one chunk workspace
   cudaStream_t side = nullptr;
@@ -313,7 +353,7 @@ bool same_shapes(const dmuon_ctx* h, const dmuon_shape_t* s, int n, bool gram = 
   if ((int)h->shapes.size() != n || !h->small || h->plan_pair != use_pairs(h, s, n, gram) ||
       h->plan_gram != gram ||
       h->plan_small != (h->small_path && h->small_ok) ||
-      h->plan_chunk_elems != chunk_limit(h) || h->plan_overlap != (h->overlap && h->chunks.size() > 1))
+      h->plan_chunk_elems != chunk_limit(h) || h->plan_balanced != h->balanced || h->plan_overlap != (h->overlap && h->chunks.size() > 1))
     return false;
   for (int i = 0; i < n; ++i)
     if (h->shapes[i].rows != s[i].rows || h->shapes[i].cols != s[i].cols) return false;
@@ -346,6 +386,8 @@ size_t chunk_small_bytes(const Layout& L, int n) {
   return rup(sizeof(MatDesc) * n, 256) + rup(sizeof(CUtensorMap) * kMapsPerMat * n, 256) +
          rup(8 * (n + 1), 256) + rup(4 * L.tile_prefix[n], 256) + rup(4 * n, 256) +
          rup(16 * L.items[0].size(), 256) + rup(16 * L.items[1].size(), 256) + rup(16 * L.items[2].size(), 256) +
+         rup(4 * (L.items[0].size() + 1), 256) + rup(4 * (L.items[1].size() + 1), 256) +
+         rup(4 * (L.items[2].size() + 1), 256) +
          (gram ? rup(sizeof(GramDesc) * n, 256) + rup(sizeof(CUtensorMap) * kGramBufs * n, 256) : 0);
 }
 
@@ -410,7 +452,7 @@ void plan_sizes(const dmuon_shape_t* shapes, int n, bool pair, int64_t limit, bo
   for (const auto& cc : plan_chunks(ps.data(), n_expl, n_large, limit, gram)) {
     const auto& c = cc.first;
     Layout L;
-    make_layout(ps.data() + c.first, c.second, L, pair, gram, cc.second);
+    make_layout(ps.data() + c.first, c.second, L, pair, 1, true, gram, cc.second);  // sizes do not depend on procs
     *ws = std::max(*ws, L.ws_bytes);
     *small += chunk_small_bytes(L, c.second);
   }
@@ -425,6 +467,7 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
   h->plan_gram = gram;
   h->plan_pair = use_pairs(h, shapes, n, gram);
   h->plan_chunk_elems = chunk_limit(h);
+  h->plan_balanced = h->balanced;
   h->plan_small = h->small_path && h->small_ok;
   int n_expl = 0;
   h->n_large = plan_order(shapes, n, h->plan_small, h->order, gram, &n_expl);
@@ -444,7 +487,8 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
     ch.i0 = parts[c].first.first;
     ch.n = parts[c].first.second;
     ch.implicit = parts[c].second;
-    make_layout(ps.data() + ch.i0, ch.n, ch.L, h->plan_pair, gram, ch.implicit);
+    make_layout(ps.data() + ch.i0, ch.n, ch.L, h->plan_pair, h->plan_pair ? h->max_clusters : h->num_sms,
+                h->plan_balanced, gram, ch.implicit);
     h->ws_bytes = std::max(h->ws_bytes, ch.L.ws_bytes);
     h->small_bytes += chunk_small_bytes(ch.L, ch.n);
   }
@@ -476,6 +520,7 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
     ch.d_partials = (float*)carve(4 * L.tile_prefix[cn]);
     ch.d_svec = (float*)carve(4 * cn);
     for (int q = 0; q < 3; ++q) ch.d_items[q] = (int4*)carve(16 * L.items[q].size());
+    for (int q = 0; q < 3; ++q) ch.d_starts[q] = (int*)carve(4 * (L.items[q].size() + 1));
     if (gram) {
       ch.d_gd = (GramDesc*)carve(sizeof(GramDesc) * cn);
       ch.d_gmaps = (CUtensorMap*)carve(sizeof(CUtensorMap) * kGramBufs * cn);
@@ -524,7 +569,11 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
     if (gram && e == cudaSuccess)
       e = cudaMemcpy(ch.d_gmaps, gmaps.data(), sizeof(CUtensorMap) * gmaps.size(), cudaMemcpyHostToDevice);
     for (int q = 0; q < 3 && e == cudaSuccess; ++q)
-      if (!L.items[q].empty()) e = cudaMemcpy(ch.d_items[q], L.items[q].data(), 16 * L.items[q].size(), cudaMemcpyHostToDevice);
+      if (!L.items[q].empty()) {
+        e = cudaMemcpy(ch.d_items[q], L.items[q].data(), 16 * L.items[q].size(), cudaMemcpyHostToDevice);
+        if (e == cudaSuccess && !L.starts[q].empty())
+          e = cudaMemcpy(ch.d_starts[q], L.starts[q].data(), 4 * L.starts[q].size(), cudaMemcpyHostToDevice);
+      }
     if (e != cudaSuccess) { free_plan(h); return fail(h, cuda_err(e), "plan upload", e); }
   }
   e = cudaMemset(h->d_flags, 0, 4 * n);
@@ -718,6 +767,7 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
       a.ptrs = dptrs;
       a.tmaps = ch.d_maps;
       a.items = ch.d_items[p];
+      a.starts = L.starts[p].empty() ? nullptr : ch.d_starts[p];
       a.n_items = (int)L.items[p].size();
       a.src = k & 1;
       a.ca = row[0]; a.cb = row[1]; a.cc = row[2];
@@ -732,11 +782,11 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
       if (a.n_items <= 0) continue;
       LaunchGuard g(h, stream, kKinds[p]);
       if (h->plan_pair) {
-        const int clusters = std::min(a.n_items, h->max_clusters);
+        const int clusters = L.procs[p];  // the processors the list was dealt to
         if ((e = launch_gemm_pair(p, a, clusters, stream)) != cudaSuccess)
           return fail(h, cuda_err(e), "ns_gemm_pair launch", e);
       } else {
-        const int grid = std::min(a.n_items, h->num_sms);
+        const int grid = L.procs[p];
         if ((e = launch_gemm(p, a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "ns_gemm launch", e);
       }
     }
@@ -787,14 +837,16 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
     a.xmaps = ch.d_maps;
     a.gmaps = ch.d_gmaps;
     a.x_operand = x_operand ? 1 : 0;
-    a.items = ch.d_items[x_operand ? kPhaseGram : kPhaseGram2];
+    const int ph = x_operand ? kPhaseGram : kPhaseGram2;
+    a.items = ch.d_items[ph];
+    a.starts = L.starts[ph].empty() ? nullptr : ch.d_starts[ph];
     a.n_items = x_operand ? n_gram : n_prod;
     a.svec = ch.d_svec;
     a.err = h->d_err;
     a.timeout_ns = h->wait_timeout_ns;
     if (a.n_items <= 0) return DMUON_OK;
     LaunchGuard g(h, stream, kind);
-    const cudaError_t ee = launch_gram_pair(a, std::min(a.n_items, h->max_clusters), stream);
+    const cudaError_t ee = launch_gram_pair(a, L.procs[ph], stream);
     return ee == cudaSuccess ? DMUON_OK : fail(h, cuda_err(ee), "ns_gram_pair launch", ee);
   };
   auto apply = [&](int src, bool first, int mode) -> int {
@@ -803,6 +855,7 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
     a.ptrs = dptrs;
     a.tmaps = ch.d_maps;
     a.items = ch.d_items[kPhaseApply];
+    a.starts = L.starts[kPhaseApply].empty() ? nullptr : ch.d_starts[kPhaseApply];
     a.n_items = (int)L.items[kPhaseApply].size();
     a.src = src;
     a.ca = 0.f;          // X' = Q X
@@ -816,7 +869,7 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
     a.timeout_ns = h->wait_timeout_ns;
     if (a.n_items <= 0) return DMUON_OK;
     LaunchGuard g(h, stream, DMUON_KIND_APPLY);
-    const cudaError_t ee = launch_gemm_pair(kPhaseApply, a, std::min(a.n_items, h->max_clusters), stream);
+    const cudaError_t ee = launch_gemm_pair(kPhaseApply, a, L.procs[kPhaseApply], stream);
     return ee == cudaSuccess ? DMUON_OK : fail(h, cuda_err(ee), "ns_gemm_pair launch", ee);
   };
   auto blank = []() {
@@ -1520,6 +1573,12 @@ int dmuon_set_overlap(dmuon_handle_t h, int on) {
   return DMUON_OK;
 }
 
+int dmuon_set_balanced_dealing(dmuon_handle_t h, int on) {
+  if (!h) return DMUON_ERR_ARG;
+  h->balanced = on != 0;
+  return DMUON_OK;
+}
+
 int dmuon_set_small_path(dmuon_handle_t h, int on) {
   if (!h) return DMUON_ERR_ARG;
   if (on && !h->small_ok) return DMUON_ERR_UNSUPPORTED;
@@ -1571,11 +1630,35 @@ int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len) {
       tiles += ch.L.tile_prefix[ch.n];
       for (int q = 0; q < 3; ++q) it[q] += ch.L.items[q].size();
     }
+    // Dealing quality per phase: the busiest processor's item cost over the
+    // mean cost per processor, summed over chunks (1 = perfectly even; costs
+    // as item_cost).
+    double busiest[3] = {0, 0, 0}, mean[3] = {0, 0, 0};
+    for (const Chunk& ch : h->chunks)
+      for (int q = 0; q < 3; ++q) {
+        const Layout& L = ch.L;
+        if (L.procs[q] <= 0) continue;
+        double total = 0, top = 0;
+        const bool strided = L.starts[q].empty();
+        const int P = L.procs[q], n_it = (int)L.items[q].size();
+        for (int c = 0; c < P; ++c) {
+          double run = 0;
+          for (int w = strided ? c : L.starts[q][c]; w < (strided ? n_it : L.starts[q][c + 1]); w += strided ? P : 1)
+            run += item_cost(L.items[q][w]);
+          total += run;
+          top = std::max(top, run);
+        }
+        busiest[q] += top;
+        mean[q] += total / L.procs[q];
+      }
+    double bal[3];
+    for (int q = 0; q < 3; ++q) bal[q] = mean[q] > 0 ? busiest[q] / mean[q] : 1.0;
     std::snprintf(line, sizeof line,
                   "small-matrix kernel %zu; chunks %zu (<= %lld elements); momentum tiles %lld; "
-                  "items gram %zu gram2 %zu apply %zu; workspace %.3f GB + %.3f MB",
+                  "items gram %zu gram2 %zu apply %zu; balance gram %.4f gram2 %.4f apply %.4f; "
+                  "workspace %.3f GB + %.3f MB",
                   h->small_descs.size(), h->chunks.size(), (long long)h->plan_chunk_elems, (long long)tiles,
-                  it[0], it[1], it[2], h->ws_bytes / 1e9, h->small_bytes / 1e6);
+                  it[0], it[1], it[2], bal[0], bal[1], bal[2], h->ws_bytes / 1e9, h->small_bytes / 1e6);
     s += line;
   } else {
     s += "no plan";

@@ -67,6 +67,7 @@ struct GramArgs {
   const CUtensorMap* gmaps;   // kGramBufs per matrix
   const int4* items;          // {mat, I, J, k_blocks}
   int n_items;
+  const int* starts;          // per CTA pair: first item (see work_range), or null
   int x_operand, src;
   int opA, opB;
   int out, out_bf16;

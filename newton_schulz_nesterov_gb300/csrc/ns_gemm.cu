@@ -279,6 +279,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = a.timeout_ns ? a.timeout_ns : kTimeoutNs;
+  const WorkRange wr = work_range(a.starts, blockIdx.x, gridDim.x, a.n_items);
 
   uint64_t* full = sm.bars;
   uint64_t* empty = sm.bars + kStages;
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       // ---------------------------------------------------------- producer
       uint32_t it = 0;
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x) {
+      for (int w = wr.w0; ok && w < wr.w1; w += wr.step) {
         const int4 item = a.items[w];
         const CUtensorMap* maps = a.tmaps + (size_t)item.x * kMapsPerMat;
         const CUtensorMap* mapA;
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
-      for (int w = blockIdx.x; ok && w < a.n_items; w += gridDim.x, ++tc) {
+      for (int w = wr.w0; ok && w < wr.w1; w += wr.step, ++tc) {
         const int4 item = a.items[w];
         const uint32_t acc = tc & 1u;
         if (!wait_bar(ptx::smem_addr(tempty + acc), ((tc >> 1) & 1u) ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 for this warp
     uint32_t* scratch = sm.scratch + (warp - 2) * kEpiWords;
     uint32_t tc = 0;
-    for (int w = blockIdx.x; w < a.n_items; w += gridDim.x, ++tc) {
+    for (int w = wr.w0; w < wr.w1; w += wr.step, ++tc) {
       const int4 item = a.items[w];
       const uint32_t acc = tc & 1u;
       if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err, tmo)) break;
@@ -462,6 +463,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
+  const WorkRange wr = work_range(a.starts, pair, npairs, a.n_items);
 
   uint64_t* full = sm.bars;
   uint64_t* empty = sm.bars + kPairStages;
@@ -497,7 +499,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
       // ---------------------------------------------------------- producer
       uint32_t it = 0;
       bool ok = true;
-      for (int w = pair; ok && w < a.n_items; w += npairs) {
+      for (int w = wr.w0; ok && w < wr.w1; w += wr.step) {
         const int4 item = a.items[w];
         const CUtensorMap* maps = a.tmaps + (size_t)item.x * kMapsPerMat;
         const CUtensorMap* mapA;
@@ -548,7 +550,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
-      for (int w = pair; ok && w < a.n_items; w += npairs, ++tc) {
+      for (int w = wr.w0; ok && w < wr.w1; w += wr.step, ++tc) {
         const int4 item = a.items[w];
         const uint32_t acc = tc & 1u;
         if (!wait_bar(ptx::smem_addr(tempty + acc), ((tc >> 1) & 1u) ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
@@ -584,7 +586,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
     const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 for this warp
     uint32_t* scratch = sm.scratch + (warp - 2) * kEpiWords;
     uint32_t tc = 0;
-    for (int w = pair; w < a.n_items; w += npairs, ++tc) {
+    for (int w = wr.w0; w < wr.w1; w += wr.step, ++tc) {
       int4 item = a.items[w];
       const uint32_t acc = tc & 1u;
       if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err, tmo)) break;

@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gram_pair_kernel(const __g
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
+  const WorkRange wr = work_range(a.starts, pair, npairs, a.n_items);
 
   uint64_t* full = sm.bars;
   uint64_t* empty = sm.bars + kPairStages;
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gram_pair_kernel(const __g
       // ---------------------------------------------------------- producer
       uint32_t it = 0;
       bool ok = true;
-      for (int w = pair; ok && w < a.n_items; w += npairs) {
+      for (int w = wr.w0; ok && w < wr.w1; w += wr.step) {
         const int4 item = a.items[w];
         const CUtensorMap* mapA;
         const CUtensorMap* mapB;
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gram_pair_kernel(const __g
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
-      for (int w = pair; ok && w < a.n_items; w += npairs, ++tc) {
+      for (int w = wr.w0; ok && w < wr.w1; w += wr.step, ++tc) {
         const int4 item = a.items[w];
         const uint32_t acc = tc & 1u;
         if (!wait_bar(ptx::smem_addr(tempty + acc), ((tc >> 1) & 1u) ^ 1u, sm.abort_flag, a.err, tmo)) {
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gram_pair_kernel(const __g
     const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 for this warp
     uint32_t* scratch = sm.scratch + (warp - 2) * kEpiWords;
     uint32_t tc = 0;
-    for (int w = pair; w < a.n_items; w += npairs, ++tc) {
+    for (int w = wr.w0; w < wr.w1; w += wr.step, ++tc) {
       int4 item = a.items[w];
       const uint32_t acc = tc & 1u;
       if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err, tmo)) break;

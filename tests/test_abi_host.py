@@ -116,6 +116,7 @@ def test_null_handle_is_rejected(lib):
     assert lib.dmuon_profile_enable(None, 1) == -1
     assert lib.dmuon_set_wait_timeout(None, 5) == -1
     assert lib.dmuon_set_small_path(None, 1) == -1
+    assert lib.dmuon_set_balanced_dealing(None, 1) == -1
     assert lib.dmuon_gram_newton_schulz(None, None, None, None, 1, 5, None, None, 0, 1e-7, None) == -1
     assert lib.dmuon_last_error(None) == b"null handle"
     assert lib.dmuon_plan_summary(None, None, 0) == -1

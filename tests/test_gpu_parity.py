@@ -224,6 +224,65 @@ def test_chunking_is_bitwise_neutral(handle):
             assert torch.equal(a, b)
 
 
+def _balance(summary):
+    tail = summary.split("balance ")[1].split(";")[0].split()
+    return {tail[i]: float(tail[i + 1]) for i in range(0, len(tail), 2)}
+
+
+def test_items_dealt_evenly_for_one_llama_layer():
+    """One Llama-3-8B layer per call: the Gram items (K = 4096 for q/k/v/o,
+    K = 14336 for gate/up/down) are dealt longest-first to the least-loaded
+    CTA pair, so the busiest pair's items cost at most 2 % more than the mean
+    (a strided dealing of the same list gives ~10 %); the step still matches
+    the oracle on a sampled matrix."""
+    layer = [(4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096), (14336, 4096), (14336, 4096),
+             (4096, 14336)]
+    gen = torch.Generator(device="cuda").manual_seed(41)
+    Ws = [torch.rand(s, generator=gen, device="cuda") - 0.5 for s in layer]
+    Gs = [torch.randn(s, generator=gen, device="cuda") * 1e-3 for s in layer]
+    Ms = [torch.randn(s, generator=gen, device="cuda") * 1e-3 for s in layer]
+    W1, G1, M1 = Ws[1].cpu(), Gs[1].cpu(), Ms[1].cpu()
+    with dm.Handle(0) as h2:
+        h2.step(Ws, Gs, Ms)
+        rc, flags = h2.status(len(layer))
+        assert rc == 0 and not any(flags)
+        summary = dm.dmuon_plan_summary(h2.h)
+    bal = _balance(summary)
+    assert "chunks 1 " in summary
+    assert bal["gram"] <= 1.02, summary
+    assert bal["gram2"] <= 1.05 and bal["apply"] <= 1.02, summary
+    ref = oracle.muon_step(W1.numpy(), G1.numpy(), M1.numpy(), lr=F32(0.02), mu=F32(0.95))
+    assert rel_fro(Ms[1].cpu().numpy(), ref["M"]) <= MOM_TOL
+    assert rel_fro(Ws[1].cpu().numpy() - W1.numpy(), ref["W"] - W1.numpy()) <= NS_TOL
+
+
+@pytest.mark.parametrize("backend,tiles", [("direct", 2), ("direct", 1), ("gram", 2)])
+def test_dealing_is_bitwise_neutral(backend, tiles):
+    """Balanced and strided dealing of the same plan give bitwise equal
+    weights and momenta (mixed K: tall, wide, square and ragged matrices in
+    one chunk, more items than CTA pairs or CTAs in every phase), and the
+    balanced plan is no less even than the strided one on this list (the
+    busiest Gram processor: ~1.05 vs ~1.42 of the mean)."""
+    gen = torch.Generator().manual_seed(43)
+    shapes = [(6000, 2560), (2048, 2048), (768, 3000), (1536, 256), (640, 640), (300, 700), (1024, 130)]
+    Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
+    Gs = [torch.randn(s, generator=gen) for s in shapes]
+    Ms = [torch.randn(s, generator=gen) for s in shapes]
+    res = {}
+    for balanced in (True, False):
+        with dm.Handle(0) as h2:
+            dm.dmuon_set_tile_mode(h2.h, tiles)
+            dm.dmuon_set_balanced_dealing(h2.h, balanced)
+            Wd, Gd, Md = _to_dev(Ws), _to_dev(Gs), _to_dev(Ms)
+            h2.step(Wd, Gd, Md, backend=backend)
+            assert h2.status()[0] == 0
+            res[balanced] = ([x.cpu() for x in Wd], [x.cpu() for x in Md], _balance(dm.dmuon_plan_summary(h2.h)))
+    for a, b in zip(res[True][0] + res[True][1], res[False][0] + res[False][1]):
+        assert torch.equal(a, b)
+    for phase in ("gram", "gram2", "apply"):
+        assert res[True][2][phase] <= res[False][2][phase] + 1e-9, (res[True][2], res[False][2])
+
+
 def test_step_recorded_in_cuda_graph(handle):
     """Three eager steps equal one eager step plus two replays of a graph
     that recorded the step, bitwise; capturing before the buffers were seen
