@@ -75,7 +75,9 @@ def tensor_peak():
 
 def apply_traffic(workload):
     """DRAM bytes per Apply launch from the committed ncu summary, scaled by
-    layers processed; None unless the kernel sources are the ones captured."""
+    layers processed; None unless the kernel sources and the launch planning
+    (work lists and their dealing, which decide L2 reuse) are the ones
+    captured."""
     import hashlib
     import re
     layers = {"llama3_8b": 32, "llama3_8b_1layer": 1}.get(workload)
@@ -88,7 +90,8 @@ def apply_traffic(workload):
     if not sha or not per:
         return None
     csrc = os.path.join(ROOT, "newton_schulz_nesterov_gb300", "csrc")
-    src = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("ns_gemm.cu", "common.cuh", "ptx.cuh"))
+    src = b"".join(open(os.path.join(csrc, f), "rb").read()
+                   for f in ("ns_gemm.cu", "common.cuh", "ptx.cuh", "dmuon_api.cu"))
     if hashlib.sha1(src).hexdigest() != sha.group(1):
         return None
     return int(per.group(1)) * layers
