@@ -145,6 +145,51 @@ def test_tile_modes_match_oracle(handle, mode):
         _step_and_check(h2, Ws, Gs, Ms)
 
 
+# The last row mixes all three terms; its polynomial 0.5 s - 0.25 s^3 + 0.125 s^5 stays away from
+# zero on (0, 1], so a one-row matrix (its one normalised singular value ~1) keeps a finite output.
+SINGLE_TERM_ROWS = [(1.0, 0.0, 0.0), (0.0, 1.0, 0.0), (0.0, 0.0, 1.0), (0.5, -0.25, 0.125)]
+TERM_SHAPES = {
+    "pair": [(1, 300), (300, 1), (64, 64), (130, 700), (700, 130), (257, 257), (520, 520)],
+    "single": [(1, 300), (64, 64), (130, 700), (700, 130), (257, 257)],
+    "small": [(1, 300), (300, 1), (64, 64), (100, 500), (500, 100), (128, 128)],
+    "gram": [(1, 300), (64, 64), (130, 700), (700, 130), (257, 257), (520, 1100)],
+}
+
+
+@pytest.mark.parametrize("path", ["pair", "single", "small", "gram"])
+@pytest.mark.parametrize("row", SINGLE_TERM_ROWS)
+def test_each_term_of_the_step(path, row):
+    """One Newton-Schulz step with one term of X' = aX + b(XX^T)X + c(XX^T)^2 X
+    at a time, on every path (CTA-pair and single-CTA GEMM kernels, the
+    small-matrix kernel, the Gram-space kernels), against the fp64 oracle:
+    a dropped, doubled or mis-signed term in any epilogue fails here on its own.
+    Shapes include one-row and one-column matrices, one 64-wide tile, and
+    ragged tiles on both sides of the diagonal."""
+    shapes = TERM_SHAPES[path]
+    gen = torch.Generator().manual_seed(47)
+    ins = [torch.randn(s, generator=gen) for s in shapes]
+    outs = [torch.empty(s, device="cuda") for s in shapes]
+    with dm.Handle(0) as h2:
+        if path == "pair":
+            dm.dmuon_set_tile_mode(h2.h, 2)
+        if path == "single":
+            dm.dmuon_set_tile_mode(h2.h, 1)
+        if path != "small":
+            dm.dmuon_set_small_path(h2.h, False)
+        if path == "gram":
+            h2.gram_newton_schulz(_to_dev(ins), outs, ns_steps=1, coeffs=[row], restarts=[])
+        else:
+            h2.newton_schulz(_to_dev(ins), outs, ns_steps=1, coeffs=[row])
+        rc, _ = h2.status()
+        assert rc == 0
+        if path == "small":
+            assert "small-matrix kernel %d;" % len(shapes) in dm.dmuon_plan_summary(h2.h)
+    for x, o, s in zip(ins, outs, shapes):
+        ref = oracle.newton_schulz(x.numpy(), 1, coeffs=[row])
+        e = rel_fro(o.cpu().numpy(), ref)
+        assert e <= 1e-2, (path, row, s, e)
+
+
 def test_newton_schulz_scaled_inputs(handle):
     """The normalisation is folded into the first iteration: tiny and huge
     input scales give the same O."""
