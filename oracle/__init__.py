@@ -38,8 +38,13 @@ rank-1 cases, and hand-computed momentum/update values.  Two readings are
 # oracle.gram holds the Gram-space Newton-Schulz backend with restarts,
 # pinned in tests/test_oracle_gram_pins.py to the direct oracle, the SVD
 # closed form and the structure of its factors.
+# oracle.polar_express derives the Polar Express coefficient table (greedy
+# minimax odd quintics with the printed safety factor), pinned in
+# tests/test_oracle_polar_express_pins.py by the alternation theorem, its
+# chaining and a closed-form limit.
 from . import aux_steps  # noqa: F401
 from . import gram  # noqa: F401
+from . import polar_express  # noqa: F401
 from .step import (  # noqa: F401
     YOU_COEFFICIENTS,
     coefficient_rows,
