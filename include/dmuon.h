@@ -179,9 +179,9 @@ int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs,
  * Standalone Newton-Schulz with the Gram-space backend (DMuon "API
  * Reference", section "gram_newton_schulz"): as dmuon_newton_schulz, with
  * restart positions `restarts` (host, n_restarts entries; NULL = {2}).
- * DMUON_ERR_ARG if a coefficient row has |a| + 2|b| + 4|c| > 40 or a
- * restart window's gain prod |a| exceeds 8192 (the fp16 range of the
- * Gram-space buffers); DMUON_ERR_UNSUPPORTED without 2-CTA clusters.
+ * DMUON_ERR_ARG if the coefficient table could drive a Gram-space buffer
+ * past the fp16 range for some input (dmuon_gram_check_coefficients, which
+ * also says why); DMUON_ERR_UNSUPPORTED without 2-CTA clusters.
  */
 int dmuon_gram_newton_schulz(dmuon_handle_t h, const float* const* inputs,
                              float* const* outputs, const dmuon_shape_t* shapes,
@@ -364,6 +364,44 @@ int dmuon_profile_read(dmuon_handle_t h, double* ms, int64_t* count,
  * 1 = even -- and workspace bytes) into buf (NUL-terminated, truncated to
  * len).  Returns the full length needed. */
 int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len);
+
+/*
+ * Polar Express coefficient table (DMuon "API Reference", section
+ * "POLAR_EXPRESS_COEFFICIENTS": the Gram backend's default in the pages,
+ * built by the method of arXiv:2505.16932 with a safety factor, values not
+ * printed).  Row k is the odd quintic p(x) = a x + b x^3 + c x^5 with the
+ * least max |1 - p(x)| over the interval of singular values that rows
+ * 0..k-1 leave -- [lower, upper] for row 0, then [1 - E, 1 + E] with E the
+ * previous row's least error -- then scaled by the safety factor s as
+ * (a / s, b / s^3, c / s^5), i.e. p(x / s).  The pages' s is 1.05;
+ * lower = 1e-3 and upper = 1 are this library's reading of the start.
+ * Rows whose interval lies within 1e-7 of 1 (after about six steps from
+ * [1e-3, 1]) take the construction's limit (15/8, -10/8, 3/8).
+ *   out  host, 3 * steps floats, rows (a, b, c).
+ * Host only (no device, no handle).  DMUON_ERR_ARG for steps outside
+ * 1..DMUON_MAX_NS_STEPS, lower <= 0, upper <= lower, safety <= 0, a null
+ * out, or an interval on which the exchange does not converge.
+ */
+int dmuon_polar_express_coefficients(int steps, double lower, double upper,
+                                     double safety, float* out);
+
+/*
+ * The Gram-space backend's fp16 range check of a coefficient table (host
+ * only): follows the largest singular value the iterate can reach (1 for
+ * the normalised input, then max |p_k| over [0, u] after step k) and
+ * bounds every fp16 buffer for all inputs -- the step factor Z, kappa R and
+ * kappa R Z (kappa <= 1024) at half the fp16 maximum, each restart window's
+ * factor at 8192 and the factor accumulated over all windows at 32768.
+ *   coeffs    host, 3 * ns_steps floats, or NULL for the default table.
+ *   restarts  host, n_restarts entries, or NULL for {2}.
+ *   why       host buffer of why_len bytes for the reason (may be NULL).
+ * DMUON_OK if the table fits, DMUON_ERR_ARG otherwise (or for bad
+ * arguments: ns_steps or n_restarts outside 0..DMUON_MAX_NS_STEPS, a null
+ * restarts with n_restarts > 0, a non-finite coefficient).
+ */
+int dmuon_gram_check_coefficients(int ns_steps, const float* coeffs,
+                                  const int* restarts, int n_restarts,
+                                  char* why, size_t why_len);
 
 /* Static string for a status code. */
 const char* dmuon_error_string(int code);

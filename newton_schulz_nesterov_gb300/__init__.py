@@ -18,7 +18,7 @@ __all__ = [
     "dmuon_newton_schulz_ptrs", "dmuon_newton_schulz_noalloc", "dmuon_get_status",
     "dmuon_gram_newton_schulz", "dmuon_gram_newton_schulz_ptrs", "BACKENDS",
     "dmuon_adamw_step", "dmuon_adamw_step_ptrs", "dmuon_clip_grad_norm", "dmuon_clip_grad_norm_ptrs",
-    "dmuon_workspace_bytes",
+    "dmuon_workspace_bytes", "dmuon_polar_express_coefficients", "dmuon_gram_check_coefficients",
     "dmuon_launch_count", "dmuon_last_error", "dmuon_profile_enable", "dmuon_profile_read",
     "dmuon_plan_summary", "dmuon_error_string", "dmuon_version", "Handle",
     "KIND_NAMES", "STATUS",
@@ -133,6 +133,12 @@ def load(path=None):
     L.dmuon_error_string.restype = ctypes.c_char_p
     L.dmuon_version.argtypes = []
     L.dmuon_version.restype = ctypes.c_char_p
+    L.dmuon_polar_express_coefficients.argtypes = [i32, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                                   ctypes.POINTER(ctypes.c_float)]
+    L.dmuon_polar_express_coefficients.restype = i32
+    L.dmuon_gram_check_coefficients.argtypes = [i32, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int),
+                                                i32, ctypes.c_char_p, ctypes.c_size_t]
+    L.dmuon_gram_check_coefficients.restype = i32
     _lib = L
     return L
 
@@ -210,6 +216,26 @@ def dmuon_workspace_bytes(shapes, backend="direct"):
     _check(load().dmuon_workspace_bytes_ex(_shape_array(shapes), len(shapes), BACKENDS[backend],
                                            ctypes.byref(out)), "dmuon_workspace_bytes")
     return out.value
+
+
+def dmuon_polar_express_coefficients(steps=5, lower=1e-3, upper=1.0, safety=1.05):
+    """Polar Express table (host only): ``steps`` rows (a, b, c) as floats."""
+    out = (ctypes.c_float * (3 * max(1, int(steps))))()
+    _check(load().dmuon_polar_express_coefficients(int(steps), float(lower), float(upper), float(safety), out),
+           "dmuon_polar_express_coefficients")
+    return [(out[3 * k], out[3 * k + 1], out[3 * k + 2]) for k in range(int(steps))]
+
+
+def dmuon_gram_check_coefficients(ns_steps=5, coeffs=None, restarts=None):
+    """The Gram-space backend's fp16 range check (host only): (True, "") or
+    (False, reason)."""
+    carr = _coeff_array(coeffs)
+    rarr, nr = _restart_array(restarts)
+    why = ctypes.create_string_buffer(256)
+    rc = load().dmuon_gram_check_coefficients(int(ns_steps), carr, rarr, nr, why, 256)
+    if rc not in (0, -1):
+        raise DmuonError(rc, "dmuon_gram_check_coefficients")
+    return rc == 0, why.value.decode()
 
 
 def _restart_array(restarts):

@@ -27,6 +27,7 @@
 
 #include "../../include/dmuon.h"
 #include "aux.cuh"
+#include "coeffs.cuh"
 #include "common.cuh"
 #include "gram.cuh"
 #include "small.cuh"
@@ -34,15 +35,6 @@
 using namespace dmuon;
 
 namespace {
-
-// DMuon "API Reference", section YOU_COEFFICIENTS: the default table.
-const float kYouCoefficients[5][3] = {
-    {4.0848f, -6.8946f, 2.927f},
-    {3.9505f, -6.3029f, 2.6377f},
-    {3.7418f, -5.5913f, 2.3037f},
-    {2.8769f, -3.1427f, 1.2046f},
-    {2.8366f, -3.0525f, 1.2012f},
-};
 
 const char* kVersion = "dmuon-gb300 0.1.0 (sm_103a, tcgen05/TMA)";
 
@@ -794,20 +786,6 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
   return DMUON_OK;
 }
 
-// Restart windows [start, end) of ns_steps steps: positions outside
-// (0, ns_steps) start no window; duplicates collapse.
-std::vector<std::pair<int, int>> restart_windows(int ns_steps, const std::vector<int>& restarts) {
-  std::vector<int> cuts;
-  for (int k : restarts)
-    if (k > 0 && k < ns_steps) cuts.push_back(k);
-  std::sort(cuts.begin(), cuts.end());
-  cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
-  std::vector<std::pair<int, int>> w;
-  int start = 0;
-  for (int k : cuts) { w.push_back({start, k}); start = k; }
-  if (ns_steps > start) w.push_back({start, ns_steps});
-  return w;
-}
 
 // Newton-Schulz of a chunk with the Gram-space backend and the update.
 // Per window: R~ = kappa s^2 X X^T, then per step Z (copied to Q at the
@@ -1174,10 +1152,7 @@ bool finite3(const float* c, int rows) {
 }
 
 // Gram-space backend: restart positions (NULL = the pages' default {2}) and
-// the fp16 range check of the coefficient table: |a| + 2|b| + 4|c| <= 40
-// per step (bounds |Z| on Gram eigenvalues up to 1.5, so kappa |R Z| <=
-// 1024 * 1.5 * 40 stays below the fp16 maximum) and a
-// window gain prod |a| <= 8192 (Q holds q(R), whose entries reach it).
+// the fp16 range check of the coefficient table (gram_table_fits).
 int gram_options(dmuon_ctx* h, int ns_steps, const float* coeffs, const int* restarts, int n_restarts,
                  std::vector<int>* out) {
   out->clear();
@@ -1187,16 +1162,10 @@ int gram_options(dmuon_ctx* h, int ns_steps, const float* coeffs, const int* res
     if (n_restarts < 0 || n_restarts > DMUON_MAX_NS_STEPS) return fail(h, DMUON_ERR_ARG, "n_restarts out of range");
     out->assign(restarts, restarts + n_restarts);
   }
-  for (const auto& w : restart_windows(ns_steps, *out)) {
-    double gain = 1.0;
-    for (int k = w.first; k < w.second; ++k) {
-      const float* row = coeffs ? coeffs + 3 * k : kYouCoefficients[std::min(k, 4)];
-      if (std::fabs(row[0]) + 2.f * std::fabs(row[1]) + 4.f * std::fabs(row[2]) > 40.f)
-        return fail(h, DMUON_ERR_ARG, "Gram-space backend: |a| + 2|b| + 4|c| above 40 in a coefficient row");
-      gain *= std::max(1.0, (double)std::fabs(row[0]));
-    }
-    if (gain > 8192.0)
-      return fail(h, DMUON_ERR_ARG, "Gram-space backend: a restart window's gain prod |a| exceeds 8192; add restarts");
+  char why[192];
+  if (!gram_table_fits(ns_steps, coeffs, *out, why, sizeof why)) {
+    std::string msg = std::string("Gram-space backend: ") + why;
+    return fail(h, DMUON_ERR_ARG, msg.c_str());
   }
   return DMUON_OK;
 }

@@ -25,7 +25,13 @@ no values to compare with):
 * the starting interval is ``[1e-3, 1]`` (u = 1 because the Frobenius-
   normalised input has spectral norm at most 1; l = 1e-3 as the smallest
   singular value the table is meant to lift);
-* no other modification than the printed safety factor is applied.
+* no other modification than the printed safety factor is applied;
+* once the interval has shrunk to within ``TINY`` of the point 1 (half-width
+  at most 1e-7, reached after about six steps from ``[1e-3, 1]``) the exchange
+  has nothing left to resolve in fp64; such steps take the construction's
+  limit, the quintic with ``p(1) = 1, p'(1) = p''(1) = 0``, i.e.
+  ``(15/8, -10/8, 3/8)``, which differs from the minimax row by about the
+  half-width.
 
 The minimax step is computed by the Remez exchange: solve for ``a, b, c, E``
 on a four-point reference, move the reference to the local extrema of
@@ -41,6 +47,9 @@ import numpy as np
 SAFETY_FACTOR = 1.05
 # Starting interval of the singular values (readings above).
 LOWER0, UPPER0 = 1e-3, 1.0
+# Half-width below which a step takes the limit row (readings above).
+TINY = 1e-7
+LIMIT_ROW = (15.0 / 8.0, -10.0 / 8.0, 3.0 / 8.0)
 
 
 def quintic(x, a, b, c):
@@ -95,8 +104,13 @@ def polar_express_steps(steps=5, lo=LOWER0, hi=UPPER0):
     ``[((a, b, c), (l, u), E), ...]``; the next interval is ``[1 - E, 1 + E]``."""
     out = []
     for _ in range(steps):
-        a, b, c, E = minimax_quintic(lo, hi)
-        out.append(((a, b, c), (lo, hi), E))
+        if lo >= 1.0 - TINY and hi <= 1.0 + TINY:
+            row = LIMIT_ROW
+            E = float(max(abs(1.0 - quintic(lo, *row)), abs(1.0 - quintic(hi, *row))))
+        else:
+            a, b, c, E = minimax_quintic(lo, hi)
+            row = (a, b, c)
+        out.append((row, (lo, hi), E))
         lo, hi = 1.0 - E, 1.0 + E
     return out
 

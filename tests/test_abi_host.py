@@ -207,3 +207,54 @@ def test_inputs_are_seeded_and_shaped():
     sv = torch.linalg.svdvals(g.double())
     assert abs(float(sv[0]) - 100.0) < 1e-3 and abs(float(sv[15]) - 1e-3) < 1e-5
     assert s.spike_rank == 16
+
+
+def test_polar_express_table_matches_the_oracle(lib):
+    """The library's Polar Express construction (its own Remez exchange, in
+    C++) against the oracle's (numpy), for the default start and others."""
+    import numpy as np
+    from oracle import polar_express as pe
+    for steps, lo, hi, s in [(5, 1e-3, 1.0, 1.05), (8, 1e-3, 1.0, 1.05), (5, 1e-2, 1.0, 1.0),
+                             (3, 0.1, 1.5, 1.02), (1, 0.5, 1.0, 1.05)]:
+        got = np.array(dm.dmuon_polar_express_coefficients(steps, lo, hi, s))
+        ref = np.array(pe.polar_express_rows(steps, lo, hi, s))
+        assert got.shape == (steps, 3)
+        assert np.max(np.abs(got - ref) / np.abs(ref)) <= 1e-6, (steps, lo, hi, s)
+
+
+def test_polar_express_argument_errors(lib):
+    out = (ctypes.c_float * 3)()
+    f = lib.dmuon_polar_express_coefficients
+    assert f(0, 1e-3, 1.0, 1.05, out) == -1
+    assert f(65, 1e-3, 1.0, 1.05, out) == -1
+    assert f(1, 0.0, 1.0, 1.05, out) == -1
+    assert f(1, 1.0, 1.0, 1.05, out) == -1
+    assert f(1, 1e-3, 1.0, 0.0, out) == -1
+    assert f(1, 1e-3, 1.0, 1.05, None) == -1
+    assert f(1, 1e-3, 1.0, 1.05, out) == 0
+
+
+def test_gram_range_check(lib):
+    """The Gram backend's fp16 range check: the default and the Polar Express
+    tables fit (the latter's first row, a ~ 8, b ~ -22, c ~ 15, is far past
+    the crude |a| + 2|b| + 4|c| <= 40 rule yet keeps every buffer small);
+    tables that could overflow a buffer are refused with the reason."""
+    ok, why = dm.dmuon_gram_check_coefficients(5)
+    assert ok and why == ""
+    assert dm.dmuon_gram_check_coefficients(5, dm.dmuon_polar_express_coefficients(5))[0]
+    assert dm.dmuon_gram_check_coefficients(5, dm.dmuon_polar_express_coefficients(5), restarts=())[0]
+    ok, why = dm.dmuon_gram_check_coefficients(8, restarts=())
+    assert not ok and "gain" in why          # one window of 8 default steps: gain 1.1e4
+    assert dm.dmuon_gram_check_coefficients(8, restarts=(3, 6))[0]
+    ok, why = dm.dmuon_gram_check_coefficients(1, [(1.0, 100.0, 0.0)])
+    assert not ok and "kappa R Z" in why     # 1024 x 101 at the top of the spectrum
+    ok, why = dm.dmuon_gram_check_coefficients(3, [(1.0, 25.0, 0.0)] * 3, restarts=())
+    assert not ok and "singular values" in why   # x + 25 x^3 sends 1 to 26
+    ok, _ = dm.dmuon_gram_check_coefficients(0)
+    assert ok
+    # argument errors
+    assert lib.dmuon_gram_check_coefficients(-1, None, None, 0, None, 0) == -1
+    assert lib.dmuon_gram_check_coefficients(65, None, None, 0, None, 0) == -1
+    assert lib.dmuon_gram_check_coefficients(5, None, None, 2, None, 0) == -1
+    nan = (ctypes.c_float * 3)(float("nan"), 0.0, 0.0)
+    assert lib.dmuon_gram_check_coefficients(1, nan, None, 0, None, 0) == -1

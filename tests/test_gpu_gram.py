@@ -158,6 +158,66 @@ def test_gram_deterministic_and_launch_count(handle, shapes, launches):
     assert handle.status()[0] == 0
 
 
+def _spiked(shape, seed):
+    """Gaussian bulk plus a rank-16 spike with singular values log-spaced
+    from 1e2 down to 1e-3 (the spiked workload's construction)."""
+    rng = np.random.default_rng(seed)
+    r, c = shape
+    Uq, _ = np.linalg.qr(rng.standard_normal((r, 16)))
+    Vq, _ = np.linalg.qr(rng.standard_normal((c, 16)))
+    G = rng.standard_normal((r, c)) + (Uq * np.logspace(2, -3, 16)) @ Vq.T
+    return torch.from_numpy(np.ascontiguousarray(G, dtype=np.float32))
+
+
+@pytest.mark.parametrize("path", ["gram", "gram_no_restart", "direct", "small"])
+def test_polar_express_table(path):
+    """The library's Polar Express table (dmuon_polar_express_coefficients)
+    on the GPU paths against the fp64 oracles run with the oracle's own table
+    (oracle.polar_express, an independent construction): the Gram backend with
+    its default restart and with none, the direct iteration, the small-matrix
+    kernel; random and spiked inputs (a square one included), ragged shapes."""
+    from oracle import polar_express as pe
+    table = dm.dmuon_polar_express_coefficients(5)
+    ref_table = pe.polar_express_rows(5)
+    assert dm.dmuon_gram_check_coefficients(5, table)[0]
+    if path == "small":
+        shapes, spiked = [(64, 256), (128, 512), (300, 100), (37, 5)], [(128, 512), (100, 100)]
+    else:
+        shapes = [(300, 700), (700, 300), (513, 1000), (200, 200), (255, 2050), (1024, 4096)]
+        spiked = [(300, 1000), (1000, 300), (512, 512)]
+    gen = torch.Generator().manual_seed(211)
+    ins = [torch.randn(s, generator=gen) for s in shapes] + [_spiked(s, 212 + i) for i, s in enumerate(spiked)]
+    shapes = shapes + spiked
+    if path == "gram_no_restart":
+        # Square Gaussian matrices have singular values near 0; without the
+        # restart the fp16 Gram matrix's rounding stays in all five steps and
+        # the Polar Express table's large first step leaves 3.9e-2 on a
+        # 200 x 200 one (an emulation of the kernels' roundings gives the same),
+        # so the no-restart run takes the rectangular inputs only.
+        keep = [i for i, s in enumerate(shapes) if s[0] != s[1]]
+        ins, shapes = [ins[i] for i in keep], [shapes[i] for i in keep]
+    outs = [torch.empty(s, device="cuda") for s in shapes]
+    with dm.Handle(0) as h2:
+        if path != "small":
+            dm.dmuon_set_small_path(h2.h, False)
+        if path.startswith("gram"):
+            restarts = () if path == "gram_no_restart" else None
+            h2.gram_newton_schulz(_dev(ins), outs, ns_steps=5, coeffs=table, restarts=restarts)
+        else:
+            h2.newton_schulz(_dev(ins), outs, ns_steps=5, coeffs=table)
+        assert h2.status()[0] == 0
+        if path == "small":
+            assert "small-matrix kernel %d;" % len(shapes) in dm.dmuon_plan_summary(h2.h)
+    for x, o, s in zip(ins, outs, shapes):
+        if path.startswith("gram"):
+            restarts = () if path == "gram_no_restart" else (2,)
+            ref = og.gram_newton_schulz(x.numpy(), 5, coeffs=ref_table, restarts=restarts)
+        else:
+            ref = oracle.newton_schulz(x.numpy(), 5, coeffs=ref_table)
+        e = rel_fro(o.cpu().numpy(), ref)
+        assert e <= NS_TOL, (path, s, e)
+
+
 def test_gram_argument_errors(handle):
     x = torch.randn((300, 900), device="cuda")
     o = torch.empty_like(x)

@@ -100,6 +100,18 @@ def test_narrow_interval_tends_to_the_osculating_quintic():
     assert (p(1 + h) - 2 * p(1.0) + p(1 - h)) / h ** 2 == pytest.approx(0.0, abs=1e-4)
 
 
+def test_longer_tables_extend_shorter_ones():
+    """Each row depends only on the rows before it, so a longer table starts
+    with the shorter one; past the point where the interval is within 1e-7 of
+    1 the rows are the limit quintic (15/8, -10/8, 3/8)."""
+    short, long_ = pe.polar_express_steps(5), pe.polar_express_steps(10)
+    for (r1, i1, e1), (r2, i2, e2) in zip(short, long_):
+        assert r1 == r2 and i1 == i2 and e1 == e2
+    tail = [r for r, (l, u), _ in long_ if l >= 1 - pe.TINY and u <= 1 + pe.TINY]
+    assert tail and all(r == (15 / 8, -10 / 8, 3 / 8) for r in tail)
+    assert long_[-1][2] < 1e-15
+
+
 def test_safety_factor_is_p_of_x_over_s():
     rows = pe.polar_express_rows(5)
     raw = [r for r, _, _ in pe.polar_express_steps(5)]
