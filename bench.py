@@ -91,7 +91,7 @@ def apply_traffic(workload):
         return None
     csrc = os.path.join(ROOT, "newton_schulz_nesterov_gb300", "csrc")
     src = b"".join(open(os.path.join(csrc, f), "rb").read()
-                   for f in ("ns_gemm.cu", "common.cuh", "ptx.cuh", "dmuon_api.cu"))
+                   for f in ("ns_gemm.cu", "common.cuh", "ptx.cuh", "plan.cuh"))
     if hashlib.sha1(src).hexdigest() != sha.group(1):
         return None
     return int(per.group(1)) * layers
