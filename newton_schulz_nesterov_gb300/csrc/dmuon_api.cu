@@ -19,7 +19,6 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
-#include <queue>
 #include <string>
 #include <vector>
 
@@ -259,8 +258,8 @@ size_t chunk_small_bytes(const Layout& L, int n) {
 }
 
 // Power-of-two scale of the Gram-space R and R Z of an m x m window: near m
-// (entries of R are ~1/m), at most 1024 so that kappa * |R Z| stays well
-// inside fp16 for coefficient rows with |a| + 2|b| + 4|c| <= 40.
+// (entries of R are ~1/m), at most 1024, the bound the coefficient table's
+// fp16 range check (gram_table_fits) assumes.
 float gram_kappa(int64_t m) {
   float k = 1.f;
   while (k * 2.f <= (float)std::min<int64_t>(m, 1024)) k *= 2.f;

@@ -11,8 +11,8 @@
 // the diagonal and write the transposed copy of each off-diagonal tile, the
 // tile saving the pages' SYRK kernels describe (section "newton_schulz").
 //
-// CTA layout (192 threads, one CTA per SM, persistent over a static
-// round-robin of work items):
+// CTA layout (192 threads, one CTA per SM, persistent over a static run of
+// work items dealt by the host, longest first to the least-loaded CTA):
 //   warp 0   TMA producer: 64-wide K blocks of both operands into a
 //            4-stage shared-memory ring (128-byte swizzle, 64x64 boxes)
 //   warp 1   TMEM allocator and single-thread tcgen05.mma issuer
