@@ -321,7 +321,7 @@ def run_ours(args, rank, world, local_rank):
     fl = flops.algorithmic_flops(shapes)
     value = fl * args.steps * world / sec / 1e12
 
-    # ---- dominant kernel roofline (B*X apply phase; tensor-bound)
+    # ---- dominant kernel roofline (the Z*X apply phase; tensor-bound)
     peak, peak_src = tensor_peak()
     # Each phase launches once per chunk and iteration; achieved rates divide
     # the phase's algorithmic work over the timed steps by its summed time.
@@ -330,9 +330,9 @@ def run_ours(args, rank, world, local_rank):
     if apply_n:
         achieved = flops.apply_flops(shapes, 5) * args.steps / (apply_ms / 1e3) / 1e12
         launches_per_step = apply_n / args.steps
-        kname = ("ns_gemm_pair_kernel<Apply> (B*X + a*X, 256x256 CTA-pair tiles)"
+        kname = ("ns_gemm_pair_kernel<Apply> (X' = Z*X, Z = aI + bA + cAA, 256x256 CTA-pair tiles)"
                  if "pairs" in dm.dmuon_plan_summary(h.h) else
-                 "ns_gemm_kernel<Apply> (B*X + a*X, 128x256 tiles)")
+                 "ns_gemm_kernel<Apply> (X' = Z*X, 128x256 tiles)")
         step_traffic = apply_traffic(args.workload)  # DRAM bytes of one iteration's Apply over all matrices
         roofline = {"kernel": kname, "bound": "tensor",
                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
