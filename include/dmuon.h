@@ -282,8 +282,10 @@ const char* dmuon_last_error(dmuon_handle_t h);
  * is how the failure path is exercised without faulting the GPU. */
 int dmuon_set_wait_timeout(dmuon_handle_t h, uint64_t ns);
 
-/* Tensor-core tiling of later plans: 0 = automatic (CTA pairs when the device
- * can co-schedule 2-CTA clusters, the default), 1 = single CTAs computing
+/* Tensor-core tiling of later plans: 0 = automatic (the default: CTA pairs when
+ * the device can co-schedule 2-CTA clusters, some chunked matrix has a short
+ * side above 128 and the chunked matrices give at least one 256x256 Gram
+ * super-tile per pair; single CTAs otherwise), 1 = single CTAs computing
  * 128x256 tiles, 2 = CTA pairs computing 256x256 tiles (cta_group::2).  The
  * result is the same maths with the same roundings; the choice only changes
  * speed.  It applies to the direct backend; the Gram backend always uses CTA
