@@ -405,6 +405,21 @@ int dmuon_gram_check_coefficients(int ns_steps, const float* coeffs,
                                   const int* restarts, int n_restarts,
                                   char* why, size_t why_len);
 
+/*
+ * Host-only preview of the plan a handle would build for this list, without
+ * a device: the tile kind the automatic choice (tile_mode 0) or the forced
+ * one (1 single CTAs, 2 CTA pairs) gives, the chunks, the work items per
+ * phase and how evenly they are dealt ("balance", as in
+ * dmuon_plan_summary), for a device with `clusters` co-resident 2-CTA
+ * clusters (0 = none) and `sms` SMs; balanced = 0 previews the strided
+ * dealing.  The small-matrix kernel is assumed on.  Writes a NUL-terminated
+ * summary into buf (truncated to len) and returns its full length, or
+ * DMUON_ERR_ARG for bad arguments (the Gram backend needs clusters >= 1).
+ */
+int dmuon_plan_preview(const dmuon_shape_t* shapes, int n_mats, int backend,
+                       int tile_mode, int clusters, int sms, int balanced,
+                       char* buf, size_t len);
+
 /* Static string for a status code. */
 const char* dmuon_error_string(int code);
 

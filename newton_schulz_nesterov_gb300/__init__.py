@@ -19,6 +19,7 @@ __all__ = [
     "dmuon_gram_newton_schulz", "dmuon_gram_newton_schulz_ptrs", "BACKENDS",
     "dmuon_adamw_step", "dmuon_adamw_step_ptrs", "dmuon_clip_grad_norm", "dmuon_clip_grad_norm_ptrs",
     "dmuon_workspace_bytes", "dmuon_polar_express_coefficients", "dmuon_gram_check_coefficients",
+    "dmuon_plan_preview",
     "dmuon_launch_count", "dmuon_last_error", "dmuon_profile_enable", "dmuon_profile_read",
     "dmuon_plan_summary", "dmuon_error_string", "dmuon_version", "Handle",
     "KIND_NAMES", "STATUS",
@@ -133,6 +134,9 @@ def load(path=None):
     L.dmuon_error_string.restype = ctypes.c_char_p
     L.dmuon_version.argtypes = []
     L.dmuon_version.restype = ctypes.c_char_p
+    L.dmuon_plan_preview.argtypes = [ctypes.POINTER(Shape), i32, i32, i32, i32, i32, i32, ctypes.c_char_p,
+                                     ctypes.c_size_t]
+    L.dmuon_plan_preview.restype = i32
     L.dmuon_polar_express_coefficients.argtypes = [i32, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                                    ctypes.POINTER(ctypes.c_float)]
     L.dmuon_polar_express_coefficients.restype = i32
@@ -224,6 +228,17 @@ def dmuon_polar_express_coefficients(steps=5, lower=1e-3, upper=1.0, safety=1.05
     _check(load().dmuon_polar_express_coefficients(int(steps), float(lower), float(upper), float(safety), out),
            "dmuon_polar_express_coefficients")
     return [(out[3 * k], out[3 * k + 1], out[3 * k + 2]) for k in range(int(steps))]
+
+
+def dmuon_plan_preview(shapes, backend="direct", tile_mode=0, clusters=76, sms=152, balanced=True):
+    """Host-only summary of the plan a handle would build for ``shapes`` on a
+    device with ``clusters`` 2-CTA clusters and ``sms`` SMs (GB300: 76, 152)."""
+    buf = ctypes.create_string_buffer(512)
+    rc = load().dmuon_plan_preview(_shape_array(shapes), len(shapes), BACKENDS[backend], int(tile_mode),
+                                   int(clusters), int(sms), 1 if balanced else 0, buf, 512)
+    if rc < 0:
+        raise DmuonError(rc, "dmuon_plan_preview")
+    return buf.value.decode()
 
 
 def dmuon_gram_check_coefficients(ns_steps=5, coeffs=None, restarts=None):

@@ -203,11 +203,30 @@ void free_plan(dmuon_ctx* h) {
 // CTA pairs unless single CTAs are requested, pairs are unavailable, or (in
 // automatic mode) every short side fits one 128-row tile, where a pair's
 // second CTA would only compute padding.
-bool use_pairs(const dmuon_ctx* h, const dmuon_shape_t* s, int n, bool gram = false) {
-  if (h->max_clusters <= 0) return false;
+// Dealing quality of phase q of a layout: the busiest processor's summed
+// item cost and the mean cost per processor (costs as item_cost).
+inline std::pair<double, double> deal_balance(const Layout& L, int q) {
+  const int P = L.procs[q], n_it = (int)L.items[q].size();
+  if (P <= 0) return {0.0, 0.0};
+  const bool strided = L.starts[q].empty();
+  double total = 0, top = 0;
+  for (int c = 0; c < P; ++c) {
+    double run = 0;
+    for (int w = strided ? c : L.starts[q][c]; w < (strided ? n_it : L.starts[q][c + 1]); w += strided ? P : 1)
+      run += (double)item_cost(L.items[q][w]);
+    total += run;
+    top = std::max(top, run);
+  }
+  return {top, total / P};
+}
+
+// Tile kind of a plan (max_clusters: resident 2-CTA clusters, 0 if none;
+// small_on: the small-matrix kernel takes the small matrices).
+bool choose_pairs(int max_clusters, int tile_mode, bool small_on, const dmuon_shape_t* s, int n, bool gram) {
+  if (max_clusters <= 0) return false;
   if (gram) return true;  // the Gram-space kernels exist for CTA pairs only
-  if (h->tile_mode == 1) return false;
-  if (h->tile_mode == 2) return true;
+  if (tile_mode == 1) return false;
+  if (tile_mode == 2) return true;
   // Automatic: pairs once some chunked matrix's short side exceeds one
   // 128-row tile and the chunked matrices give at least one 256 x 256 Gram
   // super-tile per CTA pair.  A list with fewer leaves most pairs idle and
@@ -216,12 +235,16 @@ bool use_pairs(const dmuon_ctx* h, const dmuon_shape_t* s, int n, bool gram = fa
   bool wide = false;
   int64_t items = 0;
   for (int i = 0; i < n; ++i) {
-    if (h->small_path && h->small_ok && is_small(s[i])) continue;  // the small-matrix kernel takes it
+    if (small_on && is_small(s[i])) continue;  // the small-matrix kernel takes it
     const int64_t m = std::min(s[i].rows, s[i].cols), T = cdiv(m, 256);
     wide = wide || m > kBM;
     items += T * (T + 1) / 2;
   }
-  return wide && items >= h->max_clusters;
+  return wide && items >= max_clusters;
+}
+
+bool use_pairs(const dmuon_ctx* h, const dmuon_shape_t* s, int n, bool gram = false) {
+  return choose_pairs(h->max_clusters, h->tile_mode, h->small_path && h->small_ok, s, n, gram);
 }
 
 int64_t chunk_limit(const dmuon_ctx* h) { return h->chunk_elems > 0 ? h->chunk_elems : kDefaultChunkElems; }
@@ -1485,25 +1508,13 @@ int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len) {
       for (int q = 0; q < 3; ++q) it[q] += ch.L.items[q].size();
     }
     // Dealing quality per phase: the busiest processor's item cost over the
-    // mean cost per processor, summed over chunks (1 = perfectly even; costs
-    // as item_cost).
+    // mean cost per processor, summed over chunks (1 = perfectly even).
     double busiest[3] = {0, 0, 0}, mean[3] = {0, 0, 0};
     for (const Chunk& ch : h->chunks)
       for (int q = 0; q < 3; ++q) {
-        const Layout& L = ch.L;
-        if (L.procs[q] <= 0) continue;
-        double total = 0, top = 0;
-        const bool strided = L.starts[q].empty();
-        const int P = L.procs[q], n_it = (int)L.items[q].size();
-        for (int c = 0; c < P; ++c) {
-          double run = 0;
-          for (int w = strided ? c : L.starts[q][c]; w < (strided ? n_it : L.starts[q][c + 1]); w += strided ? P : 1)
-            run += item_cost(L.items[q][w]);
-          total += run;
-          top = std::max(top, run);
-        }
-        busiest[q] += top;
-        mean[q] += total / L.procs[q];
+        const auto b = deal_balance(ch.L, q);
+        busiest[q] += b.first;
+        mean[q] += b.second;
       }
     double bal[3];
     for (int q = 0; q < 3; ++q) bal[q] = mean[q] > 0 ? busiest[q] / mean[q] : 1.0;
@@ -1517,6 +1528,52 @@ int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len) {
   } else {
     s += "no plan";
   }
+  if (buf && len) {
+    std::strncpy(buf, s.c_str(), len - 1);
+    buf[len - 1] = 0;
+  }
+  return (int)s.size();
+}
+
+int dmuon_plan_preview(const dmuon_shape_t* shapes, int n_mats, int backend, int tile_mode, int clusters,
+                       int sms, int balanced, char* buf, size_t len) {
+  if (n_mats < 0 || (n_mats > 0 && !shapes) || tile_mode < 0 || tile_mode > 2 || clusters < 0 || sms < 1 ||
+      (backend != DMUON_BACKEND_DIRECT && backend != DMUON_BACKEND_GRAM) ||
+      (backend == DMUON_BACKEND_GRAM && clusters < 1))
+    return DMUON_ERR_ARG;
+  if (n_mats > 0)
+    if (int rc = check_shapes(shapes, n_mats)) return rc;
+  const bool gram = backend == DMUON_BACKEND_GRAM;
+  std::vector<int> order;
+  int n_expl = 0;
+  const int n_large = plan_order(shapes, n_mats, true, order, gram, &n_expl);
+  std::vector<dmuon_shape_t> ps(n_mats);
+  for (int k = 0; k < n_mats; ++k) ps[k] = shapes[order[k]];
+  const bool pair = choose_pairs(clusters, tile_mode, true, shapes, n_mats, gram);
+  const int procs = pair ? clusters : sms;
+  size_t items[3] = {0, 0, 0}, chunks = 0, n_impl = 0;
+  double busiest[3] = {0, 0, 0}, mean[3] = {0, 0, 0};
+  for (const auto& cc : plan_chunks(ps.data(), n_expl, n_large, kDefaultChunkElems, gram)) {
+    Layout L;
+    make_layout(ps.data() + cc.first.first, cc.first.second, L, pair, procs, balanced != 0, gram, cc.second);
+    ++chunks;
+    if (cc.second) ++n_impl;
+    for (int q = 0; q < 3; ++q) {
+      items[q] += L.items[q].size();
+      const auto b = deal_balance(L, q);
+      busiest[q] += b.first;
+      mean[q] += b.second;
+    }
+  }
+  char line[384];
+  std::snprintf(line, sizeof line,
+                "matrices %d; backend %s; tiles %s; small-matrix kernel %d; chunks %zu (implicit-restart %zu); "
+                "items gram %zu gram2 %zu apply %zu; balance gram %.4f gram2 %.4f apply %.4f",
+                n_mats, gram ? "gram" : "direct", pair ? "256x256 CTA pairs" : "128x256 single CTAs",
+                n_mats - n_large, chunks, n_impl, items[0], items[1], items[2],
+                mean[0] > 0 ? busiest[0] / mean[0] : 1.0, mean[1] > 0 ? busiest[1] / mean[1] : 1.0,
+                mean[2] > 0 ? busiest[2] / mean[2] : 1.0);
+  const std::string s(line);
   if (buf && len) {
     std::strncpy(buf, s.c_str(), len - 1);
     buf[len - 1] = 0;

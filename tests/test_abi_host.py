@@ -258,3 +258,81 @@ def test_gram_range_check(lib):
     assert lib.dmuon_gram_check_coefficients(5, None, None, 2, None, 0) == -1
     nan = (ctypes.c_float * 3)(float("nan"), 0.0, 0.0)
     assert lib.dmuon_gram_check_coefficients(1, nan, None, 0, None, 0) == -1
+
+
+def _preview(shapes, **kw):
+    out = dm.dmuon_plan_preview(shapes, **kw)
+    fields = dict(part.strip().split(" ", 1) for part in out.split(";"))
+    bal = fields["balance"].split()
+    items = fields["items"].split()
+    return out, {"tiles": fields["tiles"], "chunks": int(fields["chunks"].split()[0]),
+                 "implicit": int(fields["chunks"].split("implicit-restart ")[1].rstrip(")")),
+                 "small": int(fields["small-matrix"].split()[-1]),
+                 "items": {items[i]: int(items[i + 1]) for i in range(0, 6, 2)},
+                 "balance": {bal[i]: float(bal[i + 1]) for i in range(0, 6, 2)}}
+
+
+def _pair_items(shapes):
+    """Work items of a CTA-pair plan counted from their definition: upper
+    256 x 256 super-tiles for the symmetric phases, all 256 x 256 output
+    tiles of the m x n iterate for the apply phase."""
+    cd = lambda a, b: -(-a // b)  # noqa: E731
+    g = a = 0
+    for r, c in shapes:
+        m, n = min(r, c), max(r, c)
+        T = cd(m, 256)
+        g += T * (T + 1) // 2
+        a += T * cd(n, 256)
+    return {"gram": g, "gram2": g, "apply": a}
+
+
+def test_plan_preview_items_dealing_and_chunks(lib):
+    """The host planner without a device: work-item counts match their
+    definition, longest-first dealing evens one Llama-3-8B layer's Gram list
+    (strided leaves the pairs that drew extra long tiles ~10 % behind), the
+    full set splits into 14 chunks of at most 2^29 elements, and the Gram
+    backend puts the 12 chunks of n >= 2m matrices on implicit restarts."""
+    layer = workloads.get("llama3_8b_1layer").shapes
+    _, p = _preview(layer)
+    assert p["tiles"] == "256x256 CTA pairs" and p["chunks"] == 1
+    assert p["items"] == _pair_items(layer)
+    assert p["balance"]["gram"] <= 1.02 and p["balance"]["apply"] <= 1.01
+    _, q = _preview(layer, balanced=False)
+    assert q["items"] == p["items"] and q["balance"]["gram"] >= 1.08
+    full = workloads.get("llama3_8b").shapes
+    _, f = _preview(full)
+    assert f["chunks"] == 14 and f["items"] == _pair_items(full) and f["balance"]["gram"] <= 1.02
+    _, gb = _preview(full, backend="gram")
+    assert gb["chunks"] == 14 and gb["implicit"] == 12
+
+
+def test_plan_preview_tile_choice(lib):
+    """Automatic tiles: CTA pairs only when some chunked matrix's short side
+    exceeds 128 and there is at least one Gram super-tile per pair; small
+    matrices go to the small-matrix kernel and do not count."""
+    d512 = workloads.get("tinymlp_d512").shapes            # 12 x 3 = 36 super-tiles
+    assert "single CTAs" in _preview(d512)[0]               # 36 < 76 pairs
+    assert "CTA pairs" in _preview(d512, clusters=36)[0]
+    assert "single CTAs" in _preview(d512, clusters=37)[0]
+    assert "CTA pairs" in _preview(d512, tile_mode=2)[0]
+    assert "single CTAs" in _preview(workloads.get("llama3_8b_1layer").shapes, tile_mode=1)[0]
+    assert "single CTAs" in _preview(d512, clusters=0, tile_mode=0)[0]
+    _, s = _preview(workloads.get("tinymlp_d128").shapes)
+    assert s["small"] == 12 and s["chunks"] == 0
+    _, t = _preview(workloads.get("tp_70b_mixed").shapes)
+    assert t["small"] == 512 and t["tiles"] == "256x256 CTA pairs" and t["items"]["gram"] == 32 * 33 // 2
+    assert "backend gram; tiles 256x256 CTA pairs" in _preview(d512, backend="gram")[0]
+
+
+def test_plan_preview_argument_errors(lib):
+    sh = (dm.Shape * 1)()
+    sh[0].rows, sh[0].cols = 64, 64
+    f = lib.dmuon_plan_preview
+    assert f(sh, 1, 1, 0, 0, 152, 1, None, 0) == -1      # Gram backend without clusters
+    assert f(sh, 1, 7, 0, 76, 152, 1, None, 0) == -1     # unknown backend
+    assert f(sh, 1, 0, 3, 76, 152, 1, None, 0) == -1     # unknown tile mode
+    assert f(sh, 1, 0, 0, 76, 0, 1, None, 0) == -1       # no SMs
+    assert f(None, 1, 0, 0, 76, 152, 1, None, 0) == -1
+    sh[0].rows = 0
+    assert f(sh, 1, 0, 0, 76, 152, 1, None, 0) == -1     # empty matrix
+    assert f(None, 0, 0, 0, 76, 152, 1, None, 0) > 0     # an empty list previews an empty plan
