@@ -42,6 +42,9 @@ def parse_args():
     p.add_argument("--workload", default="llama3_8b")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--e2e-readback", default="status", choices=["status", "weights"],
+                   help="e2e result read per step: the step's status through dmuon_get_status (4 B per matrix), "
+                        "or every updated weight matrix")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-aux", action="store_true")
@@ -544,14 +547,18 @@ def host_mem_available():
 def run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world):
     """The same step end to end through the public API with host buffers:
     every step copies its gradients in from pinned host memory and reads the
-    updated weights back to pinned host memory, inside the timed region
-    (W and M stay resident as optimizer state).  The step is issued as one
-    dmuon_step call per group of matrices (per layer for the Llama set) so
-    that group g's upload and group g-1's read-back run on two copy streams
-    while group g computes."""
+    step's result back, inside the timed region; W and M stay resident as
+    optimizer state.  The result read is the step's status through
+    dmuon_get_status (per-matrix flags, which waits for the step), or with
+    --e2e-readback weights every updated weight matrix into pinned host
+    memory.  The step is issued as one dmuon_step call per group of
+    matrices (per layer for the Llama set) so that group g's upload (and
+    group g-1's read-back) run on side streams while group g computes."""
     import torch
     import newton_schulz_nesterov_gb300 as dm
-    need = sum(g.numel() * 4 for g in Gs) + sum(x.numel() * 4 for x in Ws)
+    weights = args.e2e_readback == "weights"
+    n_mats = len(shapes)
+    need = sum(g.numel() * 4 for g in Gs) + (sum(x.numel() * 4 for x in Ws) if weights else 0)
     avail = host_mem_available()
     if avail is not None and need * world * 1.25 > avail:
         # every rank pins its own copies; leave the host room rather than risk its memory
@@ -560,7 +567,7 @@ def run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world):
                            % (need / 1e9, world, avail / 1e9)}
     try:
         Gh = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in Gs]
-        Wh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in Ws]
+        Wh = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in Ws] if weights else []
     except Exception as ex:  # host memory too small for pinned copies
         return {"value": None, "unit": "TFLOP/s (algorithmic)", "error": str(ex)[:200]}
     for g, gh in zip(Gs, Gh):
@@ -590,20 +597,25 @@ def run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world):
             dm.dmuon_step_ptrs(h.h, [wp[i] for i in grp], [gp[i] for i in grp],
                                [mp[i] for i in grp], [shapes[i] for i in grp], 0.02, 0.95, 5,
                                stream=stream)
-            done = torch.cuda.Event()
-            done.record(stream)
-            d2h_s.wait_event(done)
-            with torch.cuda.stream(d2h_s):
-                for i in grp:
-                    Wh[i].copy_(Ws[i], non_blocking=True)
+            if weights:
+                done = torch.cuda.Event()
+                done.record(stream)
+                d2h_s.wait_event(done)
+                with torch.cuda.stream(d2h_s):
+                    for i in grp:
+                        Wh[i].copy_(Ws[i], non_blocking=True)
         fin = torch.cuda.Event()
         fin.record(d2h_s)
         stream.wait_event(fin)
+        if not weights:
+            rc, _ = h.status(n_mats)   # the step's result: waits for it, reads its flags
+            if rc != 0:
+                raise RuntimeError("e2e status %d" % rc)
 
     one_step()  # plans the group shape list, fills the pointer-set cache
     torch.cuda.synchronize()
     h2d = sum(g.numel() * 4 for g in Gs)
-    d2h = sum(x.numel() * 4 for x in Ws)
+    d2h = sum(x.numel() * 4 for x in Ws) if weights else 4 * (n_mats + 1)   # flags and the error word
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -619,7 +631,8 @@ def run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world):
     return {"value": fl * args.e2e_steps * world / sec / 1e12, "unit": "TFLOP/s (algorithmic)",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
             "ms_per_step": 1e3 * sec / args.e2e_steps, "groups": len(groups),
-            "api": "dmuon_step per group, copies on two side streams"}
+            "readback": "updated weights" if weights else "step status (dmuon_get_status)",
+            "api": "dmuon_step per group, gradient uploads on a side stream"}
 
 
 def main():
