@@ -336,3 +336,71 @@ def test_plan_preview_argument_errors(lib):
     sh[0].rows = 0
     assert f(sh, 1, 0, 0, 76, 152, 1, None, 0) == -1     # empty matrix
     assert f(None, 0, 0, 0, 76, 152, 1, None, 0) > 0     # an empty list previews an empty plan
+
+
+def _gram_buffer_peaks(X, rows, restarts, kappa=1024.0):
+    """Largest magnitudes the Gram-space buffers reach for input X (fp64,
+    unrounded): kappa R, kappa R Z, Z, each window's factor and the product
+    of the window factors, following the Gram iteration's algebra."""
+    import numpy as np
+    m = X.shape[0]
+    eye = np.eye(m)
+    cuts = sorted({k for k in restarts if 0 < k < len(rows)})
+    bounds = [0] + cuts + [len(rows)]
+    peak = dict(kR=0.0, kRZ=0.0, Z=0.0, Q=0.0, total=0.0)
+    acc = eye
+    for s, e in zip(bounds, bounds[1:]):
+        R = X @ X.T
+        Q = eye
+        for a, b, c in rows[s:e]:
+            peak["kR"] = max(peak["kR"], kappa * np.abs(R).max())
+            Z = a * eye + b * R + c * R @ R
+            peak["Z"] = max(peak["Z"], np.abs(Z).max())
+            peak["kRZ"] = max(peak["kRZ"], kappa * np.abs(R @ Z).max())
+            Q = Z @ Q
+            peak["Q"] = max(peak["Q"], np.abs(Q).max())
+            R = Z @ R @ Z
+        acc = Q @ acc
+        peak["total"] = max(peak["total"], np.abs(acc).max())
+        X = Q @ X
+    return peak
+
+
+def test_gram_range_check_is_sound(lib):
+    """Every table the fp16 range check accepts keeps each Gram-space buffer
+    within the limits it promises (kappa R, kappa R Z and Z under 32768, a
+    window's factor under 8192, the accumulated factor under 32768) on inputs
+    built to reach each polynomial's extremes: singular values at 1, at the
+    points where |p| peaks, spread over (0, 1], and random ones."""
+    import numpy as np
+    rng = np.random.default_rng(31)
+    tables = [(None, (2,)), (dm.dmuon_polar_express_coefficients(5), (2,)),
+              (dm.dmuon_polar_express_coefficients(5), ()), ([(1.0, 20.0, 0.0)], ()), ([(3.0, -8.0, 6.0)] * 3, (1,))]
+    restart_sets = [(), (2,), (1, 3)]
+    you = [(4.0848, -6.8946, 2.927), (3.9505, -6.3029, 2.6377), (3.7418, -5.5913, 2.3037),
+           (2.8769, -3.1427, 1.2046), (2.8366, -3.0525, 1.2012)]
+    for _ in range(8):   # Newton-Schulz-like tables: the default rows perturbed by ~15 %
+        tables.append(([tuple(v * (1 + 0.15 * rng.standard_normal()) for v in r) for r in you],
+                       restart_sets[int(rng.integers(3))]))
+    checked = 0
+    for coeffs, restarts in tables:
+        steps = 5 if coeffs is None else len(coeffs)
+        ok, _ = dm.dmuon_gram_check_coefficients(steps, coeffs, restarts=restarts)
+        if not ok:
+            continue
+        checked += 1
+        rows = [tuple(float(v) for v in r) for r in (coeffs or [(4.0848, -6.8946, 2.927), (3.9505, -6.3029, 2.6377),
+                                                                 (3.7418, -5.5913, 2.3037), (2.8769, -3.1427, 1.2046),
+                                                                 (2.8366, -3.0525, 1.2012)])]
+        # singular values: 1, where the first step's |p| peaks on (0, 1], a spread, random
+        a, b, c = rows[0]
+        crit = [x for x in np.sqrt(np.roots([5 * c, 3 * b, a]).real.clip(0)) if 0 < x <= 1] if c else []
+        spectra = [np.ones(8), np.array(crit + [1.0] * (8 - len(crit))), np.linspace(0.05, 1, 8), rng.uniform(0, 1, 8)]
+        for sv in spectra:
+            U, _ = np.linalg.qr(rng.standard_normal((8, 8)))
+            V, _ = np.linalg.qr(rng.standard_normal((20, 8)))
+            X = (U * (sv / max(1.0, sv.max()))) @ V.T          # spectral norm <= 1
+            p = _gram_buffer_peaks(X, rows, restarts)
+            assert p["kR"] <= 32768 and p["kRZ"] <= 32768 and p["Z"] <= 32768, (rows, restarts, p)
+            assert p["Q"] <= 8192 and p["total"] <= 32768, (rows, restarts, p)
+    assert checked >= 6   # the perturbed tables that let singular values run past ~1.3 are refused
