@@ -174,3 +174,16 @@ def test_planted_slips_fail_the_pins(slip):
     assert _rel(got, ref) > 1e-3
     # and the unmodified routine passes the same check
     assert _rel(_run_with(og.gram_window_factor, G), ref) <= 1e-10
+
+
+@pytest.mark.parametrize("restarts", [(), (2,), (1, 3)])
+def test_gram_equals_direct_with_the_polar_express_table(restarts):
+    """The Gram algebra holds for any table, including the Polar Express
+    rows with their large first step (a ~ 8, b ~ -22, c ~ 15)."""
+    from oracle import polar_express as pe
+    rows = pe.polar_express_rows(5)
+    for shape in [(9, 23), (23, 9), (12, 12)]:
+        G = np.random.default_rng(hash((shape, restarts)) % 2**32).standard_normal(shape)
+        got = og.gram_newton_schulz(G, 5, coeffs=rows, restarts=restarts)
+        ref = oracle.newton_schulz(G, 5, coeffs=rows)
+        assert _rel(got, ref) <= 1e-9
