@@ -331,8 +331,13 @@ def run_ours(args, rank, world, local_rank):
     apply_ms, apply_n = prof["apply"]
     roofline = None
     if apply_n:
-        achieved = flops.apply_flops(shapes, 5) * args.steps / (apply_ms / 1e3) / 1e12
+        # the chunked path's matrices (the small-matrix kernel takes the others)
+        big = [(r, c) for r, c in shapes if min(r, c) > 128 or max(r, c) > 512]
+        achieved = flops.apply_flops(big, 5) * args.steps / (apply_ms / 1e3) / 1e12
         launches_per_step = apply_n / args.steps
+        # algorithmic DRAM bytes of an Apply launch writing X' (bf16 X read, Z read, X' written),
+        # averaged over the launches of one iteration: what `traffic` is measured against
+        alg_bytes = sum(2 * (2 * min(r, c) * max(r, c) + min(r, c) ** 2) for r, c in big) * 5 / launches_per_step
         kname = ("ns_gemm_pair_kernel<Apply> (X' = Z*X, Z = aI + bA + cAA, 256x256 CTA-pair tiles)"
                  if "pairs" in dm.dmuon_plan_summary(h.h) else
                  "ns_gemm_kernel<Apply> (X' = Z*X, 128x256 tiles)")
@@ -341,6 +346,7 @@ def run_ours(args, rank, world, local_rank):
                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "peak_source": peak_src,
                     "traffic": (step_traffic * 5 / launches_per_step) if step_traffic else None,
+                    "algorithmic_bytes": alg_bytes,
                     "launches_per_step": launches_per_step,
                     "avg_launch_ms": apply_ms / apply_n}
     phase = {k: {"ms_per_launch": (v[0] / v[1]) if v[1] else None, "launches": v[1],
