@@ -100,6 +100,29 @@ def apply_traffic(workload):
     return int(per.group(1)) * layers
 
 
+def apply_roofline(shapes, steps, apply_ms, apply_n, peak, peak_src, pairs, step_traffic, ns_steps=5):
+    """Roofline object of the Apply kernel from its summed CUDA-event time
+    (apply_ms over apply_n launches in `steps` timed steps): achieved
+    algorithmic TFLOP/s against the tensor peak, and per launch the measured
+    DRAM traffic (step_traffic: one iteration's Apply over all matrices, or
+    None) beside the algorithmic bytes of a launch writing X' (bf16 X read,
+    Z read, X' written)."""
+    from newton_schulz_nesterov_gb300 import flops
+    big = [(r, c) for r, c in shapes if min(r, c) > 128 or max(r, c) > 512]   # the chunked path's matrices
+    achieved = flops.apply_flops(big, ns_steps) * steps / (apply_ms / 1e3) / 1e12
+    launches_per_step = apply_n / steps
+    alg_bytes = sum(2 * (2 * min(r, c) * max(r, c) + min(r, c) ** 2) for r, c in big) * ns_steps / launches_per_step
+    kname = ("ns_gemm_pair_kernel<Apply> (X' = Z*X, Z = aI + bA + cAA, 256x256 CTA-pair tiles)" if pairs else
+             "ns_gemm_kernel<Apply> (X' = Z*X, 128x256 tiles)")
+    return {"kernel": kname, "bound": "tensor",
+            "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": peak_src,
+            "traffic": (step_traffic * ns_steps / launches_per_step) if step_traffic else None,
+            "algorithmic_bytes": alg_bytes,
+            "launches_per_step": launches_per_step,
+            "avg_launch_ms": apply_ms / apply_n}
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi sampled every 200 ms during the timed region."""
@@ -329,26 +352,9 @@ def run_ours(args, rank, world, local_rank):
     # Each phase launches once per chunk and iteration; achieved rates divide
     # the phase's algorithmic work over the timed steps by its summed time.
     apply_ms, apply_n = prof["apply"]
-    roofline = None
-    if apply_n:
-        # the chunked path's matrices (the small-matrix kernel takes the others)
-        big = [(r, c) for r, c in shapes if min(r, c) > 128 or max(r, c) > 512]
-        achieved = flops.apply_flops(big, 5) * args.steps / (apply_ms / 1e3) / 1e12
-        launches_per_step = apply_n / args.steps
-        # algorithmic DRAM bytes of an Apply launch writing X' (bf16 X read, Z read, X' written),
-        # averaged over the launches of one iteration: what `traffic` is measured against
-        alg_bytes = sum(2 * (2 * min(r, c) * max(r, c) + min(r, c) ** 2) for r, c in big) * 5 / launches_per_step
-        kname = ("ns_gemm_pair_kernel<Apply> (X' = Z*X, Z = aI + bA + cAA, 256x256 CTA-pair tiles)"
-                 if "pairs" in dm.dmuon_plan_summary(h.h) else
-                 "ns_gemm_kernel<Apply> (X' = Z*X, 128x256 tiles)")
-        step_traffic = apply_traffic(args.workload)  # DRAM bytes of one iteration's Apply over all matrices
-        roofline = {"kernel": kname, "bound": "tensor",
-                    "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "peak_source": peak_src,
-                    "traffic": (step_traffic * 5 / launches_per_step) if step_traffic else None,
-                    "algorithmic_bytes": alg_bytes,
-                    "launches_per_step": launches_per_step,
-                    "avg_launch_ms": apply_ms / apply_n}
+    pairs = "pairs" in dm.dmuon_plan_summary(h.h)
+    roofline = apply_roofline(shapes, args.steps, apply_ms, apply_n, peak, peak_src, pairs,
+                              apply_traffic(args.workload)) if apply_n else None
     phase = {k: {"ms_per_launch": (v[0] / v[1]) if v[1] else None, "launches": v[1],
                  "ms_per_step": v[0] / args.steps}
              for k, v in prof.items() if v[1]}

@@ -404,3 +404,21 @@ def test_gram_range_check_is_sound(lib):
             assert p["kR"] <= 32768 and p["kRZ"] <= 32768 and p["Z"] <= 32768, (rows, restarts, p)
             assert p["Q"] <= 8192 and p["total"] <= 32768, (rows, restarts, p)
     assert checked >= 6   # the perturbed tables that let singular values run past ~1.3 are refused
+
+
+def test_bench_apply_roofline_arithmetic():
+    """bench.py's roofline object from made-up timings: achieved rate, the
+    per-launch traffic and algorithmic bytes follow from the shapes."""
+    import bench
+    shapes = [(4096, 4096), (1024, 4096), (64, 256)]        # the last goes to the small-matrix kernel
+    r = bench.apply_roofline(shapes, steps=2, apply_ms=10.0, apply_n=10, peak=1000.0, peak_src="x",
+                             pairs=True, step_traffic=5e9)
+    fl = 5 * 2 * (4096 ** 3 + 1024 ** 2 * 4096)             # 2 m^2 n per iteration, 5 iterations
+    assert r["achieved"] == pytest.approx(fl * 2 / 0.010 / 1e12)
+    assert r["frac"] == pytest.approx(r["achieved"] / 1000.0)
+    assert r["launches_per_step"] == 5 and r["avg_launch_ms"] == 1.0
+    alg = 2 * (2 * 4096 * 4096 + 4096 ** 2) + 2 * (2 * 1024 * 4096 + 1024 ** 2)
+    assert r["algorithmic_bytes"] == pytest.approx(alg * 5 / 5)
+    assert r["traffic"] == pytest.approx(5e9 * 5 / 5)
+    assert "CTA-pair" in r["kernel"] and r["bound"] == "tensor"
+    assert bench.apply_roofline(shapes, 1, 1.0, 5, 1.0, "x", False, None)["traffic"] is None
