@@ -29,9 +29,11 @@ Readings of points the pages leave open:
 
 * a restart position ``k`` means "before step ``k`` (0-based)"; positions
   ``<= 0`` or ``>= ns_steps`` start no new window;
-* the coefficients default to the printed ``YOU_COEFFICIENTS`` table (the
-  pages' Gram default, Polar Express, is not printed); rows past the fifth
-  repeat the last one, as in the direct oracle.
+* the coefficients default to the Polar Express table, as the pages state for
+  ``gram_newton_schulz`` ("Defaults to POLAR_EXPRESS_COEFFICIENTS"); its
+  values are not printed, so the default is the table ``oracle.polar_express``
+  derives by the method's construction (``ns_steps`` rows; its own readings and
+  pins live there).
 
 In exact arithmetic the Gram backend equals the direct one for every
 restart set; the pins in ``tests/test_oracle_gram_pins.py`` check that,
@@ -40,8 +42,18 @@ the SVD closed form, and the structure of the factors.
 
 import numpy as np
 
+from .polar_express import polar_express_rows
 from .step import DEFAULT_EPS, coefficient_rows, frobenius_normalize, momentum_update, \
     nesterov_input, orient, update_scale, apply_update
+
+
+def gram_rows(ns_steps, coeffs=None):
+    """Per-step rows of the Gram backend: ``coeffs`` if given, else the
+    Polar Express table of ``ns_steps`` rows (DMuon "API Reference", section
+    *gram_newton_schulz*: coefficients default to POLAR_EXPRESS_COEFFICIENTS)."""
+    if coeffs is None and ns_steps > 0:
+        coeffs = polar_express_rows(ns_steps)
+    return coefficient_rows(ns_steps, coeffs)
 
 
 def restart_windows(ns_steps, restarts=(2,)):
@@ -79,7 +91,7 @@ def gram_newton_schulz_factors(G, ns_steps=5, coeffs=None, restarts=(2,), eps=DE
     output is ``O = Q_last ... Q_1 X0`` with ``X0`` the normalised oriented
     input, transposed back when ``transposed``.
     """
-    rows = coefficient_rows(ns_steps, coeffs)
+    rows = gram_rows(ns_steps, coeffs)
     Y, transposed = orient(G)
     X, normaliser = frobenius_normalize(Y, eps)
     segments = []

@@ -22,6 +22,7 @@ import pytest
 
 import oracle
 from oracle import gram as og
+from oracle import polar_express as pe
 
 SHAPES = [(7, 13), (13, 7), (16, 16), (5, 40), (40, 5), (1, 9), (9, 1), (3, 3)]
 RESTARTS = [(), (1,), (2,), (3,), (1, 3), (2, 4), (1, 2, 3, 4)]
@@ -45,10 +46,26 @@ def _svd_closed_form(G, rows, eps=1e-7):
 @pytest.mark.parametrize("restarts", RESTARTS)
 def test_gram_equals_direct(shape, restarts):
     G = np.random.default_rng(hash((shape, restarts)) % 2**32).standard_normal(shape)
+    # the Gram default (the Polar Express table) and the printed table
     got = og.gram_newton_schulz(G, 5, restarts=restarts)
-    ref = oracle.newton_schulz(G, 5)
+    ref = oracle.newton_schulz(G, 5, coeffs=pe.polar_express_rows(5))
     assert got.shape == G.shape
     assert _rel(got, ref) <= 1e-10
+    got = og.gram_newton_schulz(G, 5, coeffs=oracle.coefficient_rows(5), restarts=restarts)
+    assert _rel(got, oracle.newton_schulz(G, 5)) <= 1e-10
+
+
+def test_gram_default_table_is_polar_express():
+    """DMuon "API Reference", section gram_newton_schulz: the coefficients
+    default to POLAR_EXPRESS_COEFFICIENTS, here the table derived by
+    oracle.polar_express (its own pins), of ns_steps rows."""
+    G = np.random.default_rng(9).standard_normal((10, 17))
+    for ns in (1, 5, 7):
+        assert og.gram_rows(ns) == [tuple(r) for r in pe.polar_express_rows(ns)]
+        a = og.gram_newton_schulz(G, ns)
+        b = og.gram_newton_schulz(G, ns, coeffs=pe.polar_express_rows(ns))
+        assert np.array_equal(a, b)
+    assert og.gram_rows(0) == []
 
 
 @pytest.mark.parametrize("shape", [(6, 11), (11, 6), (8, 8)])
@@ -56,7 +73,7 @@ def test_gram_matches_svd_closed_form(shape):
     rng = np.random.default_rng(7)
     G = rng.standard_normal(shape)
     for ns in (1, 3, 5, 7):
-        rows = oracle.coefficient_rows(ns)
+        rows = pe.polar_express_rows(ns)
         got = og.gram_newton_schulz(G, ns, restarts=(2,))
         assert _rel(got, _svd_closed_form(G, rows)) <= 1e-10, ns
     coeffs = [(3.0, -3.2, 1.2), (2.5, -2.0, 0.5), (1.875, -1.25, 0.375)]
@@ -116,7 +133,7 @@ def test_single_window_factor_is_the_composed_polynomial_of_r():
     X0 = G / nrm
     U, S, _ = np.linalg.svd(X0, full_matrices=False)
     s = S.copy()
-    for a, b, c in oracle.coefficient_rows(5):
+    for a, b, c in pe.polar_express_rows(5):
         s = a * s + b * s ** 3 + c * s ** 5
     assert _rel(Q, (U * (s / S)) @ U.T) <= 1e-10
 
@@ -126,7 +143,8 @@ def test_muon_step_gram_equals_direct_step():
     for shape in [(12, 20), (20, 12)]:
         W, G, M = (rng.standard_normal(shape) for _ in range(3))
         for kw in [dict(), dict(nesterov=False), dict(wd=0.1, scale_mode=2), dict(ns_steps=3)]:
-            a = og.muon_step_gram(W, G, M, lr=0.05, mu=0.9, **kw)
+            rows = oracle.coefficient_rows(kw.get("ns_steps", 5))  # the direct default on both
+            a = og.muon_step_gram(W, G, M, lr=0.05, mu=0.9, coeffs=rows, **kw)
             b = oracle.muon_step(W, G, M, lr=0.05, mu=0.9, **kw)
             assert np.array_equal(a["M"], b["M"])
             assert _rel(a["W"] - W, b["W"] - W) <= 1e-10
