@@ -11,11 +11,13 @@ matrices/s.  Inputs (83.8 GB of fp32 W/G/M for the Llama-3-8B set) are far
 larger than the 129 MB L2, so no flush is needed between steps.
 
 ``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample
-of the same workload, on this machine's host cores.
+of the same workload (one matrix per step, cycling over its distinct
+shapes), on this machine's host cores.
 
-Multi-GPU (torchrun): every rank runs the whole workload as an independent
-replica (the matrices of a step are independent units; there is no exchange
-step on one owner), so scaling is weak; timing is max over ranks.
+Multi-GPU: under torchrun every rank runs the whole workload as an
+independent replica (the matrices of a step are independent units; there is
+no exchange step on one owner), so scaling is weak; timing is max over
+ranks.  ``--gpus N`` without torchrun starts the N ranks itself.
 """
 import argparse
 import json
@@ -42,9 +44,9 @@ def parse_args():
     p.add_argument("--workload", default="llama3_8b")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=3)
-    p.add_argument("--e2e-readback", default="status", choices=["status", "weights"],
-                   help="e2e result read per step: the step's status through dmuon_get_status (4 B per matrix), "
-                        "or every updated weight matrix")
+    p.add_argument("--e2e-readback", default="both", choices=["both", "weights", "status"],
+                   help="e2e result read per step: every updated weight matrix (reported as e2e), the step's "
+                        "status through dmuon_get_status (reported as e2e_status), or both")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-aux", action="store_true")
@@ -72,7 +74,8 @@ def tensor_peak():
     if pk:
         for key in ("bf16_tflops_sustained", "bf16_tflops"):
             if key in pk and pk[key]:
-                return float(pk[key]), "of measured (%s)" % key
+                # the products run kind::f16 with fp16 operands: nominally the same dense rate as bf16
+                return float(pk[key]), "of measured (%s; fp16 and bf16 share the nominal dense rate)" % key
     return FALLBACK_BF16_TFLOPS_SUSTAINED, "of fallback (sustained bf16, 1.7 PFLOP/s)"
 
 
@@ -105,7 +108,7 @@ def apply_roofline(shapes, steps, apply_ms, apply_n, peak, peak_src, pairs, step
     (apply_ms over apply_n launches in `steps` timed steps): achieved
     algorithmic TFLOP/s against the tensor peak, and per launch the measured
     DRAM traffic (step_traffic: one iteration's Apply over all matrices, or
-    None) beside the algorithmic bytes of a launch writing X' (bf16 X read,
+    None) beside the algorithmic bytes of a launch writing X' (fp16 X read,
     Z read, X' written)."""
     from newton_schulz_nesterov_gb300 import flops
     big = [(r, c) for r, c in shapes if min(r, c) > 128 or max(r, c) > 512]   # the chunked path's matrices
@@ -176,41 +179,68 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle
+CPU_SHAPE_BUDGET = 1.5e13   # algorithmic flops above which a shape is not timed on the host (~30 s)
+
+
 def oracle_sample(workload):
-    """Bounded CPU sample of a workload: layer-0 q, k, v of the Llama set,
-    else the first matrices up to a similar flop budget."""
-    from newton_schulz_nesterov_gb300 import workloads
-    w = workloads.get(workload)
-    if workload == "llama3_8b":
-        return [0, 1, 2], "layer-0 q (4096x4096), k, v (1024x4096): 3 of 224 matrices"
-    budget, idx, tot = 2.5e12, [], 0
-    for i, (r, c) in enumerate(w.shapes):
-        m, n = min(r, c), max(r, c)
-        f = 5 * (4 * m * m * n + 2 * m ** 3)
-        if idx and tot + f > budget:
-            break
-        idx.append(i)
-        tot += f
-    return idx, "first %d of %d matrices" % (len(idx), len(w.shapes))
-
-
-def time_oracle(workload, indices, reps=1):
-    import numpy as np
-    import oracle
+    """The CPU baseline's sample: one matrix per distinct shape of the
+    workload (the first of each), with the number of matrices of that shape,
+    for timing each once and extrapolating to the whole step by count.
+    Shapes above CPU_SHAPE_BUDGET flops are listed but not timed (their time
+    is extrapolated from the timed shapes' flop rate).
+    Returns ([(index, count, timed)], description)."""
     from newton_schulz_nesterov_gb300 import workloads, flops
     w = workloads.get(workload)
-    data = []
-    for i in indices:
-        data.append((workloads.weight(w, i).numpy(), workloads.grad(w, i, 0).numpy(),
-                     workloads.momentum(w, i).numpy()))
-    shapes = [w.shapes[i] for i in indices]
-    times = []
-    for _ in range(reps):
-        t0 = time.perf_counter()
-        for W, G, M in data:
-            oracle.muon_step(W, G, M, lr=float(np.float32(0.02)), mu=float(np.float32(0.95)))
-        times.append(time.perf_counter() - t0)
-    return times, flops.algorithmic_flops(shapes), len(indices)
+    first, count = {}, {}
+    for i, sh in enumerate(w.shapes):
+        first.setdefault(sh, i)
+        count[sh] = count.get(sh, 0) + 1
+    out = []
+    for sh, i in first.items():
+        out.append((i, count[sh], flops.algorithmic_flops([sh]) <= CPU_SHAPE_BUDGET))
+    timed = [w.shapes[i] for i, _, t in out if t]
+    desc = ("one matrix per distinct shape, timed once each: %s (of %d matrices); full step extrapolated by "
+            "shape count" % (", ".join("%dx%d" % s_ for s_ in timed), len(w.shapes)))
+    if any(not t for _, _, t in out):
+        desc += "; not timed (rate of the timed shapes): " + ", ".join(
+            "%dx%d" % w.shapes[i] for i, _, t in out if not t)
+    return out, desc
+
+
+def time_oracle_matrix(workload, i):
+    """Seconds of one fp64 oracle Muon step of matrix i of the workload."""
+    import numpy as np
+    import oracle
+    from newton_schulz_nesterov_gb300 import workloads
+    w = workloads.get(workload)
+    W, G, M = (workloads.weight(w, i).numpy(), workloads.grad(w, i, 0).numpy(), workloads.momentum(w, i).numpy())
+    t0 = time.perf_counter()
+    oracle.muon_step(W, G, M, lr=float(np.float32(0.02)), mu=float(np.float32(0.95)))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(workload):
+    """The fp64 oracle as it stands on this host's cores: one matrix per
+    distinct shape timed once, the rate over that sample, and the seconds of
+    a whole step extrapolated by shape count."""
+    from newton_schulz_nesterov_gb300 import workloads, flops
+    w = workloads.get(workload)
+    sample, desc = oracle_sample(workload)
+    secs, fl = 0.0, 0
+    per = {}
+    for i, cnt, timed in sample:
+        if timed:
+            t = time_oracle_matrix(workload, i)
+            per[i] = t
+            secs += t
+            fl += flops.algorithmic_flops([w.shapes[i]])
+    rate = fl / secs
+    full = sum(cnt * (per[i] if timed else flops.algorithmic_flops([w.shapes[i]]) / rate)
+               for i, cnt, timed in sample)
+    return {"value": rate / 1e12, "unit": "TFLOP/s (algorithmic)", "cores": cpu_threads(), "kind": "oracle",
+            "sample": desc, "seconds": secs,
+            "extrapolated": {"seconds_per_step": full, "tflops": flops.algorithmic_flops(w.shapes) / full / 1e12,
+                             "how": "per-shape oracle time x number of matrices of that shape"}}
 
 
 def cpu_threads():
@@ -224,24 +254,43 @@ def cpu_threads():
 
 
 def run_reference(args, rank):
+    """The fp64 oracle as the reference arm: each timed step is one matrix of
+    the workload's distinct shapes, in turn (warm-up steps take the smallest),
+    so the run stays within a few minutes; the rate is the sampled flops over
+    the sampled time, and the full step's seconds are extrapolated by shape
+    count."""
     if rank != 0:
         return
-    idx, desc = oracle_sample(args.workload)
+    from newton_schulz_nesterov_gb300 import workloads, flops
+    w = workloads.get(args.workload)
+    sample, desc = oracle_sample(args.workload)
+    timed = [(i, cnt) for i, cnt, t in sample if t]
+    smallest = min(timed, key=lambda ic: flops.algorithmic_flops([w.shapes[ic[0]]]))[0]
     for _ in range(args.warmup):
-        time_oracle(args.workload, idx, 1)
-    times, fl, nm = time_oracle(args.workload, idx, args.steps)
-    tot = sum(times)
-    value = fl * len(times) / tot / 1e12
+        time_oracle_matrix(args.workload, smallest)
+    secs, fl, per = 0.0, 0, {}
+    for k in range(args.steps):
+        i = timed[k % len(timed)][0]
+        t = time_oracle_matrix(args.workload, i)
+        per.setdefault(i, []).append(t)
+        secs += t
+        fl += flops.algorithmic_flops([w.shapes[i]])
+    value = fl / secs / 1e12
+    rate = fl / secs
+    full = sum(cnt * (statistics.mean(per[i]) if i in per else flops.algorithmic_flops([w.shapes[i]]) / rate)
+               for i, cnt, _ in sample)
     cores = cpu_threads()
     line = {
         "impl": "reference", "metric": "muon_step_tflops", "value": value,
         "unit": "TFLOP/s (algorithmic)", "n_gpus": args.gpus, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "matrices_per_s": nm * len(times) / tot,
-        "config": {"workload": args.workload, "sample": desc},
+        "data": "synthetic", "matrices_per_s": args.steps / secs,
+        "config": {"workload": args.workload, "sample": "each step one matrix, cycling over: " + desc},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s (algorithmic)", "cores": cores,
-                         "kind": "oracle", "sample": desc},
+                         "kind": "oracle", "sample": desc,
+                         "extrapolated": {"seconds_per_step": full,
+                                          "how": "per-shape oracle time x number of matrices of that shape"}},
         "e2e": {"value": value, "unit": "TFLOP/s (algorithmic)", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -379,15 +428,20 @@ def run_ours(args, rank, world, local_rank):
         gram = run_gram(args, Ws, Gs, Ms, shapes, stream, world, ms / args.steps, local_rank)
 
     # ---- end to end through the public API with host buffers
-    e2e = None
+    e2e = e2e_status = None
     if not args.no_e2e and args.e2e_steps > 0:
-        e2e = run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world)
+        if args.e2e_readback in ("both", "weights"):
+            e2e = run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world, weights=True)
+        if args.e2e_readback in ("both", "status"):
+            e2e_status = run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world, weights=False)
+            if e2e is None:
+                e2e = e2e_status
 
     line = {
         "metric": "muon_step_tflops", "value": value, "unit": "TFLOP/s (algorithmic)",
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "matrices_per_s": n * args.steps * world / sec,
         "dense_equiv_tflops": flops.dense_flops(shapes) * args.steps * world / sec / 1e12,
         "config": {"workload": args.workload, "matrices": n, "ns_steps": 5,
@@ -402,15 +456,12 @@ def run_ours(args, rank, world, local_rank):
         "phases": phase,
         "clocks": clk,
         "e2e": e2e,
+        "e2e_status": e2e_status,
         "aux": aux,
         "gram_backend": gram,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        idx, desc = oracle_sample(args.workload)
-        times, sfl, nm = time_oracle(args.workload, idx, 1)
-        line["cpu_baseline"] = {"value": sfl / times[0] / 1e12, "unit": "TFLOP/s (algorithmic)",
-                                "cores": cpu_threads(), "kind": "oracle", "sample": desc,
-                                "seconds": times[0]}
+        line["cpu_baseline"] = cpu_baseline(args.workload)
     h.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -556,19 +607,18 @@ def host_mem_available():
     return None
 
 
-def run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world):
+def run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world, weights=True):
     """The same step end to end through the public API with host buffers:
     every step copies its gradients in from pinned host memory and reads the
-    step's result back, inside the timed region; W and M stay resident as
-    optimizer state.  The result read is the step's status through
-    dmuon_get_status (per-matrix flags, which waits for the step), or with
-    --e2e-readback weights every updated weight matrix into pinned host
-    memory.  The step is issued as one dmuon_step call per group of
+    step's result back, inside the timed region; M stays resident as
+    optimizer state.  The result read is every updated weight matrix into
+    pinned host memory (weights=True), or the step's status through
+    dmuon_get_status (per-matrix flags, which waits for the step; W then stays
+    resident too).  The step is issued as one dmuon_step call per group of
     matrices (per layer for the Llama set) so that group g's upload (and
     group g-1's read-back) run on side streams while group g computes."""
     import torch
     import newton_schulz_nesterov_gb300 as dm
-    weights = args.e2e_readback == "weights"
     n_mats = len(shapes)
     need = sum(g.numel() * 4 for g in Gs) + (sum(x.numel() * 4 for x in Ws) if weights else 0)
     avail = host_mem_available()
@@ -647,11 +697,34 @@ def run_e2e(args, h, Ws, Gs, Ms, shapes, fl, stream, world):
             "api": "dmuon_step per group, gradient uploads on a side stream"}
 
 
+def free_port():
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def spawn_command(gpus, argv, port):
+    """Command line that reruns this script as `gpus` ranks on this node
+    (torchrun, rendezvous on 127.0.0.1), with the same arguments."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=%d" % gpus,
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+
+
 def main():
     args = parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # --gpus N without a launcher: start the N ranks here (each replica
+        # runs the whole workload; rank 0 prints the line)
+        cmd = spawn_command(args.gpus, sys.argv[1:], free_port())
+        os.execv(cmd[0], cmd)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit("bench.py: --gpus %d but WORLD_SIZE=%d" % (args.gpus, world))
     if args.impl == "reference":
         run_reference(args, rank)
         return

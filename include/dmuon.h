@@ -24,8 +24,14 @@
  * default five-row table used here).
  *
  * Precision: momentum and the update are fp32; the Newton-Schulz products
- * run on bf16 tensor cores with fp32 accumulation, with X, A, B held in bf16
- * between products; the last iteration's output goes to the update in fp32.
+ * run on 16-bit tensor cores (kind::f16 with fp16 operands) with fp32
+ * accumulation, with X, A, B held in fp16 between products, each with a
+ * power-of-two scale that keeps it in fp16's normal range (X0 = p U with p
+ * chosen from max |U|; later X as beta X, beta ~ sqrt(n); A as kappa X X^T,
+ * kappa ~ m): fp16's three extra mantissa bits over bf16 cut the rounding
+ * error about eightfold at the same tensor-core rate.  The last iteration's
+ * output goes to the update in fp32.  Coefficient tables that could drive a
+ * buffer past the fp16 range for some input are refused (DMUON_ERR_ARG).
  *
  * Threading/streams: a handle is not thread-safe.  Calls on one handle are
  * asynchronous on the given stream and must be issued on one stream (or be
@@ -76,9 +82,18 @@ typedef struct {
  * arithmetic; GRAM needs 3 m^2 n + 7 m^3 multiply-adds for five steps with
  * one restart against 7.5 m^2 n + 2.5 m^3 for DIRECT (symmetric products
  * count half), so it is cheaper whenever n > m.  GRAM keeps R and R Z in
- * fp16 scaled by a power of two near m (at most 1024), Z and Q in fp16
- * (bf16 for the Q X product); matrices taken by the small-matrix kernel
- * (dmuon_set_small_path) run the direct iteration either way. */
+ * fp16 scaled by a power of two near m (at most 1024), Z and Q in fp16, and
+ * restarts explicitly (X <- Q X, a new R from X); it never runs a window
+ * longer than two steps (a longer one is split, which leaves the result
+ * unchanged in exact arithmetic: the window products R Z and Z Q, symmetric
+ * only in exact arithmetic, are stored symmetric in fp16, and over three or
+ * more steps that costs accuracy on inputs with widely spread singular
+ * values).  Its default
+ * coefficients are the Polar Express table ("API Reference", sections
+ * "gram_newton_schulz" and "POLAR_EXPRESS_COEFFICIENTS";
+ * dmuon_polar_express_coefficients(ns_steps, 1e-3, 1, 1.05)).  Matrices
+ * taken by the small-matrix kernel (dmuon_set_small_path) run the direct
+ * iteration with the same table either way. */
 #define DMUON_BACKEND_DIRECT 0
 #define DMUON_BACKEND_GRAM   1
 
@@ -89,9 +104,10 @@ typedef struct {
     int   nesterov;       /* 1 = Nesterov lookahead input (default), 0 = M */
     int   scale_mode;     /* update scale: 0 = sqrt(max(1, rows/cols))
                            * (default), 1 = 1, 2 = 0.2*sqrt(max(rows,cols)) */
-    const float* coeffs;  /* NULL: the YOU_COEFFICIENTS rows, last row
-                           * repeated past five steps; else host memory of
-                           * ns_steps rows of (a, b, c), row-major          */
+    const float* coeffs;  /* NULL: DIRECT the YOU_COEFFICIENTS rows, last
+                           * row repeated past five steps; GRAM the Polar
+                           * Express rows; else host memory of ns_steps
+                           * rows of (a, b, c), row-major                  */
     int   backend;        /* DMUON_BACKEND_DIRECT (default) or _GRAM       */
     const int* restarts;  /* GRAM: restart positions (host), a position k
                            * starting a new window before step k (0-based);
@@ -119,13 +135,13 @@ int dmuon_create(dmuon_handle_t* out, int device);
 void dmuon_destroy(dmuon_handle_t h);
 
 /* Bytes of device memory a step over `shapes` allocates with the default
- * chunking (bf16 X ping/pong, A and B for the largest chunk, plus small
+ * chunking (fp16 X ping/pong, A and B for the largest chunk, plus small
  * per-matrix arrays), for either tiling.  Host only. */
 int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats,
                           size_t* out_bytes);
 
 /* As dmuon_workspace_bytes for a backend: DMUON_BACKEND_GRAM plans hold
- * X ping/pong plus seven m x m 16-bit buffers per matrix of the largest
+ * X ping/pong plus eight m x m fp16 buffers per matrix of the largest
  * chunk.  DMUON_ERR_ARG for an unknown backend.  Host only. */
 int dmuon_workspace_bytes_ex(const dmuon_shape_t* shapes, int n_mats, int backend, size_t* out_bytes);
 
@@ -140,9 +156,11 @@ int dmuon_workspace_bytes_ex(const dmuon_shape_t* shapes, int n_mats, int backen
  *   lr, mu      Muon learning rate and momentum coefficient.
  *   ns_steps    number of Newton-Schulz iterations, 0..DMUON_MAX_NS_STEPS.
  *   opts        NULL = defaults.  backend DMUON_BACKEND_GRAM selects the
- *               Gram-space iteration (DMUON_ERR_ARG for coefficient rows
- *               outside its fp16 range, see dmuon_gram_newton_schulz;
- *               DMUON_ERR_UNSUPPORTED without 2-CTA clusters).
+ *               Gram-space iteration (see dmuon_gram_newton_schulz;
+ *               DMUON_ERR_UNSUPPORTED without 2-CTA clusters).  Either
+ *               backend returns DMUON_ERR_ARG for a coefficient table that
+ *               could drive an fp16 buffer past its range for some input
+ *               (dmuon_last_error says which step and buffer).
  *   stream      a cudaStream_t (NULL = legacy default stream).
  *
  * The caller owns all matrix memory; pointers must be 16-byte aligned and
@@ -168,7 +186,8 @@ int dmuon_step(dmuon_handle_t h, float* const* params,
  * section "direct_newton_schulz"): outputs[i] = O of inputs[i], same shape,
  * fp32.  inputs[i] and outputs[i] are device fp32 rows_i x cols_i,
  * 16-byte aligned, and may not overlap.  coeffs: NULL = default table as in
- * dmuon_opts_t, else ns_steps host rows of (a,b,c).  eps <= 0 selects 1e-7.
+ * dmuon_opts_t, else ns_steps host rows of (a,b,c); DMUON_ERR_ARG for a table
+ * outside the fp16 range as in dmuon_step.  eps <= 0 selects 1e-7.
  */
 int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs,
                         float* const* outputs, const dmuon_shape_t* shapes,
@@ -178,10 +197,12 @@ int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs,
 /*
  * Standalone Newton-Schulz with the Gram-space backend (DMuon "API
  * Reference", section "gram_newton_schulz"): as dmuon_newton_schulz, with
- * restart positions `restarts` (host, n_restarts entries; NULL = {2}).
- * DMUON_ERR_ARG if the coefficient table could drive a Gram-space buffer
- * past the fp16 range for some input (dmuon_gram_check_coefficients, which
- * also says why); DMUON_ERR_UNSUPPORTED without 2-CTA clusters.
+ * restart positions `restarts` (host, n_restarts entries; NULL = {2}; a
+ * window longer than two steps is split) and coeffs NULL = the Polar
+ * Express table.  DMUON_ERR_ARG if the coefficient table could drive a
+ * Gram-space buffer past the fp16 range for some input
+ * (dmuon_gram_check_coefficients, which also says why);
+ * DMUON_ERR_UNSUPPORTED without 2-CTA clusters.
  */
 int dmuon_gram_newton_schulz(dmuon_handle_t h, const float* const* inputs,
                              float* const* outputs, const dmuon_shape_t* shapes,
@@ -231,14 +252,16 @@ int dmuon_clip_grad_norm(dmuon_handle_t h, float* const* grads,
  * cudaMalloc (a host framework whose allocator owns all device memory, a
  * plugin that is handed only its input and output buffers, a latency path
  * that cannot take cudaMalloc's implicit synchronisation).  It needs no
- * handle and allocates nothing: its scratch (bf16 iterate, products, tile
- * sums, descriptor, tensor maps, work lists) is one file-scope static device
- * array of about 12.9 MB that every GPU loading the library holds until
- * process exit.
+ * handle and allocates nothing: its scratch (fp16 iterate, products, tile
+ * sums and maxima, descriptor, tensor maps, work lists) is one file-scope
+ * static device array of about 13.1 MB that every GPU loading the library
+ * holds until process exit.
  *
  *   input, output  device fp32 rows x cols, row-major, 16-byte aligned, not
- *                  overlapping; output = O of input (same maths and
- *                  arithmetic as dmuon_newton_schulz)
+ *                  overlapping; output = O of input (the same maths as
+ *                  dmuon_newton_schulz on single-CTA kernels with the
+ *                  unfolded epilogue -- Z written as b A + c A A, a X added
+ *                  from X -- so roundings differ from dmuon_newton_schulz's)
  *   limits         min(rows, cols) <= 1024 and rows*cols <= 2^21, else
  *                  DMUON_ERR_ARG before anything is launched
  *   ns_steps, coeffs, eps   as in dmuon_newton_schulz
@@ -249,11 +272,15 @@ int dmuon_clip_grad_norm(dmuon_handle_t h, float* const* grads,
  *   stream         a cudaStream_t on the current device
  *
  * The first call on a device does a one-time set-up with that device current
- * (cudaGetSymbolAddress of the array, kernel attributes); make that first
- * call before any stream capture.  Every call shares the array and leaves
- * its contents behind; each call zeroes what must start at zero.  Calls
- * whose GPU work overlaps in time (unordered streams, several host threads)
- * race on the array.
+ * (cudaGetSymbolAddress of the array, kernel attributes); a set-up that
+ * failed for any reason but an unsupported device is retried by the next
+ * call.  Each call uploads its descriptor, maps and work lists with
+ * cudaMemcpyAsync from host memory, so it cannot be recorded into a CUDA
+ * graph: while `stream` is being captured it returns DMUON_ERR_ARG and
+ * touches nothing.  Every call shares the array and leaves its contents
+ * behind; each call zeroes what must start at zero.  Calls whose GPU work
+ * overlaps in time (unordered streams, several host threads) race on the
+ * array.
  */
 int dmuon_newton_schulz_noalloc(const float* input, float* output,
                                 int64_t rows, int64_t cols, int ns_steps,
@@ -326,7 +353,7 @@ int dmuon_set_balanced_dealing(dmuon_handle_t h, int on);
  * iterations and the update -- in one CTA, with the iterate in shared memory
  * and the products in tensor memory; all such matrices share one launch.
  * Off: they run through the chunked tensor-core path like the others.  Same
- * maths and bf16 roundings either way (the summation order inside a product
+ * maths and fp16 roundings either way (the summation order inside a product
  * differs, so results agree to rounding, not bitwise).  Returns
  * DMUON_ERR_UNSUPPORTED if it cannot be enabled on this device. */
 int dmuon_set_small_path(dmuon_handle_t h, int on);
@@ -392,9 +419,10 @@ int dmuon_polar_express_coefficients(int steps, double lower, double upper,
  * only): follows the largest singular value the iterate can reach (1 for
  * the normalised input, then max |p_k| over [0, u] after step k) and
  * bounds every fp16 buffer for all inputs -- the step factor Z, kappa R and
- * kappa R Z (kappa <= 1024) at half the fp16 maximum, each restart window's
- * factor at 8192 and the factor accumulated over all windows at 32768.
- *   coeffs    host, 3 * ns_steps floats, or NULL for the default table.
+ * kappa R Z (kappa <= 1024) at half the fp16 maximum and each restart
+ * window's factor (windows of at most two steps) at 8192.
+ *   coeffs    host, 3 * ns_steps floats, or NULL for the backend's default
+ *             (the Polar Express table of ns_steps rows).
  *   restarts  host, n_restarts entries, or NULL for {2}.
  *   why       host buffer of why_len bytes for the reason (may be NULL).
  * DMUON_OK if the table fits, DMUON_ERR_ARG otherwise (or for bad

@@ -27,8 +27,19 @@ std::vector<std::pair<int, int>> restart_windows(int ns_steps, const std::vector
   cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
   std::vector<std::pair<int, int>> w;
   int start = 0;
-  for (int k : cuts) { w.push_back({start, k}); start = k; }
-  if (ns_steps > start) w.push_back({start, ns_steps});
+  auto add = [&](int k0, int k1) {
+    // A window of len > kMaxGramWindow steps becomes ceil(len / kMaxGramWindow)
+    // windows as even as possible, the longer ones first.
+    const int len = k1 - k0, parts = (len + kMaxGramWindow - 1) / kMaxGramWindow;
+    int a = k0;
+    for (int i = 0; i < parts; ++i) {
+      const int l = len / parts + (i < len % parts ? 1 : 0);
+      w.push_back({a, a + l});
+      a += l;
+    }
+  };
+  for (int k : cuts) { add(start, k); start = k; }
+  if (ns_steps > start) add(start, ns_steps);
   return w;
 }
 
@@ -170,26 +181,62 @@ void set_why(char* why, size_t len, const char* fmt, int k, double v) {
 
 }  // namespace
 
-// The Gram-space buffers are fp16 (largest finite value 65504).  Following
-// the largest singular value the iterate can reach -- 1 for the normalised
+// Every stored buffer is fp16 (largest finite value 65504).  Following the
+// largest singular value the iterate can reach -- 1 for the normalised
 // input, then u' = max over [0, u] of |p_k| after step k -- bounds every
 // buffer over all inputs: with Gram eigenvalues in [0, u^2], the step's
 // factor Z = a I + b R + c R^2 has |Z| <= max |Z(l)|, kappa R and
 // kappa R Z have at most kappa u^2 and kappa max |l Z(l)| (kappa <= 1024),
-// a window's factor Q at most the product of its steps' max |Z|, and the
-// accumulated factor of implicit restarts the product over all windows.
-// Limits: 32768 (half the fp16 maximum, for rounding) for kappa R, kappa R Z,
-// Z and the accumulated factor; 8192 for a window's Q, whose entries are
-// multiplied into R at a restart.
+// and a window's factor Q at most the product of its steps' max |Z|.
+// Limits: 32768 (half the fp16 maximum, for rounding) for kappa R, kappa R Z
+// and Z; 8192 for a window's Q.  The iterate itself, stored as beta X with
+// beta <= 1024, stays below 1024 u <= 32768 wherever kappa u^2 does.  Below:
+// Z is stored without a scale, so each row needs a >= 1/64 (kMinLinear): the
+// identity part a I keeps Z's significant entries in fp16's normal range,
+// where without it the entries of c A A (about s^4 for the singular values s
+// of a normalised m x n input, s^2 ~ 1/m) fall into the subnormals for m of
+// a few hundred.  Every Newton-Schulz step has a = p'(0) > 0 (the factor by
+// which it lifts small singular values); a < 1/64 is no such step.
+constexpr double kMinLinear = 1.0 / 64.0;
+bool direct_table_fits(int ns_steps, const float* coeffs, char* why, size_t why_len) {
+  constexpr double kKappa = 1024.0, kLimit = 32768.0;
+  double u = 1.0;
+  for (int k = 0; k < ns_steps; ++k) {
+    const float* r = coefficient_row(coeffs, k);
+    const double q[3] = {r[0], r[1], r[2]};
+    if (!(q[0] >= kMinLinear)) {
+      set_why(why, why_len, "step %d: a = %.4g, below 1/64: Z = a I + b A + c A A is stored in fp16 without a "
+              "scale and needs its identity part (every Newton-Schulz step has a = p'(0) > 0)", k, q[0]);
+      return false;
+    }
+    if (kKappa * u * u > kLimit) {
+      set_why(why, why_len, "step %d: singular values may reach %.4g, past the fp16 range of kappa X X^T", k, u);
+      return false;
+    }
+    const double zmax = max_abs_factor(q, u * u);
+    if (zmax > kLimit) {
+      set_why(why, why_len, "step %d: the step factor Z may reach %.4g, past fp16", k, zmax);
+      return false;
+    }
+    u = max_abs_quintic(q, u);
+  }
+  return true;
+}
+
 bool gram_table_fits(int ns_steps, const float* coeffs, const std::vector<int>& restarts, char* why,
                      size_t why_len) {
   constexpr double kKappa = 1024.0, kLimit = 32768.0, kWindowGain = 8192.0;
-  double u = 1.0, total = 1.0;
+  double u = 1.0;
   for (const auto& w : restart_windows(ns_steps, restarts)) {
     double gain = 1.0;
     for (int k = w.first; k < w.second; ++k) {
       const float* r = coefficient_row(coeffs, k);
       const double q[3] = {r[0], r[1], r[2]};
+      if (!(q[0] >= kMinLinear)) {
+        set_why(why, why_len, "step %d: a = %.4g, below 1/64: the fp16 step factor Z = a I + b R + c R R needs "
+                "its identity part (every Newton-Schulz step has a = p'(0) > 0)", k, q[0]);
+        return false;
+      }
       const double L = u * u;
       if (kKappa * L > kLimit) {
         set_why(why, why_len, "step %d: singular values may reach %.4g, past the fp16 range of kappa R", k,
@@ -213,11 +260,6 @@ bool gram_table_fits(int ns_steps, const float* coeffs, const std::vector<int>& 
               w.second, gain);
       return false;
     }
-    total *= gain;
-  }
-  if (total > kLimit) {
-    set_why(why, why_len, "after %d steps: the accumulated factor's gain %.4g exceeds 32768", ns_steps, total);
-    return false;
   }
   if (kKappa * u * u > kLimit) {
     set_why(why, why_len, "after %d steps: singular values may reach %.4g, past the fp16 range of kappa R",
@@ -275,6 +317,12 @@ int dmuon_gram_check_coefficients(int ns_steps, const float* coeffs, const int* 
   std::vector<int> r;
   if (restarts) r.assign(restarts, restarts + n_restarts);
   else r.push_back(2);
+  std::vector<float> pe;
+  if (!coeffs && ns_steps > 0) {  // the backend's default: the Polar Express table
+    pe.resize(3 * (size_t)ns_steps);
+    if (dmuon_polar_express_coefficients(ns_steps, 1e-3, 1.0, 1.05, pe.data()) != DMUON_OK) return DMUON_ERR_ARG;
+    coeffs = pe.data();
+  }
   return gram_table_fits(ns_steps, coeffs, r, why, why_len) ? DMUON_OK : DMUON_ERR_ARG;
 }
 

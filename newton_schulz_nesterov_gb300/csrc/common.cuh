@@ -7,6 +7,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,20 +20,48 @@ namespace dmuon {
 // One matrix of the packed list, oriented so that the Newton-Schulz iterate
 // X is m x n with m <= n (m = short side).  X, A and B live in the handle's
 // workspace; W, G, M are the caller's (see MatPtrs).
+//
+// The iterate and the products are fp16 with power-of-two scales that keep
+// their entries inside fp16's normal range (fp16 has three more mantissa
+// bits than bf16; power-of-two scaling is exact):
+//   X[0] holds p U (oriented, p a per-matrix power of two chosen by the
+//        momentum pass so that max |p U| lies in [2^6, 2^14]);
+//   X[k] (after the first product) holds beta' X with beta' = beta / nu
+//        (beta ~ sqrt(n), a power of two; nu = ||X0||_F rounded down to a
+//        power of two when below 1/2, else 1 -- X0 = U / (||U|| + eps) has
+//        a norm far below 1 when ||U|| is far below eps), so the iterate's
+//        entries stay near 1 whatever the input's scale;
+//   A holds kappa X X^T, kappa ~ m (at most 1024);
+//   B holds Z = a I + b A + c A A (unscaled; its entries are O(a)).
 struct MatDesc {
   int64_t rows, cols;      // weight shape (row-major fp32)
   int64_t m, n;            // oriented iterate shape, m = min(rows, cols)
   int64_t ldx;             // leading dimension (elements) of X buffers
   int64_t lda;             // leading dimension (elements) of A and B
-  __nv_bfloat16* X[2];     // ping/pong iterate, m x n row-major
-  __nv_bfloat16* A;        // Gram X X^T, m x m
-  __nv_bfloat16* B;        // b*A + c*A*A, m x m
+  __half* X[2];            // ping/pong iterate, m x n row-major
+  __half* A;               // kappa X X^T, m x m
+  __half* B;               // Z (or b*A + c*A*A), m x m
   int64_t tile0;           // first momentum tile of this matrix
   int32_t tiles_c;         // momentum tiles along cols
   int32_t transposed;      // rows > cols
   float scale;             // update scale of this matrix
+  float kappa;             // scale of A: largest power of two <= min(m, 1024)
+  float beta;              // power of two nearest sqrt(n) (times 1/nu per call: bvec)
   float pad_;
 };
+
+// Power-of-two scales of a matrix's fp16 buffers (host and device).
+__host__ __device__ inline float scale_kappa(int64_t m) {
+  float k = 1.f;
+  while (k * 2.f <= (float)(m < 1024 ? m : 1024)) k *= 2.f;
+  return k;
+}
+__host__ __device__ inline float scale_beta(int64_t n) {
+  // 2^round(log2(sqrt(n))): the largest power of two whose square is at most 2n
+  float b = 1.f;
+  while ((double)(2.f * b) * (double)(2.f * b) <= 2.0 * (double)n) b *= 2.f;
+  return b;
+}
 
 // Caller pointers of one call (uploaded only when they change).
 struct MatPtrs {
@@ -92,7 +121,8 @@ struct GemmArgs {
   int fold;                // Gram2 adds a*I (B becomes Z = aI + B); Apply then skips its a*X term
   int final_mode;          // Apply phase: kWriteX / kUpdateW / kWriteO
   float lr, decay;         // W <- decay*W - lr*scale*O
-  const float* svec;       // per-matrix 1/(||U||_F + eps)
+  const float* svec;       // per-matrix s/p: X[0] times this is U / (||U||_F + eps)
+  const float* bvec;       // per-matrix beta': X[k] (k >= 1) holds beta' X
   int* err;                // device error word (bit 0: wait timeout)
   unsigned long long timeout_ns;  // wait without progress before giving up (0 = 4 s)
 };
@@ -107,6 +137,13 @@ __device__ __forceinline__ WorkRange work_range(const int* starts, int proc, int
   return WorkRange{proc, n_items, nproc};
 }
 
+// Momentum pass.  X[0] = fp16(p U) with p = pscale[matrix], a power of two
+// kept from the previous step (the norm is only known after the pass).  The
+// finalisation checks max |U| * p against [2^6, 2^14] -- no fp16 overflow,
+// no precision lost to subnormals -- and, when it misses, picks a new p and
+// flags the matrix; the redo pass (redo = 1) then rewrites X[0] and the tile
+// sums of the flagged matrices from G and the updated M (the same U, bit for
+// bit) and a second finalisation completes them.
 struct MomArgs {
   const MatDesc* mats;
   const MatPtrs* ptrs;
@@ -116,20 +153,29 @@ struct MomArgs {
   float mu;
   int nesterov;
   int ns_only;                 // 1: U = G (standalone NS), no momentum
-  float* partials;             // per-tile sum of squares of U
+  float* partials;             // per-tile sum of squares of p U
+  float* tmax;                 // per-tile max |U| (written by the first pass only)
+  const float* pscale;         // per-matrix prescale p
+  const int* redo;             // per-matrix redo flags (redo pass)
+  int redo_pass;               // 0: momentum pass; 1: rewrite flagged matrices only
 };
 
 struct FinalizeArgs {
   const MatDesc* mats;
   const int64_t* tile_prefix;
   const float* partials;
+  const float* tmax;
   int n_mats;
   float eps;
-  float* svec;
+  float* svec;                 // s / p
+  float* bvec;                 // beta' = beta / nu, the scale of X after the first product
+  float* pscale;               // p, replaced when it misses its window
+  int* redo;                   // per-matrix: 1 = X[0] must be rewritten with the new p
   int* flags;
+  int redo_pass;               // 1: finish the flagged matrices only, clearing their flag
 };
 
-struct Update0Args {          // ns_steps == 0: O = s*U straight to W / out
+struct Update0Args {          // ns_steps == 0: O = (s/p) X[0] straight to W / out
   const MatDesc* mats;
   const MatPtrs* ptrs;
   const int64_t* tile_prefix;

@@ -6,10 +6,16 @@
 //   ns_small    every small matrix (oriented m <= 128, n <= 512) in one
 //               launch, one CTA per matrix running its whole step
 //   then, per chunk of the other matrices:
-//   mom_norm    M <- mu*M + G, U, X0 = bf16(U or U^T), tile sums of U^2
-//   finalize    s = 1/(||U||_F + eps) per matrix
-//   ns_steps x [ Gram (A = X X^T) -> Gram2 (B = bA + cAA) -> Apply (X' = aX + BX) ]
+//   mom_norm    M <- mu*M + G, U, X0 = fp16(p U or p U^T), tile sums of
+//               (p U)^2 and tile maxima of |U|
+//   finalize    s = 1/(||U||_F + eps) per matrix, or a new power of two p
+//               for a matrix whose p U missed fp16's comfortable range
+//   mom_norm, finalize (redo pass): rewrite X0 of those matrices; both
+//               return at once when there are none
+//   ns_steps x [ Gram (A = X X^T) -> Gram2 (Z = aI + bA + cAA) -> Apply (X' = Z X) ]
 //   the last Apply updates W in place (or writes O for the standalone NS)
+// All stored iterates and products are fp16 with power-of-two scales
+// (MatDesc); the tensor cores accumulate in fp32.
 //
 // Plan order: the large matrices (in the caller's order, chunked), then the
 // small ones.  Device pointer sets and flags are kept in plan order; the
@@ -61,16 +67,14 @@ bool get_encoder() {
   return g_encode != nullptr;
 }
 
-// 16-bit (bf16 by default, else fp16) row-major rows x cols with leading
-// dimension ld (elements): 64x64 boxes, 128-byte swizzle, zero fill outside
-// the matrix.
-bool encode_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld, bool fp16 = false) {
+// fp16 row-major rows x cols with leading dimension ld (elements): 64x64
+// boxes, 128-byte swizzle, zero fill outside the matrix.
+bool encode_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld) {
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
   cuuint32_t box[2] = {(cuuint32_t)kBox, (cuuint32_t)kBox};
   cuuint32_t estr[2] = {1, 1};
-  return g_encode(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
-                  strides, box, estr,
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -92,10 +96,13 @@ struct Chunk {
   CUtensorMap* d_maps = nullptr;
   int64_t* d_prefix = nullptr;
   float* d_partials = nullptr;
-  float* d_svec = nullptr;
+  float* d_tmax = nullptr;        // per momentum tile: max |U|
+  float* d_svec = nullptr;        // per matrix: s/p
+  float* d_bvec = nullptr;        // per matrix: beta', the scale of the iterate after the first product
+  float* d_pscale = nullptr;      // per matrix: the prescale p of X[0] (kept across steps)
+  int* d_redo = nullptr;          // per matrix: X[0] to be rewritten with a new p
   int4* d_items[3] = {nullptr, nullptr, nullptr};
   int* d_starts[3] = {nullptr, nullptr, nullptr};
-  bool implicit = false;          // gram plans: restarts without forming X (n >= 2m)
   GramDesc* d_gd = nullptr;       // gram plans: per-matrix Gram-space buffers
   CUtensorMap* d_gmaps = nullptr; // gram plans: kGramBufs maps per matrix
 };
@@ -279,62 +286,28 @@ std::vector<std::pair<int, int>> split_chunks(const dmuon_shape_t* shapes, int n
   return out;
 }
 
-// Bytes of one chunk's device arrays (descriptors, maps, prefix, partials,
-// scale vector, work lists).
+// Bytes of one chunk's device arrays (descriptors, maps, prefix, tile sums and
+// maxima, scale, prescale and redo vectors, work lists).
 size_t chunk_small_bytes(const Layout& L, int n) {
   const bool gram = !L.goff.empty();
   return rup(sizeof(MatDesc) * n, 256) + rup(sizeof(CUtensorMap) * kMapsPerMat * n, 256) +
-         rup(8 * (n + 1), 256) + rup(4 * L.tile_prefix[n], 256) + rup(4 * n, 256) +
+         rup(8 * (n + 1), 256) + 2 * rup(4 * L.tile_prefix[n], 256) + 4 * rup(4 * n, 256) +
          rup(16 * L.items[0].size(), 256) + rup(16 * L.items[1].size(), 256) + rup(16 * L.items[2].size(), 256) +
          rup(4 * (L.items[0].size() + 1), 256) + rup(4 * (L.items[1].size() + 1), 256) +
          rup(4 * (L.items[2].size() + 1), 256) +
          (gram ? rup(sizeof(GramDesc) * n, 256) + rup(sizeof(CUtensorMap) * kGramBufs * n, 256) : 0);
 }
 
-// Power-of-two scale of the Gram-space R and R Z of an m x m window: near m
-// (entries of R are ~1/m), at most 1024, the bound the coefficient table's
-// fp16 range check (gram_table_fits) assumes.
-float gram_kappa(int64_t m) {
-  float k = 1.f;
-  while (k * 2.f <= (float)std::min<int64_t>(m, 1024)) k *= 2.f;
-  return k;
-}
-
 // Plan order: positions [0, n_large) hold the matrices run by the chunked
 // tensor-core path (caller order), the rest the small ones (caller order).
-//
-// Gram plans order the chunked matrices further: those restarting
-// explicitly (n < 2m) first, then those restarting implicitly (n >= 2m), so
-// that every chunk holds one kind; *n_explicit counts the first kind.
-inline bool gram_implicit(const dmuon_shape_t& s) {
-  return std::max(s.rows, s.cols) >= 2 * std::min(s.rows, s.cols);
-}
-
-int plan_order(const dmuon_shape_t* shapes, int n, bool small_path, std::vector<int>& order, bool gram = false,
-               int* n_explicit = nullptr) {
+int plan_order(const dmuon_shape_t* shapes, int n, bool small_path, std::vector<int>& order) {
   order.clear();
   for (int i = 0; i < n; ++i)
-    if (!(small_path && is_small(shapes[i])) && !(gram && gram_implicit(shapes[i]))) order.push_back(i);
-  const int n_expl = (int)order.size();
-  if (gram)
-    for (int i = 0; i < n; ++i)
-      if (!(small_path && is_small(shapes[i])) && gram_implicit(shapes[i])) order.push_back(i);
+    if (!(small_path && is_small(shapes[i]))) order.push_back(i);
   const int n_large = (int)order.size();
   for (int i = 0; i < n; ++i)
     if (small_path && is_small(shapes[i])) order.push_back(i);
-  if (n_explicit) *n_explicit = n_expl;
   return n_large;
-}
-
-// Chunks of a plan: greedy runs over [0, n_expl) and over [n_expl, n_large)
-// separately (gram plans), each flagged with its restart kind.
-std::vector<std::pair<std::pair<int, int>, bool>> plan_chunks(const dmuon_shape_t* ps, int n_expl, int n_large,
-                                                              int64_t limit, bool gram) {
-  std::vector<std::pair<std::pair<int, int>, bool>> out;
-  for (const auto& c : split_chunks(ps, n_expl, limit)) out.push_back({c, false});
-  for (const auto& c : split_chunks(ps + n_expl, n_large - n_expl, limit))
-    out.push_back({{c.first + n_expl, c.second}, gram});
-  return out;
 }
 
 // Host-side plan sizes (no device work): workspace of the largest chunk and
@@ -342,17 +315,15 @@ std::vector<std::pair<std::pair<int, int>, bool>> plan_chunks(const dmuon_shape_
 void plan_sizes(const dmuon_shape_t* shapes, int n, bool pair, int64_t limit, bool small_path, size_t* ws,
                 size_t* small, bool gram = false) {
   std::vector<int> order;
-  int n_expl = 0;
-  const int n_large = plan_order(shapes, n, small_path, order, gram, &n_expl);
+  const int n_large = plan_order(shapes, n, small_path, order);
   std::vector<dmuon_shape_t> ps(n);
   for (int k = 0; k < n; ++k) ps[k] = shapes[order[k]];
   *ws = 256;
   *small = rup(sizeof(MatPtrs) * n * kPtrSlots, 256) + rup(4 * n, 256) + 256 +
            rup(sizeof(SmallDesc) * (n - n_large), 256);
-  for (const auto& cc : plan_chunks(ps.data(), n_expl, n_large, limit, gram)) {
-    const auto& c = cc.first;
+  for (const auto& c : split_chunks(ps.data(), n_large, limit)) {
     Layout L;
-    make_layout(ps.data() + c.first, c.second, L, pair, 1, true, gram, cc.second);  // sizes do not depend on procs
+    make_layout(ps.data() + c.first, c.second, L, pair, 1, true, gram);  // sizes do not depend on procs
     *ws = std::max(*ws, L.ws_bytes);
     *small += chunk_small_bytes(L, c.second);
   }
@@ -369,26 +340,24 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
   h->plan_chunk_elems = chunk_limit(h);
   h->plan_balanced = h->balanced;
   h->plan_small = h->small_path && h->small_ok;
-  int n_expl = 0;
-  h->n_large = plan_order(shapes, n, h->plan_small, h->order, gram, &n_expl);
+  h->n_large = plan_order(shapes, n, h->plan_small, h->order);
   std::vector<dmuon_shape_t> ps(n);
   for (int k = 0; k < n; ++k) ps[k] = shapes[h->order[k]];
   const int n_small = n - h->n_large;
   h->small_descs.resize(n_small);
   for (int k = 0; k < n_small; ++k)
     h->small_descs[k] = SmallDesc{ps[h->n_large + k].rows, ps[h->n_large + k].cols, h->n_large + k, 1.f};
-  const auto parts = plan_chunks(ps.data(), n_expl, h->n_large, h->plan_chunk_elems, gram);
+  const auto parts = split_chunks(ps.data(), h->n_large, h->plan_chunk_elems);
   h->chunks.resize(parts.size());
   h->ws_bytes = 256;
   h->small_bytes = rup(sizeof(MatPtrs) * n * kPtrSlots, 256) + rup(4 * n, 256) + 256 +
                    rup(sizeof(SmallDesc) * n_small, 256);
   for (size_t c = 0; c < parts.size(); ++c) {
     Chunk& ch = h->chunks[c];
-    ch.i0 = parts[c].first.first;
-    ch.n = parts[c].first.second;
-    ch.implicit = parts[c].second;
+    ch.i0 = parts[c].first;
+    ch.n = parts[c].second;
     make_layout(ps.data() + ch.i0, ch.n, ch.L, h->plan_pair, h->plan_pair ? h->max_clusters : h->num_sms,
-                h->plan_balanced, gram, ch.implicit);
+                h->plan_balanced, gram);
     h->ws_bytes = std::max(h->ws_bytes, ch.L.ws_bytes);
     h->small_bytes += chunk_small_bytes(ch.L, ch.n);
   }
@@ -418,7 +387,11 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
     ch.d_maps = (CUtensorMap*)carve(sizeof(CUtensorMap) * kMapsPerMat * cn);
     ch.d_prefix = (int64_t*)carve(8 * (cn + 1));
     ch.d_partials = (float*)carve(4 * L.tile_prefix[cn]);
+    ch.d_tmax = (float*)carve(4 * L.tile_prefix[cn]);
     ch.d_svec = (float*)carve(4 * cn);
+    ch.d_bvec = (float*)carve(4 * cn);
+    ch.d_pscale = (float*)carve(4 * cn);
+    ch.d_redo = (int*)carve(4 * cn);
     for (int q = 0; q < 3; ++q) ch.d_items[q] = (int4*)carve(16 * L.items[q].size());
     for (int q = 0; q < 3; ++q) ch.d_starts[q] = (int*)carve(4 * (L.items[q].size() + 1));
     if (gram) {
@@ -430,27 +403,26 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
     std::vector<GramDesc> gds(gram ? cn : 0);
     for (int i = 0; i < cn; ++i) {
       MatDesc& d = L.mats[i];
-      d.X[0] = (__nv_bfloat16*)(ws + L.xoff[i]);
+      d.X[0] = (__half*)(ws + L.xoff[i]);
       d.X[1] = d.X[0] + d.m * d.ldx;
-      d.A = (__nv_bfloat16*)(ws + L.aoff[i]);
-      d.B = (__nv_bfloat16*)(ws + L.boff[i]);
+      d.A = (__half*)(ws + L.aoff[i]);
+      d.B = (__half*)(ws + L.boff[i]);
       d.scale = 1.f;
       bool ok = encode_map(&maps[kMapsPerMat * i + 0], d.X[0], d.m, d.n, d.ldx) &&
                 encode_map(&maps[kMapsPerMat * i + 1], d.X[1], d.m, d.n, d.ldx) &&
                 encode_map(&maps[kMapsPerMat * i + 2], d.A, d.m, d.m, d.lda) &&
                 encode_map(&maps[kMapsPerMat * i + 3], d.B, d.m, d.m, d.lda);
       if (gram) {
-        // Gram plans: A and B above both name the bf16 Q buffer, so the
+        // Gram plans: A and B above both name the window's last Q, so the
         // direct Apply kernel computes Q X.
         GramDesc& gd = gds[i];
         gd.m = d.m;
         gd.ld = d.lda;
-        gd.kappa = gram_kappa(d.m);
+        gd.kappa = d.kappa;
         gd.inv_kappa = 1.f / gd.kappa;
         for (int b = 0; b < kGramBufs && ok; ++b) {
-          const int64_t off = L.goff[(size_t)i * kGramBufs + b];
-          gd.buf[b] = off < 0 ? nullptr : (uint16_t*)(ws + off);   // unused in explicit chunks
-          if (off >= 0) ok = encode_map(&gmaps[kGramBufs * i + b], gd.buf[b], d.m, d.m, d.lda, b != kGbQb);
+          gd.buf[b] = (uint16_t*)(ws + L.goff[(size_t)i * kGramBufs + b]);
+          ok = encode_map(&gmaps[kGramBufs * i + b], gd.buf[b], d.m, d.m, d.lda);
         }
       }
       if (!ok) {
@@ -463,6 +435,11 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
       }
     }
     e = cudaMemcpy(ch.d_mats, L.mats.data(), sizeof(MatDesc) * cn, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) {
+      const std::vector<float> ones(cn, 1.f);  // first prescale guess; corrected by the first step
+      e = cudaMemcpy(ch.d_pscale, ones.data(), 4 * cn, cudaMemcpyHostToDevice);
+    }
+    if (e == cudaSuccess) e = cudaMemset(ch.d_redo, 0, 4 * cn);
     if (e == cudaSuccess) e = cudaMemcpy(ch.d_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(ch.d_prefix, L.tile_prefix.data(), 8 * (cn + 1), cudaMemcpyHostToDevice);
     if (gram && e == cudaSuccess) e = cudaMemcpy(ch.d_gd, gds.data(), sizeof(GramDesc) * cn, cudaMemcpyHostToDevice);
@@ -620,25 +597,30 @@ void flat_plan(FlatPlan& fp, const std::vector<FlatDesc>& descs, const std::vect
 
 bool is_vec4(const void* p, int64_t numel) { return (((uintptr_t)p & 15u) == 0) && (numel % 4 == 0); }
 
-// The launch sequence of one chunk: momentum/normalise, norm, then
-// ns_steps x (Gram, Gram2, Apply), the last Apply writing W (or O).
-// Momentum, Nesterov input, bf16 iterate and the per-matrix norm of a chunk.
+// Momentum, Nesterov input, the fp16 iterate X0 = p U and the per-matrix norm
+// of a chunk: the momentum pass, the finalisation, then the redo pass and a
+// second finalisation for matrices whose prescale p missed its window (both
+// return at once when none did).
 int run_chunk_norm(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float mu, float eps,
                    int nesterov, int ns_only, cudaStream_t stream) {
   const Layout& L = ch.L;
   const int n = ch.n;
   const int64_t nt = L.tile_prefix[n];
+  const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
   cudaError_t e;
-  {
-    MomArgs a{ch.d_mats, dptrs, ch.d_prefix, n, nt, mu, nesterov, ns_only, ch.d_partials};
-    const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
-    LaunchGuard g(h, stream, DMUON_KIND_MOMENTUM);
-    if ((e = launch_mom(a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "mom_norm launch", e);
-  }
-  {
-    FinalizeArgs a{ch.d_mats, ch.d_prefix, ch.d_partials, n, eps, ch.d_svec, h->d_flags + ch.i0};
-    LaunchGuard g(h, stream, DMUON_KIND_FINALIZE);
-    if ((e = launch_finalize(a, stream)) != cudaSuccess) return fail(h, cuda_err(e), "finalize launch", e);
+  for (int pass = 0; pass < 2; ++pass) {
+    {
+      MomArgs a{ch.d_mats, dptrs, ch.d_prefix, n, nt, mu, nesterov, ns_only, ch.d_partials, ch.d_tmax,
+                ch.d_pscale, ch.d_redo, pass};
+      LaunchGuard g(h, stream, DMUON_KIND_MOMENTUM);
+      if ((e = launch_mom(a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "mom_norm launch", e);
+    }
+    {
+      FinalizeArgs a{ch.d_mats, ch.d_prefix, ch.d_partials, ch.d_tmax, n, eps, ch.d_svec, ch.d_bvec, ch.d_pscale,
+                     ch.d_redo, h->d_flags + ch.i0, pass};
+      LaunchGuard g(h, stream, DMUON_KIND_FINALIZE);
+      if ((e = launch_finalize(a, stream)) != cudaSuccess) return fail(h, cuda_err(e), "finalize launch", e);
+    }
   }
   return DMUON_OK;
 }
@@ -677,6 +659,7 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
       a.lr = lr;
       a.decay = decay;
       a.svec = ch.d_svec;
+      a.bvec = ch.d_bvec;
       a.err = h->d_err;
       a.timeout_ns = h->wait_timeout_ns;
       if (a.n_items <= 0) continue;
@@ -696,11 +679,11 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
 
 
 // Newton-Schulz of a chunk with the Gram-space backend and the update.
-// Per window: R~ = kappa s^2 X X^T, then per step Z (copied to Q at the
-// window's first step), Q' = Z Q (later steps), W~ = R~ Z and R~' = Z W~
-// (all but the window's last step); between windows and at the end the
-// direct Apply kernel forms Q X (a = 0), the last one updating W (or
-// writing O).
+// Per window: R~ = kappa X X^T, then per step Z (the window's first Q),
+// Q' = Z Q (later steps), W~ = R~ Z and R~' = Z W~ (all but the window's last
+// step); between windows and at the end the direct Apply kernel forms Q X
+// (a = 0), the last one updating W (or writing O).  Windows longer than
+// kMaxGramWindow steps are split (restart_windows).
 int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, int ns_steps,
                    const float* coeffs, float wd, int ns_only, const std::vector<int>& restarts,
                    cudaStream_t stream) {
@@ -728,6 +711,7 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
     a.starts = L.starts[ph].empty() ? nullptr : ch.d_starts[ph];
     a.n_items = x_operand ? n_gram : n_prod;
     a.svec = ch.d_svec;
+    a.bvec = ch.d_bvec;
     a.err = h->d_err;
     a.timeout_ns = h->wait_timeout_ns;
     if (a.n_items <= 0) return DMUON_OK;
@@ -746,11 +730,12 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
     a.src = src;
     a.ca = 0.f;          // X' = Q X
     a.fold = 1;          // no a*X term to add: skip reading X in the epilogue
-    a.first = first;     // the first window's X is U unnormalised: times s
+    a.first = first;     // the first window's X is X0 = p U: times s/p
     a.final_mode = mode;
     a.lr = lr;
     a.decay = decay;
     a.svec = ch.d_svec;
+    a.bvec = ch.d_bvec;
     a.err = h->d_err;
     a.timeout_ns = h->wait_timeout_ns;
     if (a.n_items <= 0) return DMUON_OK;
@@ -769,11 +754,10 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
   // One window of steps [k0, k1): per step Z (into Z0 / Z1 alternately),
   // Q' = Z Q from the second step on (the first step's Q is its Z, read
   // from that Z buffer), and, unless it is the window's last step, W = R Z
-  // and R' = Z W.  The window's final factor goes to `qlast` (bf16 when it
-  // is kGbQb); only a one-step window copies its Z there.  Q' products of
-  // later steps alternate between Q0 and Q1; `qlast` must differ from the
-  // buffer the last Q' reads (window_qlast below picks it).
-  auto window = [&](int k0, int k1, int qlast) -> int {
+  // and R' = Z W.  The window's final factor goes to kGbQb (a one-step
+  // window writes its Z there too); Q' products of earlier steps alternate
+  // between Q0 and Q1.
+  auto window = [&](int k0, int k1) -> int {
     int rc_ = kGbR0, zc = kGbZ0, qc = -1;
     for (int k = k0; k < k1; ++k) {
       const float* row = coeffs ? coeffs + 3 * k : kYouCoefficients[std::min(k, 4)];
@@ -788,18 +772,14 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
         a.c1 = row[1];
         a.p1pow = -1;
         a.diag = row[0];
-        if (wfirst && wlast) {
-          a.out2 = qlast;
-          a.out2_bf16 = qlast == kGbQb ? 1 : 0;
-        }
+        if (wfirst && wlast) a.out2 = kGbQb;
         if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
       }
       if (!wfirst) {  // Q' = Z Q
         GramArgs a = blank();
         a.opA = zc;
         a.opB = qc;
-        a.out = wlast ? qlast : (qc == kGbQ0 ? kGbQ1 : kGbQ0);
-        a.out_bf16 = a.out == kGbQb ? 1 : 0;
+        a.out = wlast ? kGbQb : (qc == kGbQ0 ? kGbQ1 : kGbQ0);
         if ((rc = prod(a, false, DMUON_KIND_GS_PROD))) return rc;
         qc = a.out;
       } else {
@@ -822,70 +802,6 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
     }
     return DMUON_OK;
   };
-  // A Q buffer for a window's final factor that its last Q' does not read:
-  // that Q' reads the first step's Z (two steps), or Q0 / Q1 alternating
-  // from Q0 on the second step (three or more steps).
-  auto window_qlast = [](int len) { return (len >= 3 && len % 2 == 1) ? kGbQ1 : kGbQ0; };
-  if (ch.implicit) {
-    // Restarts without forming X: R_start = R~ of the window's start (Rs);
-    // at a restart W = R_start Qh, R~ = Qh W (the Gram matrix of Qh X), and
-    // the previous window's factor Qh joins the accumulator; at the end
-    // Q_total = Qh_last * accumulator, and O = s Q_total X0.
-    const int nw = (int)windows.size();
-    {
-      GramArgs a = blank();
-      a.src = 0;
-      a.out = kGbR0;
-      a.out2 = nw > 1 ? kGbRs : -1;
-      a.gpow = 1;
-      a.use_s2 = 1;
-      if ((rc = prod(a, true, DMUON_KIND_GS_GRAM))) return rc;
-    }
-    int acc = -1, qh = -1;  // accumulated factor (A0/A1; -1 = identity), last window's factor
-    for (int wi = 0; wi < nw; ++wi) {
-      const bool final_w = wi == nw - 1;
-      if (wi > 0) {
-        GramArgs t = blank();  // W = R_start Qh
-        t.opA = kGbRs;
-        t.opB = qh;
-        t.out = kGbW;
-        if ((rc = prod(t, false, DMUON_KIND_GS_PROD))) return rc;
-        GramArgs r = blank();  // R~ = Qh W, also the next window's R_start
-        r.opA = qh;
-        r.opB = kGbW;
-        r.out = kGbR0;
-        r.out2 = final_w ? -1 : kGbRs;
-        if ((rc = prod(r, false, DMUON_KIND_GS_PROD))) return rc;
-        if (acc < 0) {
-          acc = qh;  // the first window's factor was written to A0
-        } else {
-          GramArgs q = blank();  // accumulator <- Qh * accumulator
-          q.opA = qh;
-          q.opB = acc;
-          q.out = acc ^ kGbA0 ^ kGbA1;
-          if ((rc = prod(q, false, DMUON_KIND_GS_PROD))) return rc;
-          acc ^= kGbA0 ^ kGbA1;
-        }
-      }
-      const int k0 = windows[wi].first, k1 = windows[wi].second;
-      const int len = k1 - k0;
-      int qlast;
-      if (nw == 1) qlast = kGbQb;            // the only window: straight to the bf16 factor
-      else if (wi == 0) qlast = kGbA0;       // becomes the accumulator
-      else qlast = window_qlast(len);
-      if ((rc = window(k0, k1, qlast))) return rc;
-      qh = qlast;
-    }
-    if (nw > 1) {  // Q_total = Qh * accumulator, in bf16 for the product with X
-      GramArgs q = blank();
-      q.opA = qh;
-      q.opB = acc;
-      q.out = kGbQb;
-      q.out_bf16 = 1;
-      if ((rc = prod(q, false, DMUON_KIND_GS_PROD))) return rc;
-    }
-    return apply(0, true, ns_only ? kWriteO : kUpdateW);
-  }
   int src = 0;
   bool first = true;
   for (size_t wi = 0; wi < windows.size(); ++wi) {
@@ -894,16 +810,15 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
       src ^= 1;
       first = false;
     }
-    {  // R~ = kappa s^2 X X^T (s only while X is still unnormalised)
+    {  // R~ = kappa X X^T of the true X: (s/p)^2 on the first window's X0 = p U, 1/beta^2 after
       GramArgs a = blank();
       a.src = src;
       a.out = kGbR0;
       a.gpow = 1;
-      a.use_s2 = first ? 1 : 0;
+      a.xscale = first ? 1 : 2;
       if ((rc = prod(a, true, DMUON_KIND_GS_GRAM))) return rc;
     }
-    // every explicit window ends in the bf16 factor read by the Apply kernel
-    if ((rc = window(windows[wi].first, windows[wi].second, kGbQb))) return rc;
+    if ((rc = window(windows[wi].first, windows[wi].second))) return rc;
   }
   return apply(src, first, ns_only ? kWriteO : kUpdateW);
 }
@@ -1059,10 +974,45 @@ bool finite3(const float* c, int rows) {
   return true;
 }
 
-// Gram-space backend: restart positions (NULL = the pages' default {2}) and
-// the fp16 range check of the coefficient table (gram_table_fits).
+// The Gram-space backend's default coefficients ("API Reference", sections
+// gram_newton_schulz and POLAR_EXPRESS_COEFFICIENTS: Polar Express with the
+// safety factor 1.05): the table dmuon_polar_express_coefficients derives
+// from [1e-3, 1], cached per step count.  nullptr if the derivation fails.
+const float* gram_default_table(int ns_steps) {
+  static std::mutex mu;
+  static std::vector<float> cache[DMUON_MAX_NS_STEPS + 1];
+  if (ns_steps <= 0 || ns_steps > DMUON_MAX_NS_STEPS) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  std::vector<float>& v = cache[ns_steps];
+  if (v.empty()) {
+    v.resize(3 * (size_t)ns_steps);
+    if (dmuon_polar_express_coefficients(ns_steps, 1e-3, 1.0, 1.05, v.data()) != DMUON_OK) v.clear();
+  }
+  return v.empty() ? nullptr : v.data();
+}
+
+// The direct iteration's fp16 range check of the coefficient table
+// (direct_table_fits).
+int direct_options(dmuon_ctx* h, int ns_steps, const float* coeffs) {
+  char why[192];
+  if (!direct_table_fits(ns_steps, coeffs, why, sizeof why)) {
+    std::string msg = std::string("coefficient table: ") + why;
+    return fail(h, DMUON_ERR_ARG, msg.c_str());
+  }
+  return DMUON_OK;
+}
+
+// Gram-space backend: the coefficient table (NULL = its Polar Express
+// default, returned in *table), restart positions (NULL = the pages' default
+// {2}) and the fp16 range check (gram_table_fits).
 int gram_options(dmuon_ctx* h, int ns_steps, const float* coeffs, const int* restarts, int n_restarts,
-                 std::vector<int>* out) {
+                 std::vector<int>* out, const float** table) {
+  *table = coeffs;
+  if (!coeffs && ns_steps > 0) {
+    *table = gram_default_table(ns_steps);
+    if (!*table) return fail(h, DMUON_ERR_ARG, "Gram-space backend: Polar Express table derivation failed");
+  }
+  coeffs = *table;
   out->clear();
   if (!restarts) {
     out->push_back(2);
@@ -1218,8 +1168,12 @@ int dmuon_step(dmuon_handle_t h, float* const* params, const float* const* grads
   if (o.backend != DMUON_BACKEND_DIRECT && o.backend != DMUON_BACKEND_GRAM) return DMUON_ERR_ARG;
   if (int rc = check_shapes(shapes, n_mats)) return rc;
   std::vector<int> restarts;
-  if (o.backend == DMUON_BACKEND_GRAM)
-    if (int rc = gram_options(h, ns_steps, o.coeffs, o.restarts, o.n_restarts, &restarts)) return rc;
+  const float* table = o.coeffs;
+  if (o.backend == DMUON_BACKEND_GRAM) {
+    if (int rc = gram_options(h, ns_steps, o.coeffs, o.restarts, o.n_restarts, &restarts, &table)) return rc;
+  } else if (int rc = direct_options(h, ns_steps, o.coeffs)) {
+    return rc;
+  }
   std::vector<MatPtrs> ptrs(n_mats);
   for (int i = 0; i < n_mats; ++i) {
     int rc;
@@ -1229,7 +1183,7 @@ int dmuon_step(dmuon_handle_t h, float* const* params, const float* const* grads
       return DMUON_ERR_ARG;
     ptrs[i] = MatPtrs{params[i], grads[i], momentum[i], nullptr};
   }
-  return run(h, ptrs.data(), shapes, n_mats, lr, mu, ns_steps, o.coeffs, o.eps, o.weight_decay,
+  return run(h, ptrs.data(), shapes, n_mats, lr, mu, ns_steps, table, o.eps, o.weight_decay,
              o.nesterov ? 1 : 0, o.scale_mode, 0, (cudaStream_t)stream, o.backend == DMUON_BACKEND_GRAM, restarts);
 }
 
@@ -1244,6 +1198,7 @@ int dmuon_newton_schulz(dmuon_handle_t h, const float* const* inputs, float* con
   if (eps <= 0.f) eps = 1e-7f;
   if (coeffs && !finite3(coeffs, ns_steps)) return DMUON_ERR_ARG;
   if (int rc = check_shapes(shapes, n_mats)) return rc;
+  if (int rc = direct_options(h, ns_steps, coeffs)) return rc;
   std::vector<MatPtrs> ptrs(n_mats);
   for (int i = 0; i < n_mats; ++i) {
     int rc;
@@ -1267,7 +1222,8 @@ int dmuon_gram_newton_schulz(dmuon_handle_t h, const float* const* inputs, float
   if (coeffs && !finite3(coeffs, ns_steps)) return DMUON_ERR_ARG;
   if (int rc = check_shapes(shapes, n_mats)) return rc;
   std::vector<int> rs;
-  if (int rc = gram_options(h, ns_steps, coeffs, restarts, n_restarts, &rs)) return rc;
+  const float* table = coeffs;
+  if (int rc = gram_options(h, ns_steps, coeffs, restarts, n_restarts, &rs, &table)) return rc;
   std::vector<MatPtrs> ptrs(n_mats);
   for (int i = 0; i < n_mats; ++i) {
     int rc;
@@ -1275,7 +1231,7 @@ int dmuon_gram_newton_schulz(dmuon_handle_t h, const float* const* inputs, float
     if ((const void*)inputs[i] == (const void*)outputs[i]) return DMUON_ERR_ARG;
     ptrs[i] = MatPtrs{outputs[i], inputs[i], nullptr, nullptr};
   }
-  return run(h, ptrs.data(), shapes, n_mats, 0.f, 0.f, ns_steps, coeffs, eps, 0.f, 0, 1, 1,
+  return run(h, ptrs.data(), shapes, n_mats, 0.f, 0.f, ns_steps, table, eps, 0.f, 0, 1, 1,
              (cudaStream_t)stream, true, rs);
 }
 
@@ -1545,19 +1501,17 @@ int dmuon_plan_preview(const dmuon_shape_t* shapes, int n_mats, int backend, int
     if (int rc = check_shapes(shapes, n_mats)) return rc;
   const bool gram = backend == DMUON_BACKEND_GRAM;
   std::vector<int> order;
-  int n_expl = 0;
-  const int n_large = plan_order(shapes, n_mats, true, order, gram, &n_expl);
+  const int n_large = plan_order(shapes, n_mats, true, order);
   std::vector<dmuon_shape_t> ps(n_mats);
   for (int k = 0; k < n_mats; ++k) ps[k] = shapes[order[k]];
   const bool pair = choose_pairs(clusters, tile_mode, true, shapes, n_mats, gram);
   const int procs = pair ? clusters : sms;
-  size_t items[3] = {0, 0, 0}, chunks = 0, n_impl = 0;
+  size_t items[3] = {0, 0, 0}, chunks = 0;
   double busiest[3] = {0, 0, 0}, mean[3] = {0, 0, 0};
-  for (const auto& cc : plan_chunks(ps.data(), n_expl, n_large, kDefaultChunkElems, gram)) {
+  for (const auto& cc : split_chunks(ps.data(), n_large, kDefaultChunkElems)) {
     Layout L;
-    make_layout(ps.data() + cc.first.first, cc.first.second, L, pair, procs, balanced != 0, gram, cc.second);
+    make_layout(ps.data() + cc.first, cc.second, L, pair, procs, balanced != 0, gram);
     ++chunks;
-    if (cc.second) ++n_impl;
     for (int q = 0; q < 3; ++q) {
       items[q] += L.items[q].size();
       const auto b = deal_balance(L, q);
@@ -1567,10 +1521,10 @@ int dmuon_plan_preview(const dmuon_shape_t* shapes, int n_mats, int backend, int
   }
   char line[384];
   std::snprintf(line, sizeof line,
-                "matrices %d; backend %s; tiles %s; small-matrix kernel %d; chunks %zu (implicit-restart %zu); "
+                "matrices %d; backend %s; tiles %s; small-matrix kernel %d; chunks %zu; "
                 "items gram %zu gram2 %zu apply %zu; balance gram %.4f gram2 %.4f apply %.4f",
                 n_mats, gram ? "gram" : "direct", pair ? "256x256 CTA pairs" : "128x256 single CTAs",
-                n_mats - n_large, chunks, n_impl, items[0], items[1], items[2],
+                n_mats - n_large, chunks, items[0], items[1], items[2],
                 mean[0] > 0 ? busiest[0] / mean[0] : 1.0, mean[1] > 0 ? busiest[1] / mean[1] : 1.0,
                 mean[2] > 0 ? busiest[2] / mean[2] : 1.0);
   const std::string s(line);

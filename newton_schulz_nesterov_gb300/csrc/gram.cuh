@@ -14,8 +14,8 @@
 // a^2 R + 2a (B R) + B (B R) cancels heavily once singular values near 1
 // (Z's eigenvalue a + b + c is ~0.1..1 against a ~3..4), amplifying fp16
 // rounding tenfold and more; products with Z cancel only inside the fp32
-// accumulators.  The last Q of a window is written in bf16 for the Q X
-// product, whose other operand X is bf16.
+// accumulators.  The last Q of a window (buffer kGbQb) is the left operand of
+// the Q X product, run by the direct Apply kernel on the fp16 iterate.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -25,29 +25,22 @@
 namespace dmuon {
 
 // m x m buffers of one matrix, in this order in the workspace and in the
-// tensor-map array.  The first eight serve every Gram plan (Z alternates
-// between Z0 and Z1 from step to step, so the window's first factor Q = Z
-// is read from its Z buffer instead of being copied); Rs (the Gram matrix
-// at the start of the window) and the factor accumulators A0, A1 exist only
-// in chunks that restart implicitly (below).
+// tensor-map array.  Z alternates between Z0 and Z1 from step to step, so
+// the window's first factor Q = Z is read from its Z buffer instead of being
+// copied.
 enum GramBuf : int {
-  kGbR0 = 0, kGbR1 = 1, kGbZ0 = 2, kGbW = 3, kGbQ0 = 4, kGbQ1 = 5, kGbQb = 6, kGbZ1 = 7,
-  kGbRs = 8, kGbA0 = 9, kGbA1 = 10, kGramBufs = 11
+  kGbR0 = 0, kGbR1 = 1, kGbZ0 = 2, kGbW = 3, kGbQ0 = 4, kGbQ1 = 5, kGbQb = 6, kGbZ1 = 7, kGramBufs = 8
 };
-constexpr int kGramBufsExplicit = 8;
 
-// Restarts.  Explicit (matrices with n < 2m): X <- Q X (bf16) and R <- X X^T.
-// Implicit (n >= 2m): R <- Q R_start Q from m x m products only (Q is a
-// polynomial in R_start, so this is the Gram matrix of the iterate Q X
-// without forming it), the window factors are multiplied into an
-// accumulator, and one product with X happens at the end.  Per five steps
-// with one restart that is 1.5 m^2 n + 8.5 m^3 multiply-adds instead of
-// 3 m^2 n + 7 m^3; an emulation of the fp16/bf16 roundings gave equal or
-// smaller errors than the explicit restart for n >= 2m and larger ones for
-// square matrices, where it saves nothing.
+// Restarts are explicit: X <- Q X (fp16, on the Apply kernel) and a new
+// R <- X X^T.  (Restarting without forming X -- R <- Q R_start Q from m x m
+// products, one product with X at the end -- needs fewer multiply-adds for
+// n >= 2m, but keeps R_start's fp16 rounding for the whole step; an emulation
+// of the roundings put it at twice the explicit restart's error and past
+// 3e-2 on inputs whose singular values spread over 1e3..1e4.)
 
 struct GramDesc {
-  uint16_t* buf[kGramBufs];  // m x m, leading dimension ld; fp16 except kGbQb (bf16)
+  uint16_t* buf[kGramBufs];  // m x m fp16, leading dimension ld
   int64_t m, ld;
   float kappa, inv_kappa;    // power-of-two scale of R and W and its inverse
 };
@@ -56,10 +49,11 @@ struct GramDesc {
 // diagonal of one matrix) the CTA pair computes P = opA * opB^T (both
 // operands K-major; for symmetric operands that is opA * opB) and writes
 //   out  = g * P + c1 * kappa^p1pow * buf[add1] + diag * I
-//   out2 = the same values (another buffer, possibly bf16; out2 >= 0)
-// with g = g0 * kappa^gpow (times s^2 of the matrix when use_s2), into the
-// tile and its mirror.  Operands: X[src] (bf16, K = n) for the first Gram
-// of a window (x_operand = 1), else buf[opA], buf[opB] (fp16, K = m).
+//   out2 = the same values (another buffer; out2 >= 0)
+// with g = g0 * kappa^gpow times the iterate's scale squared (xscale 1: s/p
+// of X[0] = p U; 2: 1/beta' of an iterate stored as beta' X), into the tile
+// and its mirror.  Operands: X[src] (fp16, K = n) for the first Gram of a
+// window (x_operand = 1), else buf[opA], buf[opB] (fp16, K = m).
 struct GramArgs {
   const GramDesc* gd;
   const MatDesc* mats;
@@ -70,12 +64,12 @@ struct GramArgs {
   const int* starts;          // per CTA pair: first item (see work_range), or null
   int x_operand, src;
   int opA, opB;
-  int out, out_bf16;
-  int out2, out2_bf16;
-  int add1;                  // -1: none
+  int out, out2;              // out2 < 0: none
+  int add1;                   // -1: none
   float g0, c1, diag;
-  int gpow, p1pow, use_s2;    // powers of kappa, -2..1
-  const float* svec;          // per-matrix 1/(||U||_F + eps)
+  int gpow, p1pow, xscale;    // powers of kappa (-2..1); xscale 0 / 1 / 2 as above
+  const float* svec;          // per-matrix s/p
+  const float* bvec;          // per-matrix beta'
   int* err;
   unsigned long long timeout_ns;
 };

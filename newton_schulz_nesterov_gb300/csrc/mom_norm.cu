@@ -1,5 +1,6 @@
 // HBM-bound kernels of the Muon step: fused momentum / Nesterov / orientation
-// / sum-of-squares, the per-matrix norm finalisation, and the ns_steps == 0
+// / sum-of-squares writing the fp16 iterate, the per-matrix norm finalisation
+// (with the redo pass for a prescale that missed), and the ns_steps == 0
 // update.
 //
 // DMuon "API Reference", section "Muon": momentum buffer update and the
@@ -25,28 +26,48 @@ __device__ __forceinline__ float4 ld_once(const float* p) {
   return __ldcs(reinterpret_cast<const float4*>(p));  // streamed: read once
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // One CTA iteration handles a 64x64 tile of W's shape.  256 threads: thread
 // t covers columns 4*(t%16)..+3 of rows t/16 + 16*i, i = 0..3, so each warp
 // reads two full 256-byte row segments per array (coalesced float4).
-//   M <- mu*M + G ;  U = G + mu*M (nesterov) or M ;  X0 <- bf16(U or U^T)
-//   partials[tile] = sum(U^2) over the tile, fixed reduction order.
+// Momentum pass (redo_pass = 0):
+//   M <- mu*M + G ;  U = G + mu*M (nesterov) or M ;  X0 <- fp16(p U or p U^T)
+//   partials[tile] = sum((p U)^2), tmax[tile] = max |U|, fixed reduction order.
+// Redo pass (redo_pass = 1): only tiles of matrices flagged by the
+// finalisation; U is recomputed from G and the already updated M (the same
+// fmaf sequence, so the same U) and X0 and partials are rewritten with the
+// matrix's new p.  A CTA that finds no flagged matrix returns at once.
 __global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
-  __shared__ uint32_t stage[kMomTile * 33];  // 64 x 66 bf16, odd word stride
+  __shared__ uint32_t stage[kMomTile * 33];  // 64 x 66 fp16, odd word stride
   __shared__ float red[8];
-  __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage);
+  __shared__ float redm[8];
+  __shared__ int any;
+  __half* st = reinterpret_cast<__half*>(stage);
   const int tid = threadIdx.x;
   const int cl = (tid & 15) * 4;
   const int rl0 = tid >> 4;
+  const bool redo_pass = a.redo_pass != 0;
+
+  if (redo_pass) {
+    if (tid == 0) any = 0;
+    __syncthreads();
+    int mine = 0;
+    for (int i = tid; i < a.n_mats; i += blockDim.x) mine |= a.redo[i];
+    if (mine) any = 1;
+    __syncthreads();
+    if (!any) return;
+  }
 
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const int mi = find_mat(a.tile_prefix, a.n_mats, t);
+    if (redo_pass && !a.redo[mi]) continue;  // uniform over the CTA
     const MatDesc& d = a.mats[mi];
     const MatPtrs& p = a.ptrs[mi];
+    const float ps = a.pscale[mi];
     const int64_t rows = d.rows, cols = d.cols;
     const int64_t local = t - d.tile0;
     const int64_t r0 = (local / d.tiles_c) * kMomTile;
@@ -54,9 +75,9 @@ __global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
     const int64_t c = c0 + cl;
     const bool vec = (cols & 3) == 0;
     const bool tr = d.transposed != 0;
-    __nv_bfloat16* X = d.X[0];
+    __half* X = d.X[0];
     const int64_t ldx = d.ldx;
-    float ss = 0.f;
+    float ss = 0.f, mx = 0.f;
 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -71,6 +92,11 @@ __global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
           if (a.ns_only) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) u[j] = g[j];
+          } else if (redo_pass) {
+            const float4 m4 = ld_once(p.M + off);  // already mu*M + G
+            const float mn[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) u[j] = a.nesterov ? fmaf(a.mu, mn[j], g[j]) : mn[j];
           } else {
             const float4 m4 = ld_once(p.M + off);
             const float mo[4] = {m4.x, m4.y, m4.z, m4.w};
@@ -90,6 +116,9 @@ __global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
               const float g = p.G[off + j];
               if (a.ns_only) {
                 u[j] = g;
+              } else if (redo_pass) {
+                const float mn = p.M[off + j];
+                u[j] = a.nesterov ? fmaf(a.mu, mn, g) : mn;
               } else {
                 const float mn = fmaf(a.mu, p.M[off + j], g);
                 p.M[off + j] = mn;
@@ -99,24 +128,29 @@ __global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
           }
         }
       }
+      float x[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ss = fmaf(u[j], u[j], ss);
+      for (int j = 0; j < 4; ++j) {
+        x[j] = u[j] * ps;  // a power of two: exact unless out of fp32 range
+        ss = fmaf(x[j], x[j], ss);
+        mx = fmaxf(mx, fabsf(u[j]));
+      }
 
       if (!tr) {
         if (r < rows && c < cols) {
-          __nv_bfloat16* dst = X + r * ldx + c;
+          __half* dst = X + r * ldx + c;
           if (c + 4 <= cols) {
             uint2 v;
-            v.x = pack_bf16x2(u[0], u[1]);
-            v.y = pack_bf16x2(u[2], u[3]);
+            v.x = pack_h2(x[0], x[1]);
+            v.y = pack_h2(x[2], x[3]);
             *reinterpret_cast<uint2*>(dst) = v;
           } else {
-            for (int j = 0; j < 4 && c + j < cols; ++j) dst[j] = __float2bfloat16_rn(u[j]);
+            for (int j = 0; j < 4 && c + j < cols; ++j) dst[j] = __float2half_rn(x[j]);
           }
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st[(cl + j) * 66 + rl] = __float2bfloat16_rn(u[j]);
+        for (int j = 0; j < 4; ++j) st[(cl + j) * 66 + rl] = __float2half_rn(x[j]);
       }
     }
 
@@ -132,7 +166,7 @@ __global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
         const int64_t xc = r0 + seg;
         if (xr < d.m && xc < d.n) {
           const uint32_t* w = stage + cr * 33 + seg / 2;
-          __nv_bfloat16* dst = X + xr * ldx + xc;
+          __half* dst = X + xr * ldx + xc;
           if (xc + 8 <= d.n) {
             *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
           } else {
@@ -142,45 +176,113 @@ __global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
       }
     }
 
-    // Deterministic tile sum: fixed shuffle tree, then warps in order.
+    // Deterministic tile sum: fixed shuffle tree, then warps in order (the
+    // maximum does not depend on the order).
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    for (int o = 16; o > 0; o >>= 1) {
+      ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if ((tid & 31) == 0) {
+      red[tid >> 5] = ss;
+      redm[tid >> 5] = mx;
+    }
     __syncthreads();
     if (tid == 0) {
-      float s = 0.f;
+      float s = 0.f, m = 0.f;
 #pragma unroll
-      for (int w = 0; w < 8; ++w) s += red[w];
+      for (int w = 0; w < 8; ++w) {
+        s += red[w];
+        m = fmaxf(m, redm[w]);
+      }
       a.partials[t] = s;
+      if (!redo_pass) a.tmax[t] = m;
     }
     __syncthreads();
   }
 }
 
-// One CTA per matrix: fp64 sum of the tile partials in a fixed order, then
-// s = 1 / (sqrt(sum) + eps).  A non-finite sum sets the matrix's flag.
-__global__ void __launch_bounds__(256) finalize_kernel(const FinalizeArgs a) {
-  __shared__ double red[256];
-  const int mi = blockIdx.x;
-  const int64_t b = a.tile_prefix[mi], e = a.tile_prefix[mi + 1];
-  double s = 0.0;
-  for (int64_t i = b + threadIdx.x; i < e; i += blockDim.x) s += (double)a.partials[i];
-  red[threadIdx.x] = s;
-  __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-    __syncthreads();
+// s/p and beta' of a matrix from S = sum (p U)^2: X0 * (s/p) = U / (||U|| + eps)
+// with ||U|| = sqrt(S) / p, and nu = ||X0||_F = sqrt(S) / (sqrt(S) + eps p);
+// beta' = beta / 2^floor(log2 nu) when nu < 1/2 (at most 2^100), else beta.
+__device__ __forceinline__ void set_scales(const FinalizeArgs& a, int mi, double tot, double p, float beta) {
+  const double r = sqrt(tot), den = r + (double)a.eps * p;
+  a.svec[mi] = (float)(1.0 / den);
+  const double nu = r / den;
+  float b = beta;
+  if (nu < 0.5 && nu > 0.0) {
+    int ex = 0;
+    frexp(nu, &ex);  // nu = f 2^ex, f in [0.5, 1): floor(log2 nu) = ex - 1
+    b = ldexpf(beta, min(100, 1 - ex));
   }
-  if (threadIdx.x == 0) {
-    const double tot = red[0];
-    const bool finite = isfinite(tot);
-    const double nrm = sqrt(tot) + (double)a.eps;
-    a.svec[mi] = finite ? (float)(1.0 / nrm) : 0.f;
-    if (!finite) a.flags[mi] |= 1;
-  }
+  a.bvec[mi] = b;
 }
 
-// ns_steps == 0: O = s * X0 (oriented back), then the update or a plain
+// One CTA per matrix: fp64 sum of the tile partials in a fixed order (the
+// sum of (p U)^2) and the maximum of |U|.  Then, with S the sum:
+//   non-finite input (S NaN or max |U| infinite): flag, s/p = 0;
+//   zero input: s/p = 0 (X0 = 0, so every output is 0);
+//   max |U| * p inside [2^6, 2^14] and S finite: s/p and beta' (set_scales);
+//   otherwise: p <- 2^(11 - e) with max |U| = f 2^e, f in [0.5, 1) (so that
+//     max |p U| lies in [2^10, 2^11)), and the matrix is flagged for the redo
+//     pass, whose second finalisation (redo_pass = 1) computes s/p from the
+//     rewritten partials and clears the flag.
+__global__ void __launch_bounds__(256) finalize_kernel(const FinalizeArgs a) {
+  __shared__ double red[256];
+  __shared__ float redm[256];
+  const int mi = blockIdx.x;
+  if (a.redo_pass && !a.redo[mi]) return;
+  const int64_t b = a.tile_prefix[mi], e = a.tile_prefix[mi + 1];
+  double s = 0.0;
+  float mx = 0.f;
+  for (int64_t i = b + threadIdx.x; i < e; i += blockDim.x) {
+    s += (double)a.partials[i];
+    if (!a.redo_pass) mx = fmaxf(mx, a.tmax[i]);
+  }
+  red[threadIdx.x] = s;
+  redm[threadIdx.x] = mx;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) {
+      red[threadIdx.x] += red[threadIdx.x + w];
+      redm[threadIdx.x] = fmaxf(redm[threadIdx.x], redm[threadIdx.x + w]);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x != 0) return;
+  const double tot = red[0];
+  const double p = (double)a.pscale[mi];
+  const float beta = a.mats[mi].beta;
+  if (a.redo_pass) {
+    set_scales(a, mi, tot, p, beta);
+    a.redo[mi] = 0;
+    return;
+  }
+  const float m = redm[0];
+  if (isnan(tot) || isinf(m)) {
+    a.svec[mi] = 0.f;
+    a.bvec[mi] = beta;
+    a.flags[mi] |= 1;
+    return;
+  }
+  if (m == 0.f) {
+    a.svec[mi] = 0.f;
+    a.bvec[mi] = beta;
+    return;
+  }
+  const double q = (double)m * p;
+  if (isfinite(tot) && q >= 64.0 && q <= 16384.0) {
+    set_scales(a, mi, tot, p, beta);
+    return;
+  }
+  int ex = 0;
+  frexpf(m, &ex);
+  const int k = min(127, max(-126, 11 - ex));
+  a.pscale[mi] = ldexpf(1.f, k);
+  a.redo[mi] = 1;
+}
+
+// ns_steps == 0: O = (s/p) * X0 (oriented back), then the update or a plain
 // write of O.  Scalar, one element per thread iteration; only used for this
 // degenerate step count.
 __global__ void __launch_bounds__(256) update0_kernel(const Update0Args a) {
@@ -197,7 +299,7 @@ __global__ void __launch_bounds__(256) update0_kernel(const Update0Args a) {
       const int64_t r = r0 + e / kMomTile, c = c0 + e % kMomTile;
       if (r >= d.rows || c >= d.cols) continue;
       const int64_t xoff = d.transposed ? c * d.ldx + r : r * d.ldx + c;
-      const float o = s * __bfloat162float(d.X[0][xoff]);
+      const float o = s * __half2float(d.X[0][xoff]);
       float* w = p.W + r * d.cols + c;
       *w = a.write_o ? o : fmaf(a.decay, *w, -coef * o);
     }

@@ -6,26 +6,37 @@
 // allocations, plugins that are handed only input and output buffers, and
 // latency-critical paths that cannot afford cudaMalloc's implicit device
 // synchronisation.  Everything the computation needs beyond its input and
-// output -- the bf16 iterate X (ping/pong), the products A and B, the
-// per-tile sums of squares, the matrix descriptor, four TMA tensor maps and
-// the work lists -- lives in one file-scope static __device__ array of
-// kNaScratchBytes (about 12.9 MB).  Every GPU that loads the library holds
-// that array until the process exits.
+// output -- the fp16 iterate X (ping/pong), the products A and B, the
+// per-tile sums of squares and maxima, the matrix descriptor, four TMA
+// tensor maps and the work lists -- lives in one file-scope static
+// __device__ array of kNaScratchBytes (about 13.1 MB).  Every GPU that loads
+// the library holds that array until the process exits.
 //
 // Limits: short side min(rows, cols) <= 1024 and rows*cols <= 2^21; larger
 // matrices are rejected with DMUON_ERR_ARG before anything is launched.
 //
 // The array is shared by every call and keeps the last call's contents.
-// Each call clears what must start at zero (the non-finite flag and the
-// wait-timeout word) and overwrites everything else it reads.  Calls whose
-// GPU work overlaps (different streams without ordering, or several host
-// threads) race on the array and give wrong results.
+// Each call clears what must start at zero (the non-finite flag, the
+// wait-timeout word, the redo flag) and overwrites everything else it reads.
+// Calls whose GPU work overlaps (different streams without ordering, or
+// several host threads) race on the array and give wrong results.
 //
 // Set-up: the first call on a device (with that device current) resolves the
 // array's device address with cudaGetSymbolAddress, raises the kernels'
-// shared-memory limit and reads the SM count; that first call should come
-// before any stream capture.  Later calls on that device reuse the cached
-// values.
+// shared-memory limit and reads the SM count; later calls on that device
+// reuse the cached values.  A set-up that fails for a reason other than an
+// unsupported device is tried again by the next call.
+//
+// Every call copies its descriptor, tensor maps and work lists from a host
+// staging image with cudaMemcpyAsync, so a call cannot be recorded into a
+// CUDA graph: while `stream` is being captured the entry point returns
+// DMUON_ERR_ARG without touching the device.
+//
+// Arithmetic: the same kernels as dmuon_newton_schulz on single CTAs with
+// the unfolded epilogue (the Z product writes b A + c A A, the X product
+// adds a X read from X), so roundings differ from dmuon_newton_schulz's.
+// Each call starts from the prescale p = 1 for X0 = p U; inputs whose
+// entries are far from 1 take the redo pass (one more read of the input).
 #include <algorithm>
 #include <cmath>
 #include <cstddef>
@@ -35,6 +46,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/dmuon.h"
+#include "coeffs.cuh"
 #include "common.cuh"
 
 namespace dmuon {
@@ -54,11 +66,12 @@ constexpr size_t kOffX1 = kOffX0 + na_round(kNaXElems * 2);
 constexpr size_t kOffA = kOffX1 + na_round(kNaXElems * 2);
 constexpr size_t kOffB = kOffA + na_round(kNaMaxShort * kNaMaxShort * 2);
 constexpr size_t kOffPartials = kOffB + na_round(kNaMaxShort * kNaMaxShort * 2);
-constexpr size_t kOffMaps = kOffPartials + na_round(kNaMaxTiles * 4);
+constexpr size_t kOffTmax = kOffPartials + na_round(kNaMaxTiles * 4);
+constexpr size_t kOffMaps = kOffTmax + na_round(kNaMaxTiles * 4);
 constexpr size_t kOffDesc = kOffMaps + na_round(kMapsPerMat * sizeof(CUtensorMap));
 constexpr size_t kOffPtrs = kOffDesc + na_round(sizeof(MatDesc));
 constexpr size_t kOffPrefix = kOffPtrs + na_round(sizeof(MatPtrs));
-constexpr size_t kOffWords = kOffPrefix + na_round(2 * sizeof(int64_t));  // svec, flag, err
+constexpr size_t kOffWords = kOffPrefix + na_round(2 * sizeof(int64_t));  // s/p, flag, err, p, redo, beta'
 constexpr size_t kOffItems0 = kOffWords + 256;
 constexpr size_t kOffItems1 = kOffItems0 + na_round(kNaMaxSymItems * 16);
 constexpr size_t kOffItems2 = kOffItems1 + na_round(kNaMaxSymItems * 16);
@@ -76,7 +89,7 @@ struct alignas(256) HostImage {
   alignas(256) MatDesc desc;
   alignas(256) MatPtrs ptrs;
   alignas(256) int64_t prefix[2];
-  alignas(256) uint32_t words[64];  // [0] svec (float bits), [1] flag, [2] err
+  alignas(256) uint32_t words[64];  // [0] s/p, [1] flag, [2] err, [3] p (float bits), [4] redo, [5] beta'
   alignas(256) int4 items0[kNaMaxSymItems];
   alignas(256) int4 items1[kNaMaxSymItems];
   alignas(256) int4 items2[kNaMaxApplyItems];
@@ -107,7 +120,7 @@ int na_setup(int dev, DeviceSetup** out) {
   std::lock_guard<std::mutex> lock(g_na_mutex);
   DeviceSetup& s = g_na_dev[dev];
   if (!s.done) {
-    s.done = true;
+    s.rc = DMUON_OK;
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -132,6 +145,8 @@ int na_setup(int dev, DeviceSetup** out) {
       if (!g_na_encode) s.rc = DMUON_ERR_CUDA;
     }
     if (s.rc != DMUON_OK) cudaGetLastError();
+    // Only an unsupported device is final; other failures are retried.
+    s.done = s.rc == DMUON_OK || s.rc == DMUON_ERR_UNSUPPORTED;
   }
   *out = &s;
   return s.rc;
@@ -142,17 +157,12 @@ bool na_encode(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t
   cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
   cuuint32_t box[2] = {(cuuint32_t)kBox, (cuuint32_t)kBox};
   cuuint32_t estr[2] = {1, 1};
-  return g_na_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+  return g_na_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 inline int64_t na_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-// DMuon "API Reference", section YOU_COEFFICIENTS (used when coeffs is NULL).
-const float kNaYou[5][3] = {
-    {4.0848f, -6.8946f, 2.927f}, {3.9505f, -6.3029f, 2.6377f}, {3.7418f, -5.5913f, 2.3037f},
-    {2.8769f, -3.1427f, 1.2046f}, {2.8366f, -3.0525f, 1.2012f}};
 
 }  // namespace
 }  // namespace dmuon
@@ -176,7 +186,13 @@ extern "C" int dmuon_newton_schulz_noalloc(const float* input, float* output, in
       if (!std::isfinite(coeffs[i])) return DMUON_ERR_ARG;
   if (!std::isfinite(eps)) return DMUON_ERR_ARG;
   if (eps <= 0.f) eps = 1e-7f;
+  if (!direct_table_fits(ns_steps, coeffs, nullptr, 0)) return DMUON_ERR_ARG;  // fp16 range
   cudaStream_t stream = (cudaStream_t)stream_;
+  {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) { cudaGetLastError(); return DMUON_ERR_CUDA; }
+    if (cap != cudaStreamCaptureStatusNone) return DMUON_ERR_ARG;  // see the top of this file
+  }
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return DMUON_ERR_CUDA; }
@@ -195,19 +211,23 @@ extern "C" int dmuon_newton_schulz_noalloc(const float* input, float* output, in
   d.n = n;
   d.ldx = (n + 7) / 8 * 8;
   d.lda = (m + 7) / 8 * 8;
-  d.X[0] = reinterpret_cast<__nv_bfloat16*>(base + kOffX0);
-  d.X[1] = reinterpret_cast<__nv_bfloat16*>(base + kOffX1);
-  d.A = reinterpret_cast<__nv_bfloat16*>(base + kOffA);
-  d.B = reinterpret_cast<__nv_bfloat16*>(base + kOffB);
+  d.X[0] = reinterpret_cast<__half*>(base + kOffX0);
+  d.X[1] = reinterpret_cast<__half*>(base + kOffX1);
+  d.A = reinterpret_cast<__half*>(base + kOffA);
+  d.B = reinterpret_cast<__half*>(base + kOffB);
   d.tile0 = 0;
   d.tiles_c = (int32_t)na_cdiv(cols, kMomTile);
   d.scale = 1.f;
+  d.kappa = scale_kappa(m);
+  d.beta = scale_beta(n);
   const int64_t n_tiles = na_cdiv(rows, kMomTile) * d.tiles_c;
   if (n_tiles > kNaMaxTiles || na_cdiv(m, kBM) * na_cdiv(n, kBN) > kNaMaxApplyItems) return DMUON_ERR_ARG;
   img.ptrs = MatPtrs{output, input, nullptr, nullptr};
   img.prefix[0] = 0;
   img.prefix[1] = n_tiles;
   std::memset(img.words, 0, sizeof img.words);
+  const float p_start = 1.f;
+  std::memcpy(&img.words[3], &p_start, 4);
   if (!na_encode(&img.maps[0], d.X[0], m, n, d.ldx) || !na_encode(&img.maps[1], d.X[1], m, n, d.ldx) ||
       !na_encode(&img.maps[2], d.A, m, m, d.lda) || !na_encode(&img.maps[3], d.B, m, m, d.lda))
     return DMUON_ERR_CUDA;
@@ -227,7 +247,7 @@ extern "C" int dmuon_newton_schulz_noalloc(const float* input, float* output, in
     for (int64_t tj = 0; tj < na_cdiv(n, kBN); ++tj) img.items2[n_apply++] = make_int4(0, (int)ti, (int)tj, km);
 
   // One copy of the image (pageable source: staged before return), which
-  // also zeroes the flag and timeout words.
+  // also zeroes the flag, timeout and redo words and sets p = 1.
   const size_t img_bytes = offsetof(HostImage, items2) + sizeof(int4) * (size_t)n_apply;
   cudaError_t e = cudaMemcpyAsync(base + kOffMaps, &img, img_bytes, cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return DMUON_ERR_CUDA;
@@ -238,14 +258,22 @@ extern "C" int dmuon_newton_schulz_noalloc(const float* input, float* output, in
   float* svec = reinterpret_cast<float*>(base + kOffWords);
   int* flags = reinterpret_cast<int*>(base + kOffWords + 4);
   int* err = reinterpret_cast<int*>(base + kOffWords + 8);
+  float* pscale = reinterpret_cast<float*>(base + kOffWords + 12);
+  int* redo = reinterpret_cast<int*>(base + kOffWords + 16);
+  float* bvec = reinterpret_cast<float*>(base + kOffWords + 20);
   float* partials = reinterpret_cast<float*>(base + kOffPartials);
+  float* tmax = reinterpret_cast<float*>(base + kOffTmax);
   const CUtensorMap* maps = reinterpret_cast<const CUtensorMap*>(base + kOffMaps);
 
   const int grid_e = (int)std::min<int64_t>(n_tiles, (int64_t)ds->num_sms * 8);
-  if ((e = launch_mom(MomArgs{dd, dp, dprefix, 1, n_tiles, 0.f, 0, 1, partials}, grid_e, stream)) != cudaSuccess)
-    return DMUON_ERR_CUDA;
-  if ((e = launch_finalize(FinalizeArgs{dd, dprefix, partials, 1, eps, svec, flags}, stream)) != cudaSuccess)
-    return DMUON_ERR_CUDA;
+  for (int pass = 0; pass < 2; ++pass) {  // momentum-free pass, then the redo pass if p missed
+    if (launch_mom(MomArgs{dd, dp, dprefix, 1, n_tiles, 0.f, 0, 1, partials, tmax, pscale, redo, pass}, grid_e,
+                   stream) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+    if (launch_finalize(FinalizeArgs{dd, dprefix, partials, tmax, 1, eps, svec, bvec, pscale, redo, flags, pass},
+                        stream) != cudaSuccess)
+      return DMUON_ERR_CUDA;
+  }
   if (ns_steps == 0) {
     if (launch_update0(Update0Args{dd, dp, dprefix, 1, n_tiles, svec, 0.f, 1.f, 1}, grid_e, stream) != cudaSuccess)
       return DMUON_ERR_CUDA;
@@ -255,7 +283,7 @@ extern "C" int dmuon_newton_schulz_noalloc(const float* input, float* output, in
                           reinterpret_cast<const int4*>(base + kOffItems2)};
   const int counts[3] = {n_sym, n_sym, n_apply};
   for (int k = 0; k < ns_steps; ++k) {
-    const float* row = coeffs ? coeffs + 3 * k : kNaYou[std::min(k, 4)];
+    const float* row = coefficient_row(coeffs, k);  // NULL: YOU_COEFFICIENTS
     for (int p = 0; p < 3; ++p) {
       GemmArgs a{};
       a.mats = dd;
@@ -272,6 +300,7 @@ extern "C" int dmuon_newton_schulz_noalloc(const float* input, float* output, in
       a.lr = 0.f;
       a.decay = 1.f;
       a.svec = svec;
+      a.bvec = bvec;
       a.err = err;
       const int grid = std::min(counts[p], ds->num_sms);
       if (launch_gemm(p, a, grid, stream) != cudaSuccess) return DMUON_ERR_CUDA;

@@ -18,7 +18,10 @@
 //   warp 1   TMEM allocator and single-thread tcgen05.mma issuer
 //            (M=128, N=256, K=16 per instruction, fp32 accumulate)
 //   warps 2-5 epilogue: TMEM -> registers, fused scaling / a*X / b*A terms,
-//            bf16 stores (direct and mirrored) or the fp32 weight update
+//            fp16 stores (direct and mirrored) or the fp32 weight update
+// Operands are fp16 (kind::f16 with fp16 A and B, fp32 accumulate); every
+// stored buffer carries a power-of-two scale (MatDesc) that keeps its
+// entries in fp16's normal range, undone in the epilogues.
 // Two 256-column accumulators in TMEM let the epilogue of one tile overlap
 // the main loop of the next.
 //
@@ -77,16 +80,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// 32 consecutive bf16 of one row -> fp32, zero outside [0, ncols) or when
+// 32 consecutive fp16 of one row -> fp32, zero outside [0, ncols) or when
 // the row is invalid.
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* rowp, int64_t c, int64_t ncols,
+__device__ __forceinline__ void load_row32(const __half* rowp, int64_t c, int64_t ncols,
                                            bool row_ok, float (&f)[32]) {
   if (row_ok && c + 32 <= ncols) {
     const uint4* p = reinterpret_cast<const uint4*>(rowp + c);
@@ -96,19 +96,20 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* rowp, int64_t c,
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        f[q * 8 + 2 * k] = bf_lo(w[k]);
-        f[q * 8 + 2 * k + 1] = bf_hi(w[k]);
+        const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        f[q * 8 + 2 * k] = t.x;
+        f[q * 8 + 2 * k + 1] = t.y;
       }
     }
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      f[j] = (row_ok && c + j < ncols) ? __bfloat162float(rowp[c + j]) : 0.f;
+      f[j] = (row_ok && c + j < ncols) ? __half2float(rowp[c + j]) : 0.f;
   }
 }
 
-// Store 32 packed bf16 (16 words) at rowp[c..c+31], clipped to ncols.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* rowp, int64_t c, int64_t ncols,
+// Store 32 packed fp16 (16 words) at rowp[c..c+31], clipped to ncols.
+__device__ __forceinline__ void store_row32(__half* rowp, int64_t c, int64_t ncols,
                                             bool row_ok, const uint32_t (&w)[16]) {
   if (!row_ok) return;
   if (c + 32 <= ncols) {
@@ -123,10 +124,10 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* rowp, int64_t c, int6
   }
 }
 
-// Mirror store of a 32x32 bf16 block held one row per lane: lane L writes
+// Mirror store of a 32x32 fp16 block held one row per lane: lane L writes
 // column L of the block as row (c + L) of the destination, columns
 // [rbase, rbase+32) clipped to n_lim.  Uses the warp's 32x17-word scratch.
-__device__ __forceinline__ void mirror_store32(__nv_bfloat16* base, int64_t ld, int64_t c,
+__device__ __forceinline__ void mirror_store32(__half* base, int64_t ld, int64_t c,
                                                int64_t rbase, int64_t n_lim, int lane,
                                                const uint32_t (&w)[16], uint32_t* scratch) {
 #pragma unroll
@@ -158,14 +159,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
   const bool row_ok = r < m;
   const uint32_t tq = tacc + ((uint32_t)(quad * 32) << 16);
 
+  // True scale of the stored iterate: X = xs * X[src] (s/p of the first
+  // step's X[0] = p U, else 1/beta' for X stored as beta' X).
+  const float bp = a.bvec[item.x];
+  const float xs = a.first ? a.svec[item.x] : 1.f / bp;
   if constexpr (PHASE == kPhaseGram || PHASE == kPhaseGram2) {
     const bool mirror = (item.y >> 1) < item.z;
-    float alpha = 1.f;
-    if (PHASE == kPhaseGram && a.first) {
-      const float s = a.svec[item.x];
-      alpha = s * s;
-    }
-    __nv_bfloat16* dst = (PHASE == kPhaseGram) ? d.A : d.B;
+    // Gram: A = kappa xs^2 X[src] X[src]^T.  Gram2 with A = kappa X X^T:
+    // b A_true + c A_true^2 = (b/kappa) A + (c/kappa^2) A A.
+    const float ik = 1.f / d.kappa;
+    const float alpha = d.kappa * xs * xs;
+    const float gcc = a.cc * ik * ik, gcb = a.cb * ik;
+    __half* dst = (PHASE == kPhaseGram) ? d.A : d.B;
     const int64_t ld = d.lda;
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
@@ -181,7 +186,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
         float av[32];
         load_row32(d.A + r * ld, c, m, row_ok, av);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) f[j] = fmaf(a.cc, __uint_as_float(v[j]), a.cb * av[j]);
+        for (int j = 0; j < 32; ++j) f[j] = fmaf(gcc, __uint_as_float(v[j]), gcb * av[j]);
         if (a.fold) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
@@ -195,9 +200,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
       if (mirror) mirror_store32(dst, ld, c, rbase, m, lane, w, scratch);
     }
   } else {
-    const float alpha = a.first ? a.svec[item.x] : 1.f;
-    const __nv_bfloat16* xs = d.X[a.src];
-    __nv_bfloat16* xd = d.X[a.src ^ 1];
+    // X' = beta' xs (Z X[src]) stored; the final O = xs (Z X[src]) in fp32.
+    const float alpha = MODE == kWriteX ? xs * bp : xs;
+    const __half* xsrc = d.X[a.src];
+    __half* xd = d.X[a.src ^ 1];
     const int64_t ldx = d.ldx;
     const MatPtrs& p = a.ptrs[item.x];
     const float coef = a.lr * d.scale;
@@ -213,7 +219,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
         for (int j = 0; j < 32; ++j) o[j] = alpha * __uint_as_float(v[j]);
       } else {
         float xv[32];
-        load_row32(xs + r * ldx, c, n, row_ok, xv);
+        load_row32(xsrc + r * ldx, c, n, row_ok, xv);
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = alpha * fmaf(a.ca, xv[j], __uint_as_float(v[j]));
       }
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_bf16(kBM, kBN, PHASE == kPhaseApply ? 1 : 0);
+      constexpr uint32_t idesc = ptx::idesc_f16(kBM, kBN, PHASE == kPhaseApply ? 1 : 0);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             const uint64_t ad = ptx::desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = (PHASE == kPhaseApply) ? ptx::desc_sw128(sb + kk * 2048, 8192, 1024)
                                                        : ptx::desc_sw128(sb + kk * 32, 16, 1024);
-            ptx::mma_bf16(dt, ad, bd, idesc, (kb | kk) != 0);
+            ptx::mma_f16(dt, ad, bd, idesc, (kb | kk) != 0);
           }
           issued = true;
           ptx::mma_commit(ptx::smem_addr(empty + s));
@@ -546,7 +552,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_bf16(256, kBN, PHASE == kPhaseApply ? 1 : 0);
+      constexpr uint32_t idesc = ptx::idesc_f16(256, kBN, PHASE == kPhaseApply ? 1 : 0);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
@@ -568,7 +574,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
             const uint64_t ad = ptx::desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = (PHASE == kPhaseApply) ? ptx::desc_sw128(sb + kk * 2048, 8192, 1024)
                                                        : ptx::desc_sw128(sb + kk * 32, 16, 1024);
-            ptx::mma_bf16_pair(dt, ad, bd, idesc, (kb | kk) != 0);
+            ptx::mma_f16_pair(dt, ad, bd, idesc, (kb | kk) != 0);
           }
           issued = true;
           ptx::mma_commit_multicast(ptx::smem_addr(empty + s), 0x3);

@@ -3,7 +3,7 @@
 // gram_newton_schulz_factors), one persistent CTA-pair launch per phase over
 // every matrix of a chunk.
 //
-//   R~ = kappa s^2 X X^T                      (bf16 X, K = n; first of a window)
+//   R~ = kappa X X^T                          (fp16 X, K = n; first of a window)
 //   Z  = a I + (b/kappa) R~ + (c/kappa^2) R~ R~   (two buffers alternating by step;
 //                                                 a window's first Q is its Z)
 //   Q' = Z Q
@@ -14,12 +14,12 @@
 // K-major (rows of L and rows of M).  Only the 256x256 super-tiles on or
 // above the diagonal are computed; off-diagonal tiles are also written
 // transposed.  The X Q products (restart and final update) run on the
-// direct path's Apply kernel with a = 0 and Q (bf16) as its left operand.
+// direct path's Apply kernel with a = 0 and Q as its left operand.
 //
 // CTA pair (cta_group::2) as in the direct kernels: warp 0 of both CTAs
 // loads operand halves by TMA into a six-stage ring completing on rank 0's
 // barrier; warp 1 of rank 0 issues tcgen05.mma (M = 256, N = 256, K = 16;
-// fp16 or bf16 in, fp32 accumulate) into one of two TMEM accumulators;
+// fp16 in, fp32 accumulate) into one of two TMEM accumulators;
 // warps 2-5 of both CTAs run the epilogue of their 128 rows.  Every wait is
 // bounded; on expiry the CTA records bit 0 of *err, drains its own copies
 // and MMAs (bounded), frees TMEM and returns.
@@ -33,11 +33,6 @@ namespace {
 
 constexpr uint64_t kTimeoutNs = 4000000000ull;       // default: 4 s without progress
 constexpr uint64_t kDrainTimeoutNs = 4000000000ull;  // drains after an abort
-
-__host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
-  // D fp32 (bits 4-5 = 1), A and B fp16 (bits 7-9, 10-12 = 0), both K-major
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
 
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
                                        bool honour_abort, uint64_t limit_ns) {
@@ -61,11 +56,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-__device__ __forceinline__ uint32_t pack_b16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
@@ -198,9 +188,12 @@ __device__ __forceinline__ void gram_epilogue(const GramArgs& a, const int4 item
   const bool mirror = (item.y >> 1) < item.z;
   const bool diag_tile = (item.y >> 1) == item.z;
   float gs = a.g0 * kappa_pow(g, a.gpow);
-  if (a.use_s2) {
+  if (a.xscale == 1) {
     const float s = a.svec[item.x];
     gs *= s * s;
+  } else if (a.xscale == 2) {
+    const float ib = 1.f / a.bvec[item.x];
+    gs *= ib * ib;
   }
   const float c1 = a.c1 * kappa_pow(g, a.p1pow);
   const uint16_t* p1 = a.add1 >= 0 ? g.buf[a.add1] : nullptr;
@@ -228,15 +221,10 @@ __device__ __forceinline__ void gram_epilogue(const GramArgs& a, const int4 item
     }
     uint32_t w[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-      w[k] = a.out_bf16 ? pack_b16(f[2 * k], f[2 * k + 1]) : pack_f16(f[2 * k], f[2 * k + 1]);
+    for (int k = 0; k < 16; ++k) w[k] = pack_f16(f[2 * k], f[2 * k + 1]);
     store_sym_block(dst, ld, r, c, rbase, m, row_ok, diag_tile, mirror, lane, w, scratch);
-    if (dst2) {  // the same values into a second buffer
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        w[k] = a.out2_bf16 ? pack_b16(f[2 * k], f[2 * k + 1]) : pack_f16(f[2 * k], f[2 * k + 1]);
+    if (dst2)  // the same values into a second buffer
       store_sym_block(dst2, ld, r, c, rbase, m, row_ok, diag_tile, mirror, lane, w, scratch);
-    }
   }
 }
 
@@ -261,7 +249,7 @@ __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
   return s;
 }
 
-// XOP = 1: operands are X[src] (bf16); XOP = 0: buf[opA], buf[opB] (fp16).
+// XOP = 1: operands are X[src]; XOP = 0: buf[opA], buf[opB] (both fp16).
 template <int XOP>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gram_pair_kernel(const __grid_constant__ GramArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -350,7 +338,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gram_pair_kernel(const __g
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = XOP ? ptx::idesc_bf16(256, kBN, 0) : idesc_f16(256, kBN);
+      constexpr uint32_t idesc = ptx::idesc_f16(256, kBN, 0);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
@@ -374,7 +362,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gram_pair_kernel(const __g
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = ptx::desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = ptx::desc_sw128(sb + kk * 32, 16, 1024);
-            ptx::mma_bf16_pair(dt, ad, bd, idesc, (kb | kk) != 0);
+            ptx::mma_f16_pair(dt, ad, bd, idesc, (kb | kk) != 0);
           }
           issued = true;
           ptx::mma_commit_multicast(ptx::smem_addr(empty + s), 0x3);

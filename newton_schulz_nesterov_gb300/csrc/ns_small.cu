@@ -3,13 +3,15 @@
 // iterations and the update -- with the iterate, A and B resident in shared
 // memory and the products accumulated in TMEM.  For oriented shapes with
 // m <= 128 and n <= 512 (DMuon "Quick Start": TinyMLP projections at small
-// widths; 64x256 tensor-parallel shards): X is at most 128 x 512 bf16 =
+// widths; 64x256 tensor-parallel shards): X is at most 128 x 512 fp16 =
 // 128 KB, A and B 32 KB each.
 //
 // DMuon "API Reference", section "direct_newton_schulz": per step
 //   A = X X^T,  B = b A + c A A,  X = a X + B X,
-// computed here as X = Z X with Z = a I + B stored in bf16 (the a X term
-// rides in the product; no epilogue pass over X is needed).
+// computed here as X = Z X with Z = a I + B stored in fp16 (the a X term
+// rides in the product; no epilogue pass over X is needed).  The operands are
+// fp16 with power-of-two scales (X0 = p U with p from the block's max |U|,
+// later X as beta X, A as kappa X X^T), as on the chunked path.
 // section "Muon": momentum and the Nesterov input; section
 // "gram_newton_schulz_factors": normaliser = Frobenius norm + eps under the
 // orientation rule.
@@ -24,7 +26,7 @@
 // of them with several 16-byte loads in flight per thread.  In the
 // epilogues warp w reads TMEM lanes 32*(w%4).. (its rows) and takes half of
 // the columns (w/4).  Thread 0 issues the MMAs (M = 128, fp32 accumulate,
-// bf16 operands); every product completes on one mbarrier with a bounded
+// fp16 operands); every product completes on one mbarrier with a bounded
 // wait.
 #include "common.cuh"
 #include "ptx.cuh"
@@ -46,27 +48,31 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
                     ((col & 7) << 1));
 }
 
-__device__ __forceinline__ uint32_t bf16_bits(float f) {
-  const __nv_bfloat16 b = __float2bfloat16_rn(f);
+__device__ __forceinline__ uint32_t h_bits(float f) {
+  const __half b = __float2half_rn(f);
   return *reinterpret_cast<const uint16_t*>(&b);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) { return bf16_bits(lo) | (bf16_bits(hi) << 16); }
+__device__ __forceinline__ uint32_t pack_h(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 
-// Eight consecutive bf16 of one row (col % 8 == 0): one 16-byte chunk.
+// Eight consecutive fp16 of one row (col % 8 == 0): one 16-byte chunk.
 __device__ __forceinline__ void load8(const uint8_t* base, int row, int col, float (&f)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(base + swz(row, col));
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    f[2 * k] = __uint_as_float(w[k] << 16);
-    f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+    f[2 * k] = t.x;
+    f[2 * k + 1] = t.y;
   }
 }
 
 __device__ __forceinline__ void store8(uint8_t* base, int row, int col, const float (&f)[8]) {
   *reinterpret_cast<uint4*>(base + swz(row, col)) =
-      make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+      make_uint4(pack_h(f[0], f[1]), pack_h(f[2], f[3]), pack_h(f[4], f[5]), pack_h(f[6], f[7]));
 }
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -130,7 +136,7 @@ __device__ bool run_product(const Product& p, uint32_t tmem, uint32_t bar, uint3
                                      : ptx::desc_sw128(p.b_base, 16, 1024);
     for (int n0 = 0; n0 < p.n; n0 += 256) {
       const int nn = min(256, p.n - n0);
-      const uint32_t idesc = ptx::idesc_bf16(128, nn, p.b_mn_major ? 1 : 0);
+      const uint32_t idesc = ptx::idesc_f16(128, nn, p.b_mn_major ? 1 : 0);
       // MN-major B (X): K rows kb*64 + kk*16 of every 64-column block from
       // block n0/64; K-major B: rows 0..nn-1, K columns kb*64 + kk*16.
       const uint64_t bn = b0 + (uint64_t)((n0 >> 6) * (kSmallBlockBytes >> 4));
@@ -140,7 +146,7 @@ __device__ bool run_product(const Product& p, uint32_t tmem, uint32_t bar, uint3
                                          : b0 + (uint64_t)(kb * (kSmallBlockBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_bf16(tmem + n0, ak + 2 * kk, bk + (p.b_mn_major ? 128 * kk : 2 * kk), idesc, (kb | kk) != 0);
+          ptx::mma_f16(tmem + n0, ak + 2 * kk, bk + (p.b_mn_major ? 128 * kk : 2 * kk), idesc, (kb | kk) != 0);
       }
     }
     ptx::mma_commit(bar);
@@ -164,13 +170,35 @@ __device__ __forceinline__ float mom_u(const SmallArgs& a, float g, float m_old,
   return a.nesterov ? fmaf(a.mu, m_new, g) : m_new;
 }
 
-// Momentum pass: M <- mu*M + G, U, X0 = bf16(U) (or U^T) into shared
-// memory.  Returns this thread's sum of U^2 (fixed order).  Rows of 4k
-// floats go as float4 (G, M, W are 16-byte aligned); (row, column) advance
-// incrementally, no division per element.
-__device__ float momentum_pass(const SmallArgs& a, const MatPtrs& p, uint8_t* X, int rows, int cols, bool tr) {
+// U from G and the already updated momentum (the second pass).
+__device__ __forceinline__ float nest_u(const SmallArgs& a, float g, float m_new) {
+  if (a.ns_only) return g;
+  return a.nesterov ? fmaf(a.mu, m_new, g) : m_new;
+}
+
+// The two passes over G and M.  Pass 0: M <- mu*M + G and U; returns this
+// thread's max |U| (NaN inputs set *nan).  Pass 1: U again from G and the
+// updated M (the same fused multiply-adds, so the same U), X0 = fp16(p U)
+// (or p U^T) into shared memory; returns this thread's sum of (p U)^2 in a
+// fixed order.  The power of two p comes from the block's max |U| between
+// the passes, so p U never leaves fp16's normal range whatever the input's
+// scale.  Rows of 4k floats go as float4 (G, M, W are 16-byte aligned);
+// (row, column) advance incrementally, no division per element.
+__device__ float momentum_pass(const SmallArgs& a, const MatPtrs& p, uint8_t* X, int rows, int cols, bool tr,
+                               int pass, float ps, bool* nan) {
   const int tid = threadIdx.x;
-  float ss = 0.f;
+  float acc = 0.f;
+  bool bad = false;
+  auto take = [&](float u) {
+    if (pass == 0) {
+      acc = fmaxf(acc, fabsf(u));
+      bad |= u != u;
+      return 0.f;
+    }
+    const float x = u * ps;
+    acc = fmaf(x, x, acc);
+    return x;
+  };
   if ((cols & 3) == 0) {
     const int c4n = cols >> 2, total4 = rows * c4n;
     const int dr = kThreads / c4n, dc = kThreads % c4n;
@@ -198,24 +226,31 @@ __device__ float momentum_pass(const SmallArgs& a, const MatPtrs& p, uint8_t* X,
       for (int k = 0; k < kInFlight; ++k) {
         const int v = v0 + k * kThreads;
         if (v < total4) {
-          float4 mn = make_float4(0.f, 0.f, 0.f, 0.f);
-          const float u0 = mom_u(a, g[k].x, mo[k].x, mn.x);
-          const float u1 = mom_u(a, g[k].y, mo[k].y, mn.y);
-          const float u2 = mom_u(a, g[k].z, mo[k].z, mn.z);
-          const float u3 = mom_u(a, g[k].w, mo[k].w, mn.w);
-          if (!a.ns_only) M4[v] = mn;
-          ss = fmaf(u0, u0, ss);
-          ss = fmaf(u1, u1, ss);
-          ss = fmaf(u2, u2, ss);
-          ss = fmaf(u3, u3, ss);
-          const int col = 4 * cc[k];
-          if (!tr) {
-            *reinterpret_cast<uint2*>(X + swz(rr[k], col)) = make_uint2(pack_bf16(u0, u1), pack_bf16(u2, u3));
+          float u[4];
+          if (pass == 0) {
+            float4 mn = make_float4(0.f, 0.f, 0.f, 0.f);
+            u[0] = mom_u(a, g[k].x, mo[k].x, mn.x);
+            u[1] = mom_u(a, g[k].y, mo[k].y, mn.y);
+            u[2] = mom_u(a, g[k].z, mo[k].z, mn.z);
+            u[3] = mom_u(a, g[k].w, mo[k].w, mn.w);
+            if (!a.ns_only) M4[v] = mn;
           } else {
-            *reinterpret_cast<uint16_t*>(X + swz(col + 0, rr[k])) = (uint16_t)bf16_bits(u0);
-            *reinterpret_cast<uint16_t*>(X + swz(col + 1, rr[k])) = (uint16_t)bf16_bits(u1);
-            *reinterpret_cast<uint16_t*>(X + swz(col + 2, rr[k])) = (uint16_t)bf16_bits(u2);
-            *reinterpret_cast<uint16_t*>(X + swz(col + 3, rr[k])) = (uint16_t)bf16_bits(u3);
+            u[0] = nest_u(a, g[k].x, mo[k].x);
+            u[1] = nest_u(a, g[k].y, mo[k].y);
+            u[2] = nest_u(a, g[k].z, mo[k].z);
+            u[3] = nest_u(a, g[k].w, mo[k].w);
+          }
+          float x[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) x[j] = take(u[j]);
+          if (pass == 1) {
+            const int col = 4 * cc[k];
+            if (!tr) {
+              *reinterpret_cast<uint2*>(X + swz(rr[k], col)) = make_uint2(pack_h(x[0], x[1]), pack_h(x[2], x[3]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) *reinterpret_cast<uint16_t*>(X + swz(col + j, rr[k])) = (uint16_t)h_bits(x[j]);
+            }
           }
         }
       }
@@ -245,16 +280,23 @@ __device__ float momentum_pass(const SmallArgs& a, const MatPtrs& p, uint8_t* X,
       for (int k = 0; k < kInFlight; ++k) {
         const int e = e0 + k * kThreads;
         if (e < total) {
-          float mn = 0.f;
-          const float u = mom_u(a, g[k], mo[k], mn);
-          if (!a.ns_only) p.M[e] = mn;
-          ss = fmaf(u, u, ss);
-          *reinterpret_cast<uint16_t*>(X + (tr ? swz(cc[k], rr[k]) : swz(rr[k], cc[k]))) = (uint16_t)bf16_bits(u);
+          float u;
+          if (pass == 0) {
+            float mn = 0.f;
+            u = mom_u(a, g[k], mo[k], mn);
+            if (!a.ns_only) p.M[e] = mn;
+          } else {
+            u = nest_u(a, g[k], mo[k]);
+          }
+          const float x = take(u);
+          if (pass == 1)
+            *reinterpret_cast<uint16_t*>(X + (tr ? swz(cc[k], rr[k]) : swz(rr[k], cc[k]))) = (uint16_t)h_bits(x);
         }
       }
     }
   }
-  return ss;
+  if (bad) *nan = true;
+  return acc;
 }
 
 struct FinalCtx {
@@ -368,9 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t* X = base;                                  // 128 x 512 bf16, 8 blocks
-  uint8_t* A = base + 8 * kSmallBlockBytes;           // 128 x 128 bf16, 2 blocks
-  uint8_t* B = A + 2 * kSmallBlockBytes;              // 128 x 128 bf16, 2 blocks
+  uint8_t* X = base;                                  // 128 x 512 fp16, 8 blocks
+  uint8_t* A = base + 8 * kSmallBlockBytes;           // 128 x 128 fp16, 2 blocks
+  uint8_t* B = A + 2 * kSmallBlockBytes;              // 128 x 128 fp16, 2 blocks
   uint64_t* bar = reinterpret_cast<uint64_t*>(B + 2 * kSmallBlockBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);  // kWarps floats
@@ -409,8 +451,26 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
   uint32_t phase = 0;
   bool ok = true;
 
-  // ---- momentum, Nesterov input, X0, sum of squares (fixed order)
-  float ss = momentum_pass(a, p, X, rows, cols, tr);
+  // ---- momentum and Nesterov input: max |U| first, then p and X0 = p U with
+  // the sum of squares of p U (fixed order)
+  __shared__ int nan_seen;
+  if (tid == 0) nan_seen = 0;
+  __syncthreads();
+  bool nan = false;
+  float mx = momentum_pass(a, p, X, rows, cols, tr, 0, 1.f, &nan);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[warp] = mx;
+  if (nan) nan_seen = 1;
+  __syncthreads();  // also orders this CTA's momentum stores before the second pass reads them
+  mx = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red[w]);
+  int ex = 0;
+  frexpf(mx, &ex);
+  const float ps = (mx > 0.f && !isinf(mx)) ? ldexpf(1.f, min(127, max(-126, 11 - ex))) : 1.f;
+  __syncthreads();
+  float ss = momentum_pass(a, p, X, rows, cols, tr, 1, ps, &nan);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) red[warp] = ss;
@@ -419,9 +479,25 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
   double tot = 0.0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) tot += (double)red[w];
-  const bool finite = isfinite(tot);
-  const float s = finite ? (float)(1.0 / (sqrt(tot) + (double)a.eps)) : 0.f;
+  const bool finite = !nan_seen && !isinf(mx) && isfinite(tot);
+  // s = 1 / (||U|| + eps), ||U|| = sqrt(tot) / ps; X0 holds ps U, so the first
+  // products take s/ps (= 0 for a zero or non-finite input)
+  const float s = (finite && mx > 0.f) ? (float)(1.0 / (sqrt(tot) / (double)ps + (double)a.eps)) : 0.f;
+  const float s_x0 = (finite && mx > 0.f) ? (float)(1.0 / (sqrt(tot) + (double)a.eps * (double)ps)) : 0.f;
   if (tid == 0 && !finite) a.flags[d.idx] |= 1;
+  // fp16 scales: A holds kappa X X^T, X after the first product beta' X with
+  // beta' = beta / 2^floor(log2 nu) when nu = ||X0||_F = ||U|| / (||U|| + eps)
+  // is below 1/2 (an input far below eps), else beta
+  float beta = scale_beta(n);
+  {
+    const double r = sqrt(tot), nu = r / (r + (double)a.eps * (double)ps);
+    if (finite && nu < 0.5 && nu > 0.0) {
+      int ex = 0;
+      frexp(nu, &ex);
+      beta = ldexpf(beta, min(100, 1 - ex));
+    }
+  }
+  const float kap = scale_kappa(m), ikap = 1.f / kap, ibeta = 1.f / beta;
 
   const uint32_t xs = ptx::smem_addr(X), as = ptx::smem_addr(A), bs = ptx::smem_addr(B);
   const uint32_t bar_a = ptx::smem_addr(bar);
@@ -432,11 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
     const float ca = a.coeffs[k][0], cb = a.coeffs[k][1], cc = a.coeffs[k][2];
     const bool first = k == 0;
     const bool last = k == a.ns_steps - 1;
-    // A = X X^T (N = m_pad, K = n_pad); the first iteration scales by s^2
+    // X = xsc * (stored X): s/p for X0 = p U, 1/beta afterwards
+    const float xsc = first ? s_x0 : ibeta;
+    // A = kappa xsc^2 X X^T (N = m_pad, K = n_pad)
     ok = run_product(Product{xs, xs, n_pad >> 6, false, m_pad}, tmem, bar_a, phase, a.err, limit);
     if (!ok) break;
     {
-      const float alpha = first ? s * s : 1.f;
+      const float alpha = kap * xsc * xsc;
       for (int c0 = h * hw; c0 < (h + 1) * hw; c0 += 32) {
         uint32_t v[32];
         ptx::tmem_ld32(tq + c0, v);
@@ -452,9 +530,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
     ptx::tc_fence_before();
     fence_async_smem();
     __syncthreads();
-    // Z = a I + b A + c A A (N = K = m_pad), stored where B lives
+    // Z = a I + (b/kappa) A + (c/kappa^2) A A (N = K = m_pad), stored where B lives
     ok = run_product(Product{as, as, m_pad >> 6, false, m_pad}, tmem, bar_a, phase, a.err, limit);
     if (!ok) break;
+    const float gcc = cc * ikap * ikap, gcb = cb * ikap;
     for (int c0 = h * hw; c0 < (h + 1) * hw; c0 += 32) {
       uint32_t v[32];
       ptx::tmem_ld32(tq + c0, v);
@@ -464,18 +543,18 @@ __global__ void __launch_bounds__(kThreads, 1) ns_small_kernel(const __grid_cons
         load8(A, row, c0 + j, av);
 #pragma unroll
         for (int t = 0; t < 8; ++t)
-          o[t] = fmaf(cc, __uint_as_float(v[j + t]), cb * av[t]) + (c0 + j + t == row ? ca : 0.f);
+          o[t] = fmaf(gcc, __uint_as_float(v[j + t]), gcb * av[t]) + (c0 + j + t == row ? ca : 0.f);
         store8(B, row, c0 + j, o);
       }
     }
     ptx::tc_fence_before();
     fence_async_smem();
     __syncthreads();
-    // X' = Z X (M = 128, N = n_pad, K = m_pad; X as the MN-major operand);
-    // the first iteration scales by s
+    // X' = beta xsc Z X stored (M = 128, N = n_pad, K = m_pad; X as the
+    // MN-major operand); the last product gives O = xsc Z X in fp32
     ok = run_product(Product{bs, xs, m_pad >> 6, true, n_pad}, tmem, bar_a, phase, a.err, limit);
     if (!ok) break;
-    const float alpha = first ? s : 1.f;
+    const float alpha = last ? xsc : xsc * beta;
     const int half = n_pad >> 1;
     if (!last) {
       for (int c0 = h * half; c0 < (h + 1) * half; c0 += 32) {

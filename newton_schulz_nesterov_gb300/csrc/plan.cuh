@@ -23,9 +23,9 @@ inline int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 struct Layout {
   std::vector<MatDesc> mats;       // device pointers filled in once allocated
   std::vector<int64_t> xoff, aoff, boff;  // workspace byte offsets
-  std::vector<int64_t> goff;       // Gram-space buffers: kGramBufs per matrix (gram plans; -1 unused)
+  std::vector<int64_t> goff;       // Gram-space buffers: kGramBufs per matrix (gram plans)
   std::vector<int64_t> tile_prefix;
-  size_t ws_bytes = 0;             // big bf16 workspace
+  size_t ws_bytes = 0;             // big fp16 workspace
   std::vector<int4> items[3];
   std::vector<int> starts[3];      // per processor: first item of its run (procs + 1 entries)
   int procs[3] = {0, 0, 0};        // persistent CTAs (or CTA pairs) to launch per phase
@@ -73,15 +73,15 @@ inline void deal_items(std::vector<int4>& items, int procs, bool balanced, std::
   starts[used] = k;
 }
 
-// Workspace of a chunk.  Direct plans: X[0], X[1] (m x n bf16), A, B
-// (m x m bf16) per matrix.  Gram plans: X[0], X[1] and the kGramBufs m x m
-// buffers of the Gram-space window (R[2], B, T, Q[2] fp16; Q bf16).
+// Workspace of a chunk.  Direct plans: X[0], X[1] (m x n fp16), A, B
+// (m x m fp16) per matrix.  Gram plans: X[0], X[1] and the kGramBufs m x m
+// fp16 buffers of the Gram-space window (R[2], Z[2], W, Q[2], the window's
+// last Q).
 inline void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair, int procs, bool balanced,
-                 bool gram = false, bool implicit = false) {
+                 bool gram = false) {
   L.mats.assign(n, MatDesc{});
   L.xoff.resize(n); L.aoff.resize(n); L.boff.resize(n);
   L.goff.assign(gram ? (size_t)n * kGramBufs : 0, -1);
-  const int nbuf = implicit ? kGramBufs : kGramBufsExplicit;
   L.tile_prefix.assign(n + 1, 0);
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off += (size_t)rup((int64_t)bytes, 256); return (int64_t)o; };
@@ -94,9 +94,11 @@ inline void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair
     d.n = std::max(d.rows, d.cols);
     d.ldx = rup(d.n, 8);
     d.lda = rup(d.m, 8);
+    d.kappa = scale_kappa(d.m);
+    d.beta = scale_beta(d.n);
     L.xoff[i] = take((size_t)(2 * d.m * d.ldx * 2));  // X[0] and X[1] back to back
     if (gram) {
-      for (int b = 0; b < nbuf; ++b) L.goff[(size_t)i * kGramBufs + b] = take((size_t)(d.m * d.lda * 2));
+      for (int b = 0; b < kGramBufs; ++b) L.goff[(size_t)i * kGramBufs + b] = take((size_t)(d.m * d.lda * 2));
       L.aoff[i] = L.boff[i] = L.goff[(size_t)i * kGramBufs + kGbQb];
     } else {
       L.aoff[i] = take((size_t)(d.m * d.lda * 2));

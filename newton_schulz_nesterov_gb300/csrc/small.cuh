@@ -11,7 +11,7 @@ namespace dmuon {
 // Oriented shapes handled by the fused kernel: m <= 128, n <= 512.
 constexpr int kSmallMaxM = 128;
 constexpr int kSmallMaxN = 512;
-constexpr int kSmallBlockBytes = 128 * 128;  // one 64-column block of 128 rows (bf16)
+constexpr int kSmallBlockBytes = 128 * 128;  // one 64-column block of 128 rows (fp16)
 constexpr int kSmallThreads = 256;
 constexpr int kSmallSmem = 1024 /*align slack*/ + 12 * kSmallBlockBytes + 256;
 

@@ -31,37 +31,47 @@ def apply_flops(shapes, ns_steps=5):
 
 def elementwise_bytes(shapes):
     """Algorithmic HBM bytes of the momentum/normalise pass: read G and M,
-    write M (fp32) and the bf16 iterate: 14 bytes per element."""
+    write M (fp32) and the fp16 iterate: 14 bytes per element."""
     return sum(14 * r * c for r, c in shapes)
+
+
+def gram_windows(ns_steps, restarts=(2,), max_window=2):
+    """Restart windows the Gram backend runs: the restart positions inside
+    (0, ns_steps), each window longer than ``max_window`` steps split into
+    ceil(len / max_window) windows as even as possible, longer ones first."""
+    cuts = sorted({int(k) for k in restarts if 0 < int(k) < ns_steps})
+    bounds = [0] + cuts + [ns_steps]
+    out = []
+    for i in range(len(bounds) - 1):
+        a, b = bounds[i], bounds[i + 1]
+        if b <= a:
+            continue
+        length = b - a
+        parts = -(-length // max_window)
+        for j in range(parts):
+            w = length // parts + (1 if j < length % parts else 0)
+            out.append((a, a + w))
+            a += w
+    return out
 
 
 def gram_flops(shapes, ns_steps=5, restarts=(2,)):
     """Algorithmic flops of the Gram-space backend, symmetric products as one
-    triangle.  Per restart window: per step Z from R R (m^3), Q' = Z Q on all
-    but the window's first step (m^3), R Z and Z (R Z) on all but its last
-    (2 m^3).  Matrices with n < 2m restart explicitly: per window X X^T
-    (m^2 n) and a closing Q X (2 m^2 n); five steps with a restart before
-    the third give 6 m^2 n + 14 m^3.  Matrices with n >= 2m restart
-    implicitly: one X X^T and one final Q X (3 m^2 n), two m^3 products per
-    restart, one more per restart after the first (the factor accumulator)
-    and one for the total factor: 3 m^2 n + 17 m^3 for the same schedule."""
-    cuts = sorted({int(k) for k in restarts if 0 < int(k) < ns_steps})
-    bounds = [0] + cuts + [ns_steps]
-    windows = [(bounds[i], bounds[i + 1]) for i in range(len(bounds) - 1) if bounds[i + 1] > bounds[i]]
+    triangle.  Per restart window: X X^T (m^2 n) and a closing Q X (2 m^2 n);
+    per step Z from R R (m^3), Q' = Z Q on all but the window's first step
+    (m^3), R Z and Z (R Z) on all but its last (2 m^3).  Windows are at most
+    two steps long, so five steps (with the default restart before the
+    third, or none) run as windows of 2, 2 and 1 steps: 9 m^2 n + 11 m^3."""
+    windows = gram_windows(ns_steps, restarts)
     tot = 0
     for r, c in shapes:
         m, n = min(r, c), max(r, c)
-        implicit = n >= 2 * m
         for start, end in windows:
-            if not implicit:
-                tot += 3 * m * m * n
+            tot += 3 * m * m * n
             for k in range(start, end):
                 tot += m ** 3
                 if k > start:
                     tot += m ** 3
                 if k < end - 1:
                     tot += 2 * m ** 3
-        if implicit and windows:
-            nw = len(windows)
-            tot += 3 * m * m * n + 2 * m ** 3 * (nw - 1) + m ** 3 * max(0, nw - 2) + (m ** 3 if nw > 1 else 0)
     return tot

@@ -12,6 +12,7 @@ import re
 import pytest
 
 import newton_schulz_nesterov_gb300 as dm
+import oracle
 from newton_schulz_nesterov_gb300 import _build, flops, workloads
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -156,22 +157,21 @@ def test_workload_shapes_and_flop_totals():
 
 
 def test_gram_flop_count():
-    """Gram backend: per window Z (m^3 per step), Q' (m^3, not on the
-    window's first step), R Z and Z (R Z) (2 m^3, not on its last).
-    n < 2m (explicit restarts): per window X X^T (m^2 n) and Q X (2 m^2 n).
-    n >= 2m (implicit restarts): one X X^T and one Q X, 2 m^3 per restart,
-    m^3 per accumulation after the first restart and for the total factor."""
-    m, n = 96, 150                                                            # explicit
-    assert flops.gram_flops([(m, n)]) == 6 * m * m * n + 14 * m ** 3         # restart before step 2
-    assert flops.gram_flops([(n, m)], 5, ()) == 3 * m * m * n + (5 + 4 + 2 * 4) * m ** 3     # one window
+    """Gram backend: per window X X^T (m^2 n) and Q X (2 m^2 n), Z (m^3 per
+    step), Q' (m^3, not on the window's first step), R Z and Z (R Z) (2 m^3,
+    not on its last); windows longer than two steps are split."""
+    m, n = 96, 150
+    assert flops.gram_windows(5, (2,)) == flops.gram_windows(5, ()) == [(0, 2), (2, 4), (4, 5)]
+    assert flops.gram_flops([(m, n)]) == 9 * m * m * n + 11 * m ** 3
+    assert flops.gram_flops([(n, m)], 5, ()) == flops.gram_flops([(n, m)], 5, (2, 4))
     assert flops.gram_flops([(m, n)], 1, (2,)) == 3 * m * m * n + m ** 3      # one window, one step
+    assert flops.gram_flops([(m, n)], 2, ()) == 3 * m * m * n + 5 * m ** 3    # Z, W, R', Z, Q'
     assert flops.gram_flops([(m, n)], 3, (1, 2)) == 3 * (3 * m * m * n + m ** 3)
     assert flops.gram_flops([(m, n)], 0) == 0
-    m, n = 96, 300                                                            # implicit
-    assert flops.gram_flops([(m, n)]) == 3 * m * m * n + 17 * m ** 3
-    assert flops.gram_flops([(n, m)], 5, ()) == 3 * m * m * n + 17 * m ** 3  # one window: same count
-    assert flops.gram_flops([(m, n)], 3, (1, 2)) == 3 * m * m * n + (3 + 2 * 2 + 1 + 1) * m ** 3
-    # cheaper than the direct iteration when n > m, equal for square matrices
+    assert flops.gram_windows(8, ()) == [(0, 2), (2, 4), (4, 6), (6, 8)]
+    assert flops.gram_windows(7, (2, 4)) == [(0, 2), (2, 4), (4, 6), (6, 7)]
+    assert flops.gram_windows(5, (1,)) == [(0, 1), (1, 3), (3, 5)]
+    # 9 m^2 n + 11 m^3 against 15 m^2 n + 5 m^3: cheaper when n > m, equal for square matrices
     assert flops.gram_flops([(1024, 4096)]) < flops.algorithmic_flops([(1024, 4096)])
     assert flops.gram_flops([(1024, 1024)]) == flops.algorithmic_flops([(1024, 1024)])  # break-even at n = m
 
@@ -180,8 +180,7 @@ def test_gram_workspace_bytes(lib):
     shapes = list(workloads.get("llama3_8b").shapes)
     direct = dm.dmuon_workspace_bytes(shapes)
     gram = dm.dmuon_workspace_bytes(shapes, "gram")
-    # chunks gain up to ten m x m 16-bit buffers per matrix in place of A and B; Gram plans group
-    # the square matrices (explicit restarts) apart from the rectangular ones (implicit restarts)
+    # chunks hold eight m x m fp16 buffers per matrix in place of A and B
     assert direct < gram < 4 * direct
     out = ctypes.c_size_t()
     arr = (dm.Shape * 1)(dm.Shape(64, 64))
@@ -243,13 +242,18 @@ def test_gram_range_check(lib):
     assert ok and why == ""
     assert dm.dmuon_gram_check_coefficients(5, dm.dmuon_polar_express_coefficients(5))[0]
     assert dm.dmuon_gram_check_coefficients(5, dm.dmuon_polar_express_coefficients(5), restarts=())[0]
-    ok, why = dm.dmuon_gram_check_coefficients(8, restarts=())
-    assert not ok and "gain" in why          # one window of 8 default steps: gain 1.1e4
+    # eight steps without restarts run as four windows of two steps
+    assert dm.dmuon_gram_check_coefficients(8, restarts=())[0]
+    assert dm.dmuon_gram_check_coefficients(8, oracle.coefficient_rows(8), restarts=())[0]
     assert dm.dmuon_gram_check_coefficients(8, restarts=(3, 6))[0]
     ok, why = dm.dmuon_gram_check_coefficients(1, [(1.0, 100.0, 0.0)])
     assert not ok and "kappa R Z" in why     # 1024 x 101 at the top of the spectrum
     ok, why = dm.dmuon_gram_check_coefficients(3, [(1.0, 25.0, 0.0)] * 3, restarts=())
     assert not ok and "singular values" in why   # x + 25 x^3 sends 1 to 26
+    for row in ((0.0, 1.0, 0.0), (0.0, 0.0, 1.0), (-1.0, 2.0, 0.0), (0.01, 1.0, 0.0)):
+        ok, why = dm.dmuon_gram_check_coefficients(1, [row])
+        assert not ok and "1/64" in why          # no identity part: the fp16 Z would lose its small entries
+    assert dm.dmuon_gram_check_coefficients(1, [(1.0 / 64, 1.0, 0.0)])[0]
     ok, _ = dm.dmuon_gram_check_coefficients(0)
     assert ok
     # argument errors
@@ -266,7 +270,6 @@ def _preview(shapes, **kw):
     bal = fields["balance"].split()
     items = fields["items"].split()
     return out, {"tiles": fields["tiles"], "chunks": int(fields["chunks"].split()[0]),
-                 "implicit": int(fields["chunks"].split("implicit-restart ")[1].rstrip(")")),
                  "small": int(fields["small-matrix"].split()[-1]),
                  "items": {items[i]: int(items[i + 1]) for i in range(0, 6, 2)},
                  "balance": {bal[i]: float(bal[i + 1]) for i in range(0, 6, 2)}}
@@ -290,8 +293,8 @@ def test_plan_preview_items_dealing_and_chunks(lib):
     """The host planner without a device: work-item counts match their
     definition, longest-first dealing evens one Llama-3-8B layer's Gram list
     (strided leaves the pairs that drew extra long tiles ~10 % behind), the
-    full set splits into 14 chunks of at most 2^29 elements, and the Gram
-    backend puts the 12 chunks of n >= 2m matrices on implicit restarts."""
+    full set splits into 14 chunks of at most 2^29 elements, for either
+    backend."""
     layer = workloads.get("llama3_8b_1layer").shapes
     _, p = _preview(layer)
     assert p["tiles"] == "256x256 CTA pairs" and p["chunks"] == 1
@@ -303,7 +306,7 @@ def test_plan_preview_items_dealing_and_chunks(lib):
     _, f = _preview(full)
     assert f["chunks"] == 14 and f["items"] == _pair_items(full) and f["balance"]["gram"] <= 1.02
     _, gb = _preview(full, backend="gram")
-    assert gb["chunks"] == 14 and gb["implicit"] == 12
+    assert gb["chunks"] == 14 and gb["items"] == _pair_items(full)
 
 
 def test_plan_preview_tile_choice(lib):

@@ -18,9 +18,10 @@ from newton_schulz_nesterov_gb300 import _build, workloads  # noqa: E402
 import oracle  # noqa: E402
 from oracle import gram as og  # noqa: E402
 
+from _parity import assert_momentum  # noqa: E402
+
 pytestmark = pytest.mark.gpu
 
-MOM_TOL = 1e-6
 NS_TOL = 3e-2
 F32 = lambda x: float(np.float32(x))  # noqa: E731
 
@@ -86,13 +87,25 @@ def test_gram_restart_sets(handle, ns_steps, restarts, coeffs):
 
 
 def test_gram_scaled_inputs(handle):
+    """Inputs over the whole fp32 range (1e-30 ... 1e30), one call per scale
+    on one handle and all scales in one list, against the fp64 Gram oracle."""
     gen = torch.Generator().manual_seed(205)
     base = torch.randn((300, 520), generator=gen)
-    for scale in (1e-6, 1e-3, 1.0, 1e3):
+    scales = (1e-30, 1e-20, 1e-6, 1e-3, 1.0, 1e3, 1e15, 1e30)
+    for scale in scales:
         x = (base * scale).cuda()
         o = torch.empty_like(x)
         handle.gram_newton_schulz([x], [o])
-        assert rel_fro(o.cpu().numpy(), og.gram_newton_schulz(x.cpu().numpy())) <= NS_TOL, scale
+        assert handle.status()[0] == 0
+        assert bool(torch.isfinite(o).all()), scale
+        ref = og.gram_newton_schulz(x.cpu().numpy().astype(np.float64))
+        assert rel_fro(o.cpu().numpy(), ref) <= NS_TOL, scale
+    xs = [(base[:, : 300 + 20 * k] * sc).cuda() for k, sc in enumerate(scales)]
+    outs = [torch.empty_like(x) for x in xs]
+    handle.gram_newton_schulz(xs, outs)
+    assert handle.status()[0] == 0
+    for x, o, sc in zip(xs, outs, scales):
+        assert rel_fro(o.cpu().numpy(), og.gram_newton_schulz(x.cpu().numpy().astype(np.float64))) <= NS_TOL, sc
 
 
 @pytest.mark.parametrize("kw", [dict(), dict(nesterov=False), dict(wd=0.1), dict(scale_mode=2),
@@ -112,20 +125,22 @@ def test_gram_step(handle, kw):
         ref = og.muon_step_gram(Ws[i].numpy(), Gs[i].numpy(), Ms[i].numpy(), lr=F32(0.05), mu=F32(0.9),
                                 wd=F32(wd), ns_steps=ns, restarts=(2,) if rs is None else rs, **kw)
         W0 = Ws[i].numpy().astype(np.float64)
-        assert rel_fro(Md[i].cpu().numpy(), ref["M"]) <= MOM_TOL
+        assert_momentum(Md[i].cpu().numpy(), ref["M"])
         e = rel_fro(Wd[i].cpu().numpy().astype(np.float64) - W0, ref["W"] - W0)
         assert e <= NS_TOL, (s, kw, e)
 
 
 def test_gram_and_direct_backends_agree(handle):
-    """Same step with both backends on one handle (the plan switches): both
-    meet the bar and agree with each other."""
+    """Same step with both backends on one handle (the plan switches) and
+    the same coefficient table (the Gram backend's default, Polar Express):
+    both meet the bar and agree with each other."""
     shapes = [(512, 1536), (1536, 512)]
     Ws, Gs, Ms = _inputs(shapes, 209)
+    table = dm.dmuon_polar_express_coefficients(5)
     res = {}
     for backend in ("direct", "gram", "direct"):
         Wd, Gd, Md = _dev(Ws), _dev(Gs), _dev(Ms)
-        handle.step(Wd, Gd, Md, backend=backend)
+        handle.step(Wd, Gd, Md, backend=backend, coeffs=table)
         assert handle.status()[0] == 0
         res.setdefault(backend, []).append([w.cpu() for w in Wd])
     for a, b in zip(res["direct"][0], res["direct"][1]):
@@ -135,12 +150,10 @@ def test_gram_and_direct_backends_agree(handle):
 
 
 @pytest.mark.parametrize("shapes,launches", [
-    # n >= 2m: implicit restarts.  2 (momentum, norm) + X X^T + window 1 (Z, W, R', Z, Q')
-    # + restart (R_start Q, Q W) + window 2 (Z, W, R', Z, Q', W, R', Z, Q') + total factor + Q X
+    # 4 (momentum pass, norm, redo pass, its norm) + window [0, 2) (X X^T, Z W R', Z Q') + Q X
+    # + window [2, 4) (the same) + Q X + window [4, 5) (X X^T, Z) + final Q X, whatever the aspect ratio
     ([(300, 900), (700, 300)], 21),
-    # n < 2m: explicit restarts.  2 + window 1 (X X^T, 3 + 2 products) + restart Q X
-    # + window 2 (X X^T, 3 + 4 + 2 products) + final Q X
-    ([(300, 500), (700, 400)], 20),
+    ([(300, 500), (700, 400)], 21),
 ])
 def test_gram_deterministic_and_launch_count(handle, shapes, launches):
     Ws, Gs, Ms = _inputs(shapes, 211)
@@ -188,14 +201,6 @@ def test_polar_express_table(path):
     gen = torch.Generator().manual_seed(211)
     ins = [torch.randn(s, generator=gen) for s in shapes] + [_spiked(s, 212 + i) for i, s in enumerate(spiked)]
     shapes = shapes + spiked
-    if path == "gram_no_restart":
-        # Square Gaussian matrices have singular values near 0; without the
-        # restart the fp16 Gram matrix's rounding stays in all five steps and
-        # the Polar Express table's large first step leaves 3.9e-2 on a
-        # 200 x 200 one (an emulation of the kernels' roundings gives the same),
-        # so the no-restart run takes the rectangular inputs only.
-        keep = [i for i, s in enumerate(shapes) if s[0] != s[1]]
-        ins, shapes = [ins[i] for i in keep], [shapes[i] for i in keep]
     outs = [torch.empty(s, device="cuda") for s in shapes]
     with dm.Handle(0) as h2:
         if path != "small":
@@ -218,22 +223,64 @@ def test_polar_express_table(path):
         assert e <= NS_TOL, (path, s, e)
 
 
+GRAM_STRESS = ["ill_300x700_r164", "ill_128x4096_r1e3", "ill_500x500_r1e4", "gauss_200x200", "gauss_384x384",
+               "spiked_512x512", "spiked_700x300"]
+
+
+def _stress_input(name):
+    """The inputs on which the fp16 Gram form is weakest: singular values
+    spread log-uniformly over [1/ratio, 1] (ratio 164 is the spread
+    1.1e-3 ... 0.18 of a normalised 300 x 700 matrix), square Gaussian
+    matrices (singular values down to ~0) and Gaussian bulks with a rank-16
+    spike from 1e2 down to 1e-3."""
+    from _parity import spectrum_matrix
+    kind, shape = name.split("_")[:2]
+    r, c = (int(v) for v in shape.split("x"))
+    if kind == "ill":
+        ratio = float(name.split("_r")[1])
+        return torch.from_numpy(spectrum_matrix(r, c, ratio, 41))
+    if kind == "gauss":
+        return torch.randn((r, c), generator=torch.Generator().manual_seed(43))
+    return _spiked((r, c), 45)
+
+
+@pytest.mark.parametrize("restarts", [(2,), (), (1,)])
+@pytest.mark.parametrize("table", ["polar_express", "you"])
+def test_gram_stress_inputs(handle, table, restarts):
+    """Every stress input, both tables, the default restart and none (both
+    run as windows of 2 + 2 + 1 steps) and a restart before the second step
+    (windows of 1 + 2 + 2): each within 3e-2 of the fp64 Gram oracle."""
+    from oracle import polar_express as pe
+    coeffs = None if table == "polar_express" else oracle.coefficient_rows(5)
+    ins = [_stress_input(n) for n in GRAM_STRESS]
+    outs = [torch.empty_like(x, device="cuda") for x in ins]
+    handle.gram_newton_schulz(_dev(ins), outs, ns_steps=5, coeffs=coeffs, restarts=restarts)
+    assert handle.status()[0] == 0
+    ref_coeffs = pe.polar_express_rows(5) if coeffs is None else coeffs
+    for name, x, o in zip(GRAM_STRESS, ins, outs):
+        ref = og.gram_newton_schulz(x.numpy().astype(np.float64), 5, coeffs=ref_coeffs, restarts=restarts)
+        e = rel_fro(o.cpu().numpy(), ref)
+        assert e <= NS_TOL, (name, table, restarts, e)
+
+
 def test_gram_argument_errors(handle):
     x = torch.randn((300, 900), device="cuda")
     o = torch.empty_like(x)
     p = [x.data_ptr()], [o.data_ptr()], [(300, 900)]
     before = dm.dmuon_launch_count(handle.h)
     # a window of 8 steps without restart: gain prod |a| ~ 1.1e4 > 8192
-    assert dm.dmuon_gram_newton_schulz_ptrs(handle.h, *p, ns_steps=8, restarts=(), check=False) == -1
-    assert "gain" in dm.dmuon_last_error(handle.h)
     assert dm.dmuon_gram_newton_schulz_ptrs(handle.h, *p, ns_steps=1, coeffs=[(1.0, 25.0, 0.0)],
                                             check=False) == -1
+    assert "fp16" in dm.dmuon_last_error(handle.h)   # x + 25 x^3: singular values past kappa R's range
+    assert dm.dmuon_gram_newton_schulz_ptrs(handle.h, *p, ns_steps=1, coeffs=[(0.0, 0.0, 1.0)], check=False) == -1
+    assert "1/64" in dm.dmuon_last_error(handle.h)
     assert dm.dmuon_launch_count(handle.h) == before
-    # with restarts the same 8 steps are fine
-    assert dm.dmuon_gram_newton_schulz_ptrs(handle.h, *p, ns_steps=8, restarts=(3, 6), check=False) == 0
-    assert handle.status()[0] == 0
-    ref = og.gram_newton_schulz(x.cpu().numpy(), 8, restarts=(3, 6))
-    assert rel_fro(o.cpu().numpy(), ref) <= NS_TOL
+    # eight steps without a restart run as four windows of two steps, the same function
+    for restarts in ((), (3, 6)):
+        assert dm.dmuon_gram_newton_schulz_ptrs(handle.h, *p, ns_steps=8, restarts=restarts, check=False) == 0
+        assert handle.status()[0] == 0
+        ref = og.gram_newton_schulz(x.cpu().numpy(), 8, restarts=restarts)
+        assert rel_fro(o.cpu().numpy(), ref) <= NS_TOL
 
 
 def test_gram_step_in_cuda_graph(handle):
@@ -277,7 +324,7 @@ def test_gram_full_llama3_8b_sampled(handle):
     for i in sample:
         ref = og.muon_step_gram(W0[i].numpy(), Gd[i].cpu().numpy(), M0[i].numpy(), lr=F32(0.02), mu=F32(0.95))
         w0 = W0[i].numpy().astype(np.float64)
-        assert rel_fro(Md[i].cpu().numpy(), ref["M"]) <= MOM_TOL
+        assert_momentum(Md[i].cpu().numpy(), ref["M"])
         e = rel_fro(Wd[i].cpu().numpy().astype(np.float64) - w0, ref["W"] - w0)
         assert e <= NS_TOL, (i, w.shapes[i], e)
     del Wd, Md, Gd
@@ -339,7 +386,7 @@ def _gram_full_size_sampled(name, sample):
     for i in sample:
         ref = og.muon_step_gram(W0[i].numpy(), Gd[i].cpu().numpy(), M0[i].numpy(), lr=F32(0.02), mu=F32(0.95))
         w0 = W0[i].numpy().astype(np.float64)
-        assert rel_fro(Md[i].cpu().numpy(), ref["M"]) <= MOM_TOL
+        assert_momentum(Md[i].cpu().numpy(), ref["M"])
         e = rel_fro(Wd[i].cpu().numpy().astype(np.float64) - w0, ref["W"] - w0)
         assert e <= NS_TOL, (name, i, w.shapes[i], e)
     del Wd, Md, Gd
@@ -361,9 +408,9 @@ def test_gram_full_tp_70b_mixed_sampled(handle):
 
 
 def test_gram_chunking_is_bitwise_neutral(handle):
-    """One chunk per restart kind, many chunks, and many chunks with the
-    next chunk's momentum pass overlapped (chunks alternating between two
-    workspaces that hold their Gram-window buffers) give the same bits."""
+    """One chunk, many chunks, and many chunks with the next chunk's
+    momentum pass overlapped (chunks alternating between two workspaces that
+    hold their Gram-window buffers) give the same bits."""
     gen = torch.Generator().manual_seed(217)
     shapes = [(300, 500), (500, 300), (257, 257), (200, 900), (900, 200), (130, 900)]
     Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
@@ -381,8 +428,7 @@ def test_gram_chunking_is_bitwise_neutral(handle):
             res[elems] = ([x.cpu() for x in Wd + Md], summary)
     import re
     n_chunks = {k: int(re.search(r"chunks (\d+) ", v[1]).group(1)) for k, v in res.items()}
-    # one chunk per restart kind (square-ish matrices restart explicitly, n >= 2m implicitly)
-    assert n_chunks[1 << 29] == 2 and n_chunks[200_000] > 2
+    assert n_chunks[1 << 29] == 1 and n_chunks[200_000] > 2
     for key in (200_000, 200_001):
         for a, b in zip(res[1 << 29][0], res[key][0]):
             assert torch.equal(a, b)
