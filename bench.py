@@ -51,6 +51,10 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-aux", action="store_true")
     p.add_argument("--no-gram", action="store_true")
+    p.add_argument("--fused", default="auto", choices=["auto", "always", "never"],
+                   help="direct backend: one launch per chunk for all products (auto: the library's rule)")
+    p.add_argument("--no-split", action="store_true",
+                   help="skip the per-phase breakdown (a few steps with one launch per phase)")
     p.add_argument("--tile-mode", type=int, default=0, choices=[0, 1, 2],
                    help="direct backend tiles: 0 automatic, 1 single CTAs (128x256), 2 CTA pairs (256x256)")
     p.add_argument("--dealing", default="balanced", choices=["balanced", "strided"],
@@ -103,6 +107,28 @@ def apply_traffic(workload):
     return int(per.group(1)) * layers
 
 
+def fused_traffic(workload):
+    """DRAM bytes per fused launch from the committed ncu summary of the
+    fused kernel, None unless the kernel sources and the launch planning
+    hash to the captured version and the workload is the one captured."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", "ns_fused_pair_llama3_8b.md")
+    if workload != "llama3_8b" or not os.path.exists(path):
+        return None
+    text = open(path).read()
+    sha = re.search(r"source_sha1:\s*([0-9a-f]{40})", text)
+    per = re.search(r"dram_bytes_per_launch:\s*(\d+)", text)
+    if not sha or not per:
+        return None
+    csrc = os.path.join(ROOT, "newton_schulz_nesterov_gb300", "csrc")
+    src = b"".join(open(os.path.join(csrc, f), "rb").read()
+                   for f in ("ns_gemm.cu", "common.cuh", "ptx.cuh", "plan.cuh"))
+    if hashlib.sha1(src).hexdigest() != sha.group(1):
+        return None
+    return int(per.group(1))
+
+
 def apply_roofline(shapes, steps, apply_ms, apply_n, peak, peak_src, pairs, step_traffic, ns_steps=5):
     """Roofline object of the Apply kernel from its summed CUDA-event time
     (apply_ms over apply_n launches in `steps` timed steps): achieved
@@ -124,6 +150,31 @@ def apply_roofline(shapes, steps, apply_ms, apply_n, peak, peak_src, pairs, step
             "algorithmic_bytes": alg_bytes,
             "launches_per_step": launches_per_step,
             "avg_launch_ms": apply_ms / apply_n}
+
+
+def fused_roofline(shapes, steps, fused_ms, fused_n, peak, peak_src, pairs, launch_traffic, ns_steps=5):
+    """Roofline object of the fused Newton-Schulz kernel (every Gram, Gram2
+    and Apply product of a chunk in one launch) from its summed CUDA-event
+    time (fused_ms over fused_n launches in `steps` timed steps): the chunked
+    matrices' algorithmic flops 5 (3 m^2 n + m^3) over that time against the
+    tensor peak, and per launch the measured DRAM traffic (launch_traffic,
+    or None) beside the algorithmic bytes of all its products (per
+    iteration: X read and A written by the Gram, A read and Z written by the
+    Gram2, Z and X read and X' written by the Apply, 2-byte elements)."""
+    from newton_schulz_nesterov_gb300 import flops
+    big = [(r, c) for r, c in shapes if min(r, c) > 128 or max(r, c) > 512]
+    achieved = flops.algorithmic_flops(big, ns_steps) * steps / (fused_ms / 1e3) / 1e12
+    launches_per_step = fused_n / steps
+    per_iter = sum(2 * (3 * min(r, c) * max(r, c) + 4 * min(r, c) ** 2) for r, c in big)
+    kname = ("ns_gemm_pair_kernel<Fused> (all Gram, Gram2 and Apply products of a chunk, 256x256 CTA-pair tiles)"
+             if pairs else "ns_gemm_kernel<Fused> (all products of a chunk, 128x256 tiles)")
+    return {"kernel": kname, "bound": "tensor",
+            "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": peak_src,
+            "traffic": launch_traffic,
+            "algorithmic_bytes": per_iter * ns_steps / launches_per_step,
+            "launches_per_step": launches_per_step,
+            "avg_launch_ms": fused_ms / fused_n}
 
 
 # ------------------------------------------------------------------ clocks
@@ -339,6 +390,7 @@ def run_ours(args, rank, world, local_rank):
     if args.tile_mode:
         dm.dmuon_set_tile_mode(h.h, args.tile_mode)
     dm.dmuon_set_balanced_dealing(h.h, args.dealing == "balanced")
+    dm.dmuon_set_fused_phases(h.h, {"auto": 2, "always": 1, "never": 0}[args.fused])
     for step in range(w.warm_steps):
         Gw = [workloads.grad(w, i, step, dev) for i in range(n)]
         h.step(Ws, Gw, Ms, lr=lr, mu=mu)
@@ -401,9 +453,16 @@ def run_ours(args, rank, world, local_rank):
     # Each phase launches once per chunk and iteration; achieved rates divide
     # the phase's algorithmic work over the timed steps by its summed time.
     apply_ms, apply_n = prof["apply"]
+    fused_ms, fused_n = prof["ns_fused"]
     pairs = "pairs" in dm.dmuon_plan_summary(h.h)
-    roofline = apply_roofline(shapes, args.steps, apply_ms, apply_n, peak, peak_src, pairs,
-                              apply_traffic(args.workload)) if apply_n else None
+    if fused_n:
+        roofline = fused_roofline(shapes, args.steps, fused_ms, fused_n, peak, peak_src, pairs,
+                                  fused_traffic(args.workload))
+    elif apply_n:
+        roofline = apply_roofline(shapes, args.steps, apply_ms, apply_n, peak, peak_src, pairs,
+                                  apply_traffic(args.workload))
+    else:
+        roofline = None
     phase = {k: {"ms_per_launch": (v[0] / v[1]) if v[1] else None, "launches": v[1],
                  "ms_per_step": v[0] / args.steps}
              for k, v in prof.items() if v[1]}
@@ -416,6 +475,12 @@ def run_ours(args, rank, world, local_rank):
         mom_ms_step = prof["momentum"][0] / args.steps
         phase["momentum"]["achieved_gbs"] = flops.elementwise_bytes(big) / (mom_ms_step / 1e3) / 1e9
         phase["momentum"]["frac_of_hbm"] = phase["momentum"]["achieved_gbs"] / hbm_peak
+
+    # ---- the same step with one launch per phase and iteration: where the
+    # fused kernel's time goes, phase by phase (CUDA events per launch)
+    split = None
+    if fused_n and not args.no_split:
+        split = phase_split(args, h, wp, gp, mp, shapes, stream, lr, mu)
 
     # ---- the rest of Muon.step: AdamW and clipping rooflines (HBM-bound)
     aux = None
@@ -454,6 +519,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches,
         "roofline": roofline,
         "phases": phase,
+        "phases_per_phase_launches": split,
         "clocks": clk,
         "e2e": e2e,
         "e2e_status": e2e_status,
@@ -465,6 +531,45 @@ def run_ours(args, rank, world, local_rank):
     h.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def phase_split(args, h, wp, gp, mp, shapes, stream, lr, mu):
+    """A few steps with the fused launch switched off (one launch per phase
+    and iteration, the same tiles and arithmetic): milliseconds per step of
+    each phase by CUDA events, and the whole step, beside the fused
+    headline.  The handle is left fused again."""
+    import torch
+    import newton_schulz_nesterov_gb300 as dm
+    from newton_schulz_nesterov_gb300 import flops
+    dm.dmuon_set_fused_phases(h.h, False)
+    try:
+        for _ in range(2):
+            dm.dmuon_step_ptrs(h.h, wp, gp, mp, shapes, lr, mu, 5, stream=stream)
+        dm.dmuon_profile_read(h.h)
+        dm.dmuon_profile_enable(h.h, True)
+        steps = 3
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            dm.dmuon_step_ptrs(h.h, wp, gp, mp, shapes, lr, mu, 5, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dm.dmuon_profile_enable(h.h, False)
+        prof = dm.dmuon_profile_read(h.h)
+    finally:
+        dm.dmuon_set_fused_phases(h.h, {"auto": 2, "always": 1, "never": 0}[args.fused])
+    big = [(r, c) for r, c in shapes if min(r, c) > 128 or max(r, c) > 512]
+    out = {"steps": steps, "ms_per_step": e0.elapsed_time(e1) / steps}
+    for k, v in prof.items():
+        if v[1]:
+            out[k] = {"ms_per_step": v[0] / steps, "launches": v[1]}
+    work = {"gram": 5 * sum(min(s_) ** 2 * max(s_) for s_ in big), "gram2": 5 * sum(min(s_) ** 3 for s_ in big),
+            "apply": flops.apply_flops(big)}
+    for k, fl in work.items():
+        if k in out and out[k]["ms_per_step"] > 0:
+            out[k]["algorithmic_tflops"] = fl / (out[k]["ms_per_step"] / 1e3) / 1e12
+    return out
 
 
 def run_gram(args, Ws, Gs, Ms, shapes, stream, world, direct_ms, device):

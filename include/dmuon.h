@@ -345,6 +345,24 @@ int dmuon_set_overlap(dmuon_handle_t h, int on);
  * depend on who computes it).  dmuon_plan_summary reports the balance. */
 int dmuon_set_balanced_dealing(dmuon_handle_t h, int on);
 
+/* Direct backend, calls from now on: whether every Gram, Gram2 and Apply
+ * product of every iteration of a chunk runs in ONE persistent launch instead
+ * of one launch per phase and iteration.  mode 0: never; 1: always; 2
+ * (default): for chunks whose three phases hold at most 8 work items per
+ * persistent CTA (or CTA pair), where launch fills and drains dominate.  In
+ * the fused launch each CTA (pair) runs, iteration by iteration and phase by
+ * phase, the same dealt work items as the per-phase launches; before loading
+ * a tile's operands it waits (bounded, like every wait of the kernels) until
+ * its matrix's counter of finished tiles shows that matrix's previous phase
+ * complete.  The result is bitwise the same either way.  Measured on GB300:
+ * faster for small lists (TinyMLP d=512: 0.42 against 0.49 ms per step),
+ * slower for large ones (Llama-3-8B set: 395 against 330 ms; its CTAs drift
+ * apart across phases and read 41 % more from DRAM), hence the automatic
+ * rule.  Needs every CTA of the launch resident at once (one per SM, as
+ * launched): work on other streams only delays it, and a wait that runs out
+ * reports DMUON_ERR_TIMEOUT.  DMUON_ERR_ARG for another mode. */
+int dmuon_set_fused_phases(dmuon_handle_t h, int mode);
+
 /* Small-matrix kernel for later plans (default on): every matrix whose
  * oriented shape has m = min(rows, cols) <= 128 and n = max(rows, cols) <= 512
  * (the TinyMLP projections of DMuon "Quick Start" at small widths; the
@@ -382,7 +400,9 @@ int64_t dmuon_launch_count(dmuon_handle_t h);
 #define DMUON_KIND_SMALL    8
 #define DMUON_KIND_GS_GRAM  9   /* Gram backend: R = kappa s^2 X X^T        */
 #define DMUON_KIND_GS_PROD  10  /* Gram backend: m x m window products     */
-#define DMUON_NUM_KINDS     11
+#define DMUON_KIND_NS_FUSED 11  /* direct backend: every product of every
+                                 * iteration of a chunk in one launch       */
+#define DMUON_NUM_KINDS     12
 int dmuon_profile_enable(dmuon_handle_t h, int on);
 int dmuon_profile_read(dmuon_handle_t h, double* ms, int64_t* count,
                        int n_kinds);

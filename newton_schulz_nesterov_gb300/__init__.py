@@ -35,7 +35,7 @@ STATUS = {
     -7: "DMUON_ERR_UNSUPPORTED",
 }
 KIND_NAMES = ("momentum", "finalize", "gram", "gram2", "apply", "update0", "adamw", "clip", "small",
-              "gs_gram", "gs_prod")
+              "gs_gram", "gs_prod", "ns_fused")
 
 
 class DmuonError(RuntimeError):
@@ -113,6 +113,8 @@ def load(path=None):
     L.dmuon_set_overlap.restype = i32
     L.dmuon_set_balanced_dealing.argtypes = [vp, i32]
     L.dmuon_set_balanced_dealing.restype = i32
+    L.dmuon_set_fused_phases.argtypes = [vp, i32]
+    L.dmuon_set_fused_phases.restype = i32
     L.dmuon_set_small_path.argtypes = [vp, i32]
     L.dmuon_set_small_path.restype = i32
     L.dmuon_set_chunk_elements.argtypes = [vp, i64]
@@ -436,6 +438,14 @@ def dmuon_set_chunk_elements(h, elems):
 def dmuon_set_balanced_dealing(h, on=True):  # default on in the library
     """Longest-first dealing of work items to the least-loaded CTA (pair) for later plans."""
     _check(load().dmuon_set_balanced_dealing(h, 1 if on else 0), "dmuon_set_balanced_dealing")
+
+
+def dmuon_set_fused_phases(h, mode=2):  # default 2 (automatic) in the library
+    """Direct backend: every product of every iteration of a chunk in one
+    persistent launch -- 0 never, 1 always (True), 2 for chunks of few work
+    items (the default); False selects 0."""
+    m = 1 if mode is True else (0 if mode is False else int(mode))
+    _check(load().dmuon_set_fused_phases(h, m), "dmuon_set_fused_phases")
 
 
 def dmuon_set_small_path(h, on=True):  # default on in the library

@@ -47,7 +47,9 @@ struct MatDesc {
   float scale;             // update scale of this matrix
   float kappa;             // scale of A: largest power of two <= min(m, 1024)
   float beta;              // power of two nearest sqrt(n) (times 1/nu per call: bvec)
-  float pad_;
+  int32_t sym_items;       // work items of this matrix in each symmetric phase (Gram, Gram2)
+  int32_t apply_items;     // work items of this matrix in each Apply phase
+  int32_t pad_;
 };
 
 // Power-of-two scales of a matrix's fp16 buffers (host and device).
@@ -102,7 +104,7 @@ constexpr int kPairStageBytes = 2 * kPairHalfBytes;      // 32 KB per CTA
 constexpr int kPairSmem =
     1024 /*align slack*/ + kPairStages * kPairStageBytes + 4 * kEpiWords * 4 + 256;
 
-enum Phase : int { kPhaseGram = 0, kPhaseGram2 = 1, kPhaseApply = 2 };
+enum Phase : int { kPhaseGram = 0, kPhaseGram2 = 1, kPhaseApply = 2, kPhaseFused = 3 };
 enum FinalMode : int { kWriteX = 0, kUpdateW = 1, kWriteO = 2 };
 
 // Tensor maps per matrix: X[0], X[1], A, B (box 64x64, 128B swizzle).
@@ -125,6 +127,21 @@ struct GemmArgs {
   const float* bvec;       // per-matrix beta': X[k] (k >= 1) holds beta' X
   int* err;                // device error word (bit 0: wait timeout)
   unsigned long long timeout_ns;  // wait without progress before giving up (0 = 4 s)
+  // Fused launches (kPhaseFused): every stage s = 3k + p (iteration k, phase
+  // p) of every matrix in one launch.  Each processor runs, for k = 0 ..
+  // n_iters-1 and p = 0, 1, 2, its share of phase p's dealt list (fitems[p],
+  // fstarts[p] over fprocs[p] processors; the lists of the per-phase
+  // launches); a tile of stage s waits until its matrix's counter shows every
+  // tile of the stages before s done (each epilogue warp adds 1 per finished
+  // tile).  coef[k] is iteration k's (a, b, c); the last iteration's Apply
+  // uses final_mode, earlier ones write X.
+  const int4* fitems[3];
+  const int* fstarts[3];
+  int fn_items[3];
+  int fprocs[3];
+  int n_iters;
+  int* counters;           // per matrix, zero at launch
+  float coef[64][3];
 };
 
 // Items of one persistent processor (a CTA, or a CTA pair): its own run

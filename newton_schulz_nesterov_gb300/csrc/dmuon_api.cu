@@ -101,6 +101,7 @@ struct Chunk {
   float* d_bvec = nullptr;        // per matrix: beta', the scale of the iterate after the first product
   float* d_pscale = nullptr;      // per matrix: the prescale p of X[0] (kept across steps)
   int* d_redo = nullptr;          // per matrix: X[0] to be rewritten with a new p
+  int* d_counters = nullptr;      // per matrix: finished tiles of a fused launch (zeroed before it)
   int4* d_items[3] = {nullptr, nullptr, nullptr};
   int* d_starts[3] = {nullptr, nullptr, nullptr};
   GramDesc* d_gd = nullptr;       // gram plans: per-matrix Gram-space buffers
@@ -151,6 +152,8 @@ struct dmuon_ctx {
   // a side stream, two alternating chunk workspaces and fork/join events.
   bool overlap = false;                     // requested (off: measured neutral at the power cap)
   bool balanced = true;                     // requested: work items dealt longest-first to the least loaded
+  int fused = 2;                            // direct backend, one launch per chunk for all products:
+                                            // 0 never, 1 always, 2 for chunks of few work items
   bool plan_balanced = true;                // in the current plan
   bool plan_overlap = false;                // in the current plan (needs >= 2 chunks)
   size_t ws_chunk = 0;                      // bytes of one chunk workspace
@@ -172,6 +175,15 @@ namespace {
 // a time, instead of the whole list, measured ~6 % faster on the Llama-3-8B
 // set and bounds the workspace by the largest chunk.
 constexpr int64_t kDefaultChunkElems = int64_t(1) << 29;
+
+// Automatic fused launch (dmuon_set_fused_phases mode 2): chunks whose three
+// phases hold at most this many work items per persistent processor, where
+// launch fills and drains dominate.  Measured on GB300: TinyMLP d=512 (528
+// items over 152 CTAs) 0.42 ms per step fused against 0.49 ms per phase; the
+// Llama-3-8B set (thousands of items per chunk) 395 ms fused against 330 ms,
+// the fused kernel's processors drifting apart across phases and reading 41 %
+// more from DRAM.
+constexpr int64_t kFuseItemsPerProc = 8;
 
 int cuda_err(cudaError_t e) { return e == cudaSuccess ? DMUON_OK : (e == cudaErrorMemoryAllocation ? DMUON_ERR_OOM : DMUON_ERR_CUDA); }
 
@@ -291,7 +303,7 @@ std::vector<std::pair<int, int>> split_chunks(const dmuon_shape_t* shapes, int n
 size_t chunk_small_bytes(const Layout& L, int n) {
   const bool gram = !L.goff.empty();
   return rup(sizeof(MatDesc) * n, 256) + rup(sizeof(CUtensorMap) * kMapsPerMat * n, 256) +
-         rup(8 * (n + 1), 256) + 2 * rup(4 * L.tile_prefix[n], 256) + 4 * rup(4 * n, 256) +
+         rup(8 * (n + 1), 256) + 2 * rup(4 * L.tile_prefix[n], 256) + 5 * rup(4 * n, 256) +
          rup(16 * L.items[0].size(), 256) + rup(16 * L.items[1].size(), 256) + rup(16 * L.items[2].size(), 256) +
          rup(4 * (L.items[0].size() + 1), 256) + rup(4 * (L.items[1].size() + 1), 256) +
          rup(4 * (L.items[2].size() + 1), 256) +
@@ -392,6 +404,7 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
     ch.d_bvec = (float*)carve(4 * cn);
     ch.d_pscale = (float*)carve(4 * cn);
     ch.d_redo = (int*)carve(4 * cn);
+    ch.d_counters = (int*)carve(4 * cn);
     for (int q = 0; q < 3; ++q) ch.d_items[q] = (int4*)carve(16 * L.items[q].size());
     for (int q = 0; q < 3; ++q) ch.d_starts[q] = (int*)carve(4 * (L.items[q].size() + 1));
     if (gram) {
@@ -638,6 +651,51 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
     const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
     LaunchGuard g(h, stream, DMUON_KIND_UPDATE0);
     if ((e = launch_update0(a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "update0 launch", e);
+    return DMUON_OK;
+  }
+  int64_t chunk_items = 0;
+  for (int p = 0; p < 3; ++p) chunk_items += (int64_t)L.items[p].size();
+  const int avail = h->plan_pair ? h->max_clusters : h->num_sms;
+  const bool fuse = h->fused == 1 || (h->fused == 2 && chunk_items <= kFuseItemsPerProc * (int64_t)avail);
+  if (fuse && ns_steps <= 64) {
+    // One launch for every product of every iteration: each tile waits on its
+    // matrix's counter of finished tiles (zeroed here) for the stage before.
+    GemmArgs a{};
+    a.mats = ch.d_mats;
+    a.ptrs = dptrs;
+    a.tmaps = ch.d_maps;
+    int grid = 0;
+    for (int p = 0; p < 3; ++p) {
+      a.fitems[p] = ch.d_items[p];
+      a.fstarts[p] = L.starts[p].empty() ? nullptr : ch.d_starts[p];
+      a.fn_items[p] = (int)L.items[p].size();
+      a.fprocs[p] = L.procs[p];
+      grid = std::max(grid, L.procs[p]);
+    }
+    a.n_iters = ns_steps;
+    for (int k = 0; k < ns_steps; ++k) {
+      const float* row = coeffs ? coeffs + 3 * k : kYouCoefficients[std::min(k, 4)];
+      for (int q = 0; q < 3; ++q) a.coef[k][q] = row[q];
+    }
+    a.counters = ch.d_counters;
+    a.fold = 1;
+    a.final_mode = ns_only ? kWriteO : kUpdateW;
+    a.lr = lr;
+    a.decay = decay;
+    a.svec = ch.d_svec;
+    a.bvec = ch.d_bvec;
+    a.err = h->d_err;
+    a.timeout_ns = h->wait_timeout_ns;
+    if (grid <= 0) return DMUON_OK;
+    if ((e = cudaMemsetAsync(ch.d_counters, 0, 4 * (size_t)n, stream)) != cudaSuccess)
+      return fail(h, cuda_err(e), "counter reset", e);
+    LaunchGuard g(h, stream, DMUON_KIND_NS_FUSED);
+    if (h->plan_pair) {
+      if ((e = launch_gemm_pair(kPhaseFused, a, grid, stream)) != cudaSuccess)
+        return fail(h, cuda_err(e), "ns_gemm_pair fused launch", e);
+    } else if ((e = launch_gemm(kPhaseFused, a, grid, stream)) != cudaSuccess) {
+      return fail(h, cuda_err(e), "ns_gemm fused launch", e);
+    }
     return DMUON_OK;
   }
   static const int kKinds[3] = {DMUON_KIND_GRAM, DMUON_KIND_GRAM2, DMUON_KIND_APPLY};
@@ -1409,6 +1467,12 @@ int dmuon_set_overlap(dmuon_handle_t h, int on) {
 int dmuon_set_balanced_dealing(dmuon_handle_t h, int on) {
   if (!h) return DMUON_ERR_ARG;
   h->balanced = on != 0;
+  return DMUON_OK;
+}
+
+int dmuon_set_fused_phases(dmuon_handle_t h, int mode) {
+  if (!h || mode < 0 || mode > 2) return DMUON_ERR_ARG;
+  h->fused = mode;
   return DMUON_OK;
 }
 

@@ -45,6 +45,7 @@ struct Smem {
   uint64_t* bars;      // full[kStages], empty[kStages], tfull[2], tempty[2], drain
   uint32_t* tmem_slot;
   volatile int* abort_flag;
+  uint32_t* tile_done;  // fused launches: epilogue warps done per accumulator slot
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
@@ -56,6 +57,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes + 4 * kEpiWords * 4);
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + 2 * kStages + 5);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+  s.tile_done = s.tmem_slot + 2;
   return s;
 }
 
@@ -147,9 +149,135 @@ __device__ __forceinline__ void mirror_store32(__half* base, int64_t ld, int64_t
   store_row32(base + dr * ld, rbase, n_lim, dr < n_lim, t);
 }
 
+// Per-item view of a launch: the phase, the iteration and the K blocks of an
+// item, and that iteration's parameters.
+struct ItemInfo {
+  int ph, it, kbn;
+};
+
+// The items of one persistent processor in the order it runs them: its run
+// of the launch's list, or (fused launches) for each iteration k and phase p
+// its run of phase p's list.  Every role of the processor (producer, MMA
+// issuer, epilogue warps) walks the same sequence.
+template <int PHASE>
+struct ItemCursor {
+  const GemmArgs& a;
+  int proc, nproc, k, p, w, w1, step;
+  __device__ __forceinline__ ItemCursor(const GemmArgs& a_, int proc_, int nproc_)
+      : a(a_), proc(proc_), nproc(nproc_), k(0), p(-1), w(0), w1(0), step(1) {
+    if constexpr (PHASE != kPhaseFused) {
+      const WorkRange r = work_range(a.starts, proc, nproc, a.n_items);
+      w = r.w0;
+      w1 = r.w1;
+      step = r.step;
+    }
+  }
+  __device__ __forceinline__ bool next(int4& item, ItemInfo& inf) {
+    if constexpr (PHASE != kPhaseFused) {
+      if (w >= w1) return false;
+      item = a.items[w];
+      w += step;
+      inf = ItemInfo{PHASE, 0, item.w};
+      return true;
+    } else {
+      while (w >= w1) {
+        if (++p == 3) {
+          p = 0;
+          if (++k >= a.n_iters) return false;
+        }
+        w = w1 = 0;
+        if (proc < a.fprocs[p]) {
+          const WorkRange r = work_range(a.fstarts[p], proc, a.fprocs[p], a.fn_items[p]);
+          w = r.w0;
+          w1 = r.w1;
+          step = r.step;
+        }
+      }
+      item = a.fitems[p][w];
+      w += step;
+      inf = ItemInfo{p, k, item.w};
+      return true;
+    }
+  }
+};
+
+struct StageParams {
+  int src, first;
+  float ca, cb, cc;
+};
+template <int PHASE>
+__device__ __forceinline__ StageParams stage_params(const GemmArgs& a, int it) {
+  if constexpr (PHASE == kPhaseFused)
+    return StageParams{it & 1, it == 0 ? 1 : 0, a.coef[it][0], a.coef[it][1], a.coef[it][2]};
+  else
+    return StageParams{a.src, a.first, a.ca, a.cb, a.cc};
+}
+
+// Fused launches: a tile of stage s = 3k + p waits until its matrix's counter
+// shows every tile of the stages before it done (`warps` increments per
+// tile); the counter never runs ahead of a stage whose tiles are still
+// waiting, so reaching the sum over stages < s means all of them finished.
+__device__ __forceinline__ uint32_t stage_need(const MatDesc& d, int ph, int it, int warps) {
+  return (uint32_t)warps *
+         (uint32_t)(it * (2 * d.sym_items + d.apply_items) + (ph >= 1 ? d.sym_items : 0) + (ph >= 2 ? d.sym_items : 0));
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait (same limit and abort protocol as the mbarrier waits) until
+// *cnt >= need, then a proxy fence so that the TMA loads issued next see the
+// other CTAs' generic stores the counter vouches for.
+__device__ __noinline__ bool wait_counter(const int* cnt, int need, volatile int* abort_flag, int* err,
+                                          uint64_t limit_ns, int* seen) {
+  if ((*seen = ld_acquire(cnt)) < need) {
+    const uint64_t t0 = ptx::globaltimer();
+    while ((*seen = ld_acquire(cnt)) < need) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer() - t0 > limit_ns) {
+        *abort_flag = 1;
+        atomicOr(err, 1);
+        return false;
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+// An epilogue warp has stored its part of a tile.  The four warps of the CTA
+// count themselves on a shared-memory word of the tile's accumulator slot
+// (acquire-release at CTA scope, nobody blocks: a warp that gave up on a
+// wait never holds the others); the fourth resets the word and, after a
+// GPU-scope release fence that covers every store of the tile, adds 1 to the
+// matrix's counter.  Called before the warp releases the accumulator, so the
+// slot's next tile cannot be counted before the reset.
+__device__ __forceinline__ void signal_tile(int* cnt, uint32_t done_word, int lane) {
+  __syncwarp();
+  if (lane == 0) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(done_word) : "memory");
+    if (old == 3) {
+      asm volatile("st.relaxed.cta.shared::cta.u32 [%0], 0;" ::"r"(done_word) : "memory");
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      atomicAdd(cnt, 1);
+    }
+  }
+  __syncwarp();
+}
+
+// Producer side: a counter value seen before for the same matrix (counters
+// only grow) spares the acquire poll.
+struct CounterCache {
+  int mat = -1, val = 0;
+};
+
 template <int PHASE, int MODE>
-__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item, uint32_t tacc,
-                                              int quad, int lane, uint32_t* scratch) {
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const StageParams& sp, const int4 item,
+                                              uint32_t tacc, int quad, int lane, uint32_t* scratch) {
   const MatDesc& d = a.mats[item.x];
   const int64_t m = d.m, n = d.n;
   const int64_t row0 = (int64_t)item.y * kBM;
@@ -162,14 +290,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
   // True scale of the stored iterate: X = xs * X[src] (s/p of the first
   // step's X[0] = p U, else 1/beta' for X stored as beta' X).
   const float bp = a.bvec[item.x];
-  const float xs = a.first ? a.svec[item.x] : 1.f / bp;
+  const float xs = sp.first ? a.svec[item.x] : 1.f / bp;
   if constexpr (PHASE == kPhaseGram || PHASE == kPhaseGram2) {
     const bool mirror = (item.y >> 1) < item.z;
     // Gram: A = kappa xs^2 X[src] X[src]^T.  Gram2 with A = kappa X X^T:
     // b A_true + c A_true^2 = (b/kappa) A + (c/kappa^2) A A.
     const float ik = 1.f / d.kappa;
     const float alpha = d.kappa * xs * xs;
-    const float gcc = a.cc * ik * ik, gcb = a.cb * ik;
+    const float gcc = sp.cc * ik * ik, gcb = sp.cb * ik;
     __half* dst = (PHASE == kPhaseGram) ? d.A : d.B;
     const int64_t ld = d.lda;
 #pragma unroll 1
@@ -190,7 +318,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
         if (a.fold) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (r == c + j) f[j] += a.ca;
+            if (r == c + j) f[j] += sp.ca;
         }
       }
       uint32_t w[16];
@@ -202,8 +330,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
   } else {
     // X' = beta' xs (Z X[src]) stored; the final O = xs (Z X[src]) in fp32.
     const float alpha = MODE == kWriteX ? xs * bp : xs;
-    const __half* xsrc = d.X[a.src];
-    __half* xd = d.X[a.src ^ 1];
+    const __half* xsrc = d.X[sp.src];
+    __half* xd = d.X[sp.src ^ 1];
     const int64_t ldx = d.ldx;
     const MatPtrs& p = a.ptrs[item.x];
     const float coef = a.lr * d.scale;
@@ -221,7 +349,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
         float xv[32];
         load_row32(xsrc + r * ldx, c, n, row_ok, xv);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = alpha * fmaf(a.ca, xv[j], __uint_as_float(v[j]));
+        for (int j = 0; j < 32; ++j) o[j] = alpha * fmaf(sp.ca, xv[j], __uint_as_float(v[j]));
       }
       if constexpr (MODE == kWriteX) {
         uint32_t w[16];
@@ -278,6 +406,34 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const int4 item
   }
 }
 
+// The epilogue of one item: the launch's own phase, or (fused launches) the
+// item's phase and iteration, the last iteration's Apply in the launch's
+// final mode.
+template <int PHASE, int MODE>
+__device__ __forceinline__ void epilogue_item(const GemmArgs& a, const ItemInfo& inf, const int4 item, uint32_t tacc,
+                                              int quad, int lane, uint32_t* scratch) {
+  const StageParams sp = stage_params<PHASE>(a, inf.it);
+  if constexpr (PHASE != kPhaseFused) {
+    epilogue_tile<PHASE, MODE>(a, sp, item, tacc, quad, lane, scratch);
+  } else {
+    if (inf.ph == kPhaseGram) {
+      epilogue_tile<kPhaseGram, kWriteX>(a, sp, item, tacc, quad, lane, scratch);
+    } else if (inf.ph == kPhaseGram2) {
+      // This epilogue reads A tiles that other CTAs stored: an acquire of the
+      // matrix's counter (already past this stage's need, which the producer
+      // waited for) orders those stores before this thread's loads.
+      (void)ld_acquire(a.counters + item.x);
+      epilogue_tile<kPhaseGram2, kWriteX>(a, sp, item, tacc, quad, lane, scratch);
+    }
+    else if (inf.it < a.n_iters - 1)
+      epilogue_tile<kPhaseApply, kWriteX>(a, sp, item, tacc, quad, lane, scratch);
+    else if (a.final_mode == kUpdateW)
+      epilogue_tile<kPhaseApply, kUpdateW>(a, sp, item, tacc, quad, lane, scratch);
+    else
+      epilogue_tile<kPhaseApply, kWriteO>(a, sp, item, tacc, quad, lane, scratch);
+  }
+}
+
 template <int PHASE, int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -285,7 +441,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = a.timeout_ns ? a.timeout_ns : kTimeoutNs;
-  const WorkRange wr = work_range(a.starts, blockIdx.x, gridDim.x, a.n_items);
 
   uint64_t* full = sm.bars;
   uint64_t* empty = sm.bars + kStages;
@@ -304,6 +459,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     }
     ptx::mbar_init(ptx::smem_addr(drain), 1);
     *sm.abort_flag = 0;
+    sm.tile_done[0] = sm.tile_done[1] = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -320,21 +476,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       // ---------------------------------------------------------- producer
       uint32_t it = 0;
       bool ok = true;
-      for (int w = wr.w0; ok && w < wr.w1; w += wr.step) {
-        const int4 item = a.items[w];
+      ItemCursor<PHASE> cur(a, (int)blockIdx.x, (int)gridDim.x);
+      CounterCache cc;
+      int4 item;
+      ItemInfo inf;
+      while (ok && cur.next(item, inf)) {
+        const int src = PHASE == kPhaseFused ? (inf.it & 1) : a.src;
+        if (PHASE == kPhaseFused) {
+          const int need = (int)stage_need(a.mats[item.x], inf.ph, inf.it, 1);
+          if (need > 0 && !(cc.mat == item.x && cc.val >= need)) {
+            if (!wait_counter(a.counters + item.x, need, sm.abort_flag, a.err, tmo, &cc.val)) { ok = false; break; }
+            cc.mat = item.x;
+          }
+        }
         const CUtensorMap* maps = a.tmaps + (size_t)item.x * kMapsPerMat;
         const CUtensorMap* mapA;
         const CUtensorMap* mapB;
-        if (PHASE == kPhaseGram) {
-          mapA = maps + a.src; mapB = maps + a.src;
-        } else if (PHASE == kPhaseGram2) {
+        if (inf.ph == kPhaseGram) {
+          mapA = maps + src; mapB = maps + src;
+        } else if (inf.ph == kPhaseGram2) {
           mapA = maps + 2; mapB = maps + 2;
         } else {
-          mapA = maps + 3; mapB = maps + a.src;
+          mapA = maps + 3; mapB = maps + src;
         }
         const int row0 = item.y * kBM;
         const int col0 = item.z * kBN;
-        for (int kb = 0; kb < item.w; ++kb, ++it) {
+        for (int kb = 0; kb < inf.kbn; ++kb, ++it) {
           const uint32_t s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           if (!wait_bar(ptx::smem_addr(empty + s), ph ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
@@ -347,7 +514,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           ptx::tma_load_2d(sa + kBoxBytes, mapA, k0, row0 + kBox, fb);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            if (PHASE == kPhaseApply)
+            if (inf.ph == kPhaseApply)
               ptx::tma_load_2d(sb + q * kBoxBytes, mapB, col0 + q * kBox, k0, fb);
             else
               ptx::tma_load_2d(sb + q * kBoxBytes, mapB, k0, col0 + q * kBox, fb);
@@ -366,17 +533,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_f16(kBM, kBN, PHASE == kPhaseApply ? 1 : 0);
+      constexpr uint32_t idesc_sym = ptx::idesc_f16(kBM, kBN, 0), idesc_app = ptx::idesc_f16(kBM, kBN, 1);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
-      for (int w = wr.w0; ok && w < wr.w1; w += wr.step, ++tc) {
-        const int4 item = a.items[w];
+      ItemCursor<PHASE> cur(a, (int)blockIdx.x, (int)gridDim.x);
+      int4 item;
+      ItemInfo inf;
+      for (; ok && cur.next(item, inf); ++tc) {
         const uint32_t acc = tc & 1u;
         if (!wait_bar(ptx::smem_addr(tempty + acc), ((tc >> 1) & 1u) ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t dt = tmem_base + acc * kBN;
-        for (int kb = 0; kb < item.w; ++kb, ++it) {
+        const bool mn = inf.ph == kPhaseApply;  // X as the MN-major B operand
+        const uint32_t idesc = mn ? idesc_app : idesc_sym;
+        for (int kb = 0; kb < inf.kbn; ++kb, ++it) {
           const uint32_t s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           if (!wait_bar(ptx::smem_addr(full + s), ph, sm.abort_flag, a.err, tmo)) { ok = false; break; }
@@ -386,8 +557,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = ptx::desc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = (PHASE == kPhaseApply) ? ptx::desc_sw128(sb + kk * 2048, 8192, 1024)
-                                                       : ptx::desc_sw128(sb + kk * 32, 16, 1024);
+            const uint64_t bd = mn ? ptx::desc_sw128(sb + kk * 2048, 8192, 1024)
+                                   : ptx::desc_sw128(sb + kk * 32, 16, 1024);
             ptx::mma_f16(dt, ad, bd, idesc, (kb | kk) != 0);
           }
           issued = true;
@@ -406,12 +577,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 for this warp
     uint32_t* scratch = sm.scratch + (warp - 2) * kEpiWords;
     uint32_t tc = 0;
-    for (int w = wr.w0; w < wr.w1; w += wr.step, ++tc) {
-      const int4 item = a.items[w];
+    ItemCursor<PHASE> cur(a, (int)blockIdx.x, (int)gridDim.x);
+    int4 item;
+    ItemInfo inf;
+    for (; cur.next(item, inf); ++tc) {
       const uint32_t acc = tc & 1u;
       if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err, tmo)) break;
       ptx::tc_fence_after();
-      epilogue_tile<PHASE, MODE>(a, item, tmem_base + acc * kBN, quad, lane, scratch);
+      epilogue_item<PHASE, MODE>(a, inf, item, tmem_base + acc * kBN, quad, lane, scratch);
+      if (PHASE == kPhaseFused) signal_tile(a.counters + item.x, ptx::smem_addr(sm.tile_done + acc), lane);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(tempty + acc));
@@ -443,6 +617,7 @@ struct PairSmem {
   uint64_t* bars;      // full[6], empty[6], tfull[2], tempty[2], drain
   uint32_t* tmem_slot;
   volatile int* abort_flag;
+  uint32_t* tile_done;  // fused launches: epilogue warps done per accumulator slot
 };
 
 __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
@@ -455,6 +630,7 @@ __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
   s.bars = reinterpret_cast<uint64_t*>(after + 4 * kEpiWords * 4);
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + 2 * kPairStages + 5);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+  s.tile_done = s.tmem_slot + 2;
   return s;
 }
 
@@ -469,7 +645,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
-  const WorkRange wr = work_range(a.starts, pair, npairs, a.n_items);
 
   uint64_t* full = sm.bars;
   uint64_t* empty = sm.bars + kPairStages;
@@ -488,6 +663,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
     }
     ptx::mbar_init(ptx::smem_addr(drain), 1);
     *sm.abort_flag = 0;
+    sm.tile_done[0] = sm.tile_done[1] = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {  // one warp of each rank allocates the pair's TMEM together
@@ -505,21 +681,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
       // ---------------------------------------------------------- producer
       uint32_t it = 0;
       bool ok = true;
-      for (int w = wr.w0; ok && w < wr.w1; w += wr.step) {
-        const int4 item = a.items[w];
+      ItemCursor<PHASE> cur(a, pair, npairs);
+      CounterCache cc;
+      int4 item;
+      ItemInfo inf;
+      while (ok && cur.next(item, inf)) {
+        const int src = PHASE == kPhaseFused ? (inf.it & 1) : a.src;
+        if (PHASE == kPhaseFused) {  // each rank loads its own halves: both wait
+          const int need = (int)stage_need(a.mats[item.x], inf.ph, inf.it, 2);
+          if (need > 0 && !(cc.mat == item.x && cc.val >= need)) {
+            if (!wait_counter(a.counters + item.x, need, sm.abort_flag, a.err, tmo, &cc.val)) { ok = false; break; }
+            cc.mat = item.x;
+          }
+        }
         const CUtensorMap* maps = a.tmaps + (size_t)item.x * kMapsPerMat;
         const CUtensorMap* mapA;
         const CUtensorMap* mapB;
-        if (PHASE == kPhaseGram) {
-          mapA = maps + a.src; mapB = maps + a.src;
-        } else if (PHASE == kPhaseGram2) {
+        if (inf.ph == kPhaseGram) {
+          mapA = maps + src; mapB = maps + src;
+        } else if (inf.ph == kPhaseGram2) {
           mapA = maps + 2; mapB = maps + 2;
         } else {
-          mapA = maps + 3; mapB = maps + a.src;
+          mapA = maps + 3; mapB = maps + src;
         }
         const int rowA = item.y * 256 + (int)rank * 128;
         const int rowB = item.z * 256 + (int)rank * 128;
-        for (int kb = 0; kb < item.w; ++kb, ++it) {
+        for (int kb = 0; kb < inf.kbn; ++kb, ++it) {
           const uint32_t s = it % kPairStages;
           const uint32_t ph = (it / kPairStages) & 1u;
           if (!wait_bar(ptx::smem_addr(empty + s), ph ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
@@ -531,7 +718,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
           const int k0 = kb * kBK;
           ptx::tma_load_2d_pair(sa, mapA, k0, rowA, fb);
           ptx::tma_load_2d_pair(sa + kBoxBytes, mapA, k0, rowA + kBox, fb);
-          if (PHASE == kPhaseApply) {
+          if (inf.ph == kPhaseApply) {
             ptx::tma_load_2d_pair(sb, mapB, rowB, k0, fb);
             ptx::tma_load_2d_pair(sb + kBoxBytes, mapB, rowB + kBox, k0, fb);
           } else {
@@ -552,17 +739,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_f16(256, kBN, PHASE == kPhaseApply ? 1 : 0);
+      constexpr uint32_t idesc_sym = ptx::idesc_f16(256, kBN, 0), idesc_app = ptx::idesc_f16(256, kBN, 1);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
-      for (int w = wr.w0; ok && w < wr.w1; w += wr.step, ++tc) {
-        const int4 item = a.items[w];
+      ItemCursor<PHASE> cur(a, pair, npairs);
+      int4 item;
+      ItemInfo inf;
+      for (; ok && cur.next(item, inf); ++tc) {
         const uint32_t acc = tc & 1u;
         if (!wait_bar(ptx::smem_addr(tempty + acc), ((tc >> 1) & 1u) ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t dt = tmem_base + acc * kBN;
-        for (int kb = 0; kb < item.w; ++kb, ++it) {
+        const bool mn = inf.ph == kPhaseApply;  // X as the MN-major B operand
+        const uint32_t idesc = mn ? idesc_app : idesc_sym;
+        for (int kb = 0; kb < inf.kbn; ++kb, ++it) {
           const uint32_t s = it % kPairStages;
           const uint32_t ph = (it / kPairStages) & 1u;
           if (!wait_bar(ptx::smem_addr(full + s), ph, sm.abort_flag, a.err, tmo)) { ok = false; break; }
@@ -572,8 +763,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = ptx::desc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = (PHASE == kPhaseApply) ? ptx::desc_sw128(sb + kk * 2048, 8192, 1024)
-                                                       : ptx::desc_sw128(sb + kk * 32, 16, 1024);
+            const uint64_t bd = mn ? ptx::desc_sw128(sb + kk * 2048, 8192, 1024)
+                                   : ptx::desc_sw128(sb + kk * 32, 16, 1024);
             ptx::mma_f16_pair(dt, ad, bd, idesc, (kb | kk) != 0);
           }
           issued = true;
@@ -592,13 +783,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
     const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 for this warp
     uint32_t* scratch = sm.scratch + (warp - 2) * kEpiWords;
     uint32_t tc = 0;
-    for (int w = wr.w0; w < wr.w1; w += wr.step, ++tc) {
-      int4 item = a.items[w];
+    ItemCursor<PHASE> cur(a, pair, npairs);
+    int4 item;
+    ItemInfo inf;
+    for (; cur.next(item, inf); ++tc) {
       const uint32_t acc = tc & 1u;
       if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err, tmo)) break;
       ptx::tc_fence_after();
       item.y = item.y * 2 + (int)rank;  // this rank's 128-row tile
-      epilogue_tile<PHASE, MODE>(a, item, tmem_base + acc * kBN, quad, lane, scratch);
+      epilogue_item<PHASE, MODE>(a, inf, item, tmem_base + acc * kBN, quad, lane, scratch);
+      if (PHASE == kPhaseFused) signal_tile(a.counters + item.x, ptx::smem_addr(sm.tile_done + acc), lane);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_addr(tempty + acc), 0));
@@ -628,13 +822,16 @@ cudaError_t gemm_configure() {
   if ((e = configure_one<kPhaseGram2, kWriteX>()) != cudaSuccess) return e;
   if ((e = configure_one<kPhaseApply, kWriteX>()) != cudaSuccess) return e;
   if ((e = configure_one<kPhaseApply, kUpdateW>()) != cudaSuccess) return e;
+  if ((e = configure_one<kPhaseFused, kWriteX>()) != cudaSuccess) return e;
   return configure_one<kPhaseApply, kWriteO>();
 }
 
 // Apply launches pick the kernel variant of their final mode, so each
 // variant carries only the epilogue it runs.
 cudaError_t launch_gemm(int phase, const GemmArgs& a, int grid, cudaStream_t s) {
-  if (phase == kPhaseGram) {
+  if (phase == kPhaseFused) {
+    ns_gemm_kernel<kPhaseFused, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+  } else if (phase == kPhaseGram) {
     ns_gemm_kernel<kPhaseGram, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
   } else if (phase == kPhaseGram2) {
     ns_gemm_kernel<kPhaseGram2, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
@@ -673,6 +870,7 @@ cudaError_t gemm_pair_configure(int* max_clusters) {
   if ((e = configure_pair_one<kPhaseGram2, kWriteX>(nullptr)) != cudaSuccess) return e;
   if ((e = configure_pair_one<kPhaseApply, kWriteX>(nullptr)) != cudaSuccess) return e;
   if ((e = configure_pair_one<kPhaseApply, kUpdateW>(nullptr)) != cudaSuccess) return e;
+  if ((e = configure_pair_one<kPhaseFused, kWriteX>(nullptr)) != cudaSuccess) return e;
   return configure_pair_one<kPhaseApply, kWriteO>(nullptr);
 }
 
@@ -694,6 +892,7 @@ cudaError_t launch_pair_one(const GemmArgs& a, int clusters, cudaStream_t s) {
 }
 
 cudaError_t launch_gemm_pair(int phase, const GemmArgs& a, int clusters, cudaStream_t s) {
+  if (phase == kPhaseFused) return launch_pair_one<kPhaseFused, kWriteX>(a, clusters, s);
   if (phase == kPhaseGram) return launch_pair_one<kPhaseGram, kWriteX>(a, clusters, s);
   if (phase == kPhaseGram2) return launch_pair_one<kPhaseGram2, kWriteX>(a, clusters, s);
   if (a.final_mode == kUpdateW) return launch_pair_one<kPhaseApply, kUpdateW>(a, clusters, s);

@@ -114,7 +114,8 @@ inline void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair
   // take one 128-row half of it.
   for (int p = 0; p < 3; ++p) L.items[p].clear();
   for (int i = 0; i < n; ++i) {
-    const MatDesc& d = L.mats[i];
+    MatDesc& d = L.mats[i];
+    const size_t sym0 = L.items[kPhaseGram].size(), app0 = L.items[kPhaseApply].size();
     const int64_t T = cdiv(d.m, 256);
     const int kg = (int)cdiv(d.n, kBK), km = (int)cdiv(d.m, kBK);
     if (pair) {
@@ -126,6 +127,8 @@ inline void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair
       for (int64_t tj = 0; tj < cdiv(d.n, kBN); ++tj)
         for (int64_t I = 0; I < T; ++I)
           L.items[kPhaseApply].push_back(make_int4(i, (int)I, (int)tj, km));
+      d.sym_items = (int32_t)(L.items[kPhaseGram].size() - sym0);
+      d.apply_items = (int32_t)(L.items[kPhaseApply].size() - app0);
       continue;
     }
     for (int64_t I = 0; I < T; ++I)
@@ -141,6 +144,8 @@ inline void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair
     for (int64_t tj = 0; tj < cdiv(d.n, kBN); ++tj)
       for (int64_t ti = 0; ti < cdiv(d.m, kBM); ++ti)
         L.items[kPhaseApply].push_back(make_int4(i, (int)ti, (int)tj, km));
+    d.sym_items = (int32_t)(L.items[kPhaseGram].size() - sym0);
+    d.apply_items = (int32_t)(L.items[kPhaseApply].size() - app0);
   }
   for (int p = 0; p < 3; ++p) deal_items(L.items[p], procs, balanced, L.starts[p], L.procs[p]);
 }

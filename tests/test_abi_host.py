@@ -409,6 +409,23 @@ def test_gram_range_check_is_sound(lib):
     assert checked >= 6   # the perturbed tables that let singular values run past ~1.3 are refused
 
 
+def test_bench_fused_roofline_arithmetic():
+    """The fused kernel's roofline object from made-up timings: all of the
+    chunked matrices' algorithmic flops over the kernel's time, and per
+    launch the algorithmic bytes of every product of a chunk."""
+    import bench
+    shapes = [(4096, 4096), (1024, 4096), (64, 256)]        # the last goes to the small-matrix kernel
+    r = bench.fused_roofline(shapes, steps=2, fused_ms=40.0, fused_n=4, peak=1000.0, peak_src="x",
+                             pairs=True, launch_traffic=7e9)
+    fl = 5 * (3 * 4096 ** 3 + 4096 ** 3) + 5 * (3 * 1024 ** 2 * 4096 + 1024 ** 3)
+    assert r["achieved"] == pytest.approx(fl * 2 / 0.040 / 1e12)
+    assert r["launches_per_step"] == 2 and r["avg_launch_ms"] == 10.0
+    per_iter = 2 * (3 * 4096 * 4096 + 4 * 4096 ** 2) + 2 * (3 * 1024 * 4096 + 4 * 1024 ** 2)
+    assert r["algorithmic_bytes"] == pytest.approx(per_iter * 5 / 2)
+    assert r["traffic"] == 7e9 and "Fused" in r["kernel"]
+    assert bench.fused_traffic("tinymlp_d128") is None
+
+
 def test_bench_apply_roofline_arithmetic():
     """bench.py's roofline object from made-up timings: achieved rate, the
     per-launch traffic and algorithmic bytes follow from the shapes."""

@@ -328,8 +328,8 @@ def test_chunking_is_bitwise_neutral(handle):
     """The same list stepped as one chunk and as many small chunks, with the
     next chunk's momentum pass overlapped or not, gives bitwise identical
     weights and momenta (each matrix's arithmetic does not depend on its
-    neighbours); each chunk issues its own 4 + 3*ns launches (momentum pass,
-    norm, prescale redo pass, its norm, then three products per step)."""
+    neighbours); each chunk issues its own launches: momentum pass, norm,
+    prescale redo pass, its norm, then one fused launch of all products."""
     gen = torch.Generator().manual_seed(29)
     shapes = [(300, 500), (500, 300), (257, 257), (64, 640), (640, 64), (130, 900)]
     Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
@@ -347,8 +347,8 @@ def test_chunking_is_bitwise_neutral(handle):
             launches = dm.dmuon_launch_count(h2.h) - before
             summary = dm.dmuon_plan_summary(h2.h)
             res[elems] = ([x.cpu() for x in Wd], [x.cpu() for x in Md], launches, summary)
-    assert res[1 << 29][2] == 19 and "chunks 1 " in res[1 << 29][3]
-    assert res[160_000][2] > 19 and res[160_000][2] % 19 == 0
+    assert res[1 << 29][2] == 5 and "chunks 1 " in res[1 << 29][3]   # a small list: fused automatically
+    assert res[160_000][2] > 5 and res[160_000][2] % 5 == 0
     for key in (160_000, 160_001):   # overlapped and serial chunk schedules
         for a, b in zip(res[1 << 29][0] + res[1 << 29][1], res[key][0] + res[key][1]):
             assert torch.equal(a, b)
@@ -516,44 +516,97 @@ def test_argument_errors_with_live_handle(handle):
     assert dm.dmuon_launch_count(h) == before  # nothing launched
 
 
-def test_wait_timeout_is_reported_and_context_recovers(handle):
+@pytest.mark.parametrize("fused", [1, 0])
+def test_wait_timeout_is_reported_and_context_recovers(handle, fused):
     """A 1 ns wait limit makes the GEMM kernels give up at their first
-    non-immediate wait: they drain, free TMEM and return; the host reads
-    DMUON_ERR_TIMEOUT, and with the default limit restored the next step is
-    correct again."""
+    non-immediate wait (an mbarrier, or in the fused launch a tile counter):
+    they drain, free TMEM and return; the host reads DMUON_ERR_TIMEOUT, and
+    with the default limit restored the next step is correct again.  Both
+    the fused launch and the per-phase launches."""
     shapes = [(384, 200), (200, 640)]
     gen = torch.Generator().manual_seed(3)
     Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
     Gs = [torch.randn(s, generator=gen) for s in shapes]
     Ms = [torch.randn(s, generator=gen) for s in shapes]
     dm.dmuon_set_wait_timeout(handle.h, 1)
+    dm.dmuon_set_fused_phases(handle.h, fused)
     try:
         handle.step(_to_dev(Ws), _to_dev(Gs), _to_dev(Ms))
         rc, _ = handle.status(2)
     finally:
         dm.dmuon_set_wait_timeout(handle.h, 0)
+        dm.dmuon_set_fused_phases(handle.h, 2)
     assert rc == -6
     assert handle.status(2)[0] == 0   # the error word was cleared by the read
     _step_and_check(handle, Ws, Gs, Ms)
 
 
-def test_launch_count_and_profile(handle):
+@pytest.mark.parametrize("fused", [True, False])
+def test_launch_count_and_profile(handle, fused):
     shapes = [(256, 512), (512, 256)]
     Ws = [torch.zeros(s, device="cuda") for s in shapes]
     Gs = [torch.randn(s, device="cuda") for s in shapes]
     Ms = [torch.zeros(s, device="cuda") for s in shapes]
-    dm.dmuon_profile_enable(handle.h, True)
-    dm.dmuon_profile_read(handle.h)
-    before = dm.dmuon_launch_count(handle.h)
-    handle.step(Ws, Gs, Ms, ns_steps=5)
-    assert dm.dmuon_launch_count(handle.h) - before == 4 + 3 * 5
-    prof = dm.dmuon_profile_read(handle.h)
-    dm.dmuon_profile_enable(handle.h, False)
+    dm.dmuon_set_fused_phases(handle.h, fused)
+    try:
+        dm.dmuon_profile_enable(handle.h, True)
+        dm.dmuon_profile_read(handle.h)
+        before = dm.dmuon_launch_count(handle.h)
+        handle.step(Ws, Gs, Ms, ns_steps=5)
+        assert dm.dmuon_launch_count(handle.h) - before == (4 + 1 if fused else 4 + 3 * 5)
+        prof = dm.dmuon_profile_read(handle.h)
+        dm.dmuon_profile_enable(handle.h, False)
+    finally:
+        dm.dmuon_set_fused_phases(handle.h, 2)
     # the momentum kernel runs twice (the pass and the prescale redo pass), as does the finalisation
     assert prof["momentum"][1] == 2 and prof["finalize"][1] == 2
-    assert prof["gram"][1] == 5 and prof["apply"][1] == 5
+    if fused:
+        assert prof["ns_fused"][1] == 1 and prof["gram"][1] == 0 and prof["apply"][1] == 0
+    else:
+        assert prof["gram"][1] == 5 and prof["apply"][1] == 5 and prof["ns_fused"][1] == 0
     assert all(v[0] >= 0 for v in prof.values())
     assert "matrices 2" in dm.dmuon_plan_summary(handle.h)
+    assert handle.status()[0] == 0
+
+
+@pytest.mark.parametrize("tiles", [1, 2])
+def test_fused_phases_bitwise_equal_per_phase_launches(tiles):
+    """One fused launch per chunk runs the same tiles with the same
+    arithmetic as one launch per phase and iteration: weights and momenta
+    bitwise equal, on single CTAs and CTA pairs, for a list mixing shapes
+    (k/v-like short sides, tall and wide, ragged), over two chunks, with the
+    weight update, a standalone Newton-Schulz call and 1, 2 and 7 steps."""
+    gen = torch.Generator().manual_seed(53)
+    shapes = [(300, 700), (700, 300), (1024, 256), (257, 1100), (512, 512), (130, 2000), (96, 640)]
+    Ws = [torch.rand(s, generator=gen) - 0.5 for s in shapes]
+    Gs = [torch.randn(s, generator=gen) for s in shapes]
+    Ms = [torch.randn(s, generator=gen) for s in shapes]
+    res = {}
+    for fused in (True, False):
+        with dm.Handle(0) as h2:
+            dm.dmuon_set_tile_mode(h2.h, tiles)
+            dm.dmuon_set_small_path(h2.h, False)
+            dm.dmuon_set_chunk_elements(h2.h, 700_000)
+            dm.dmuon_set_fused_phases(h2.h, fused)
+            out = []
+            for ns in (5, 1, 2, 7):
+                Wd, Gd, Md = _to_dev(Ws), _to_dev(Gs), _to_dev(Ms)
+                h2.step(Wd, Gd, Md, ns_steps=ns)
+                assert h2.status()[0] == 0
+                out += [x.cpu() for x in Wd + Md]
+            O = [torch.empty(s, device="cuda") for s in shapes]
+            h2.newton_schulz(_to_dev(Gs), O)
+            assert h2.status()[0] == 0
+            out += [o.cpu() for o in O]
+            assert "chunks 3 " in dm.dmuon_plan_summary(h2.h)
+            res[fused] = out
+    for a, b in zip(res[True], res[False]):
+        assert torch.equal(a, b)
+    with dm.Handle(0) as h3:   # and the fused launch against the oracle
+        dm.dmuon_set_tile_mode(h3.h, tiles)
+        dm.dmuon_set_small_path(h3.h, False)
+        dm.dmuon_set_chunk_elements(h3.h, 700_000)
+        _step_and_check(h3, Ws, Gs, Ms)
 
 
 # ---------------------------------------------------------------- full size
