@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-aux", action="store_true")
     p.add_argument("--no-gram", action="store_true")
+    p.add_argument("--fp16-iters", type=int, default=0,
+                   help="direct backend: leading iterations with fp16 operands (0: the library's default)")
     p.add_argument("--fused", default="auto", choices=["auto", "always", "never"],
                    help="direct backend: one launch per chunk for all products (auto: the library's rule)")
     p.add_argument("--no-split", action="store_true",
@@ -391,6 +393,8 @@ def run_ours(args, rank, world, local_rank):
         dm.dmuon_set_tile_mode(h.h, args.tile_mode)
     dm.dmuon_set_balanced_dealing(h.h, args.dealing == "balanced")
     dm.dmuon_set_fused_phases(h.h, {"auto": 2, "always": 1, "never": 0}[args.fused])
+    if args.fp16_iters:
+        dm.dmuon_set_fp16_iterations(h.h, args.fp16_iters)
     for step in range(w.warm_steps):
         Gw = [workloads.grad(w, i, step, dev) for i in range(n)]
         h.step(Ws, Gw, Ms, lr=lr, mu=mu)
@@ -506,7 +510,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": "muon_step_tflops", "value": value, "unit": "TFLOP/s (algorithmic)",
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16/bf16", "data": "synthetic",
         "matrices_per_s": n * args.steps * world / sec,
         "dense_equiv_tflops": flops.dense_flops(shapes) * args.steps * world / sec / 1e12,
         "config": {"workload": args.workload, "matrices": n, "ns_steps": 5,
@@ -515,6 +519,8 @@ def run_ours(args, rank, world, local_rank):
                           if resident > 129e6 else
                           "inputs fit in L2 (%.1f MB resident W/G/M; a latency case, not flushed)" % (resident / 1e6)),
                    "dealing": args.dealing,
+                   "operands": "fp16 in the first %s iterations, bf16 after; fp32 accumulate"
+                               % (args.fp16_iters or 3),
                    "parallelism": "replicas x%d" % world if world > 1 else "single GPU"},
         "gpu_launches": launches,
         "roofline": roofline,

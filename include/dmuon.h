@@ -24,14 +24,19 @@
  * default five-row table used here).
  *
  * Precision: momentum and the update are fp32; the Newton-Schulz products
- * run on 16-bit tensor cores (kind::f16 with fp16 operands) with fp32
- * accumulation, with X, A, B held in fp16 between products, each with a
- * power-of-two scale that keeps it in fp16's normal range (X0 = p U with p
- * chosen from max |U|; later X as beta X, beta ~ sqrt(n); A as kappa X X^T,
- * kappa ~ m): fp16's three extra mantissa bits over bf16 cut the rounding
- * error about eightfold at the same tensor-core rate.  The last iteration's
- * output goes to the update in fp32.  Coefficient tables that could drive a
- * buffer past the fp16 range for some input are refused (DMUON_ERR_ARG).
+ * run on 16-bit tensor cores with fp32 accumulation, with X, A, B held in 16
+ * bits between products, each with a power-of-two scale that keeps it in
+ * fp16's normal range (X0 = p U with p chosen from max |U|; later X as
+ * beta X, beta ~ sqrt(n); A as kappa X X^T, kappa ~ m).  The first
+ * iterations use fp16 operands, whose three extra mantissa bits over bf16
+ * cut the rounding error about eightfold where it matters most (small
+ * singular values are still in their linear regime); the direct backend's
+ * later iterations use bf16, which costs less energy at the same rate
+ * (dmuon_set_fp16_iterations; the Gram backend, the small-matrix kernel and
+ * the allocation-free entry point are fp16 throughout).  The last
+ * iteration's output goes to the update in fp32.  Coefficient tables that
+ * could drive a buffer past the fp16 range for some input are refused
+ * (DMUON_ERR_ARG).
  *
  * Threading/streams: a handle is not thread-safe.  Calls on one handle are
  * asynchronous on the given stream and must be issued on one stream (or be
@@ -344,6 +349,15 @@ int dmuon_set_overlap(dmuon_handle_t h, int on);
  * The result is bitwise the same either way (each tile's arithmetic does not
  * depend on who computes it).  dmuon_plan_summary reports the balance. */
 int dmuon_set_balanced_dealing(dmuon_handle_t h, int on);
+
+/* Direct backend (chunked matrices), calls from now on: the number of
+ * leading Newton-Schulz iterations whose products take fp16 operands (>= 1;
+ * default 3; 64 or more: every iteration); later iterations take bf16 with
+ * the same scales.  fp16 draws more power than bf16 at the same tensor-core
+ * rate, so on a GB300 held at its power cap each bf16 iteration is slightly
+ * faster; the first iterations carry most of the rounding error of inputs
+ * with widely spread singular values.  DMUON_ERR_ARG for iters < 1. */
+int dmuon_set_fp16_iterations(dmuon_handle_t h, int iters);
 
 /* Direct backend, calls from now on: whether every Gram, Gram2 and Apply
  * product of every iteration of a chunk runs in ONE persistent launch instead

@@ -115,6 +115,8 @@ def load(path=None):
     L.dmuon_set_balanced_dealing.restype = i32
     L.dmuon_set_fused_phases.argtypes = [vp, i32]
     L.dmuon_set_fused_phases.restype = i32
+    L.dmuon_set_fp16_iterations.argtypes = [vp, i32]
+    L.dmuon_set_fp16_iterations.restype = i32
     L.dmuon_set_small_path.argtypes = [vp, i32]
     L.dmuon_set_small_path.restype = i32
     L.dmuon_set_chunk_elements.argtypes = [vp, i64]
@@ -438,6 +440,12 @@ def dmuon_set_chunk_elements(h, elems):
 def dmuon_set_balanced_dealing(h, on=True):  # default on in the library
     """Longest-first dealing of work items to the least-loaded CTA (pair) for later plans."""
     _check(load().dmuon_set_balanced_dealing(h, 1 if on else 0), "dmuon_set_balanced_dealing")
+
+
+def dmuon_set_fp16_iterations(h, iters=3):  # default 3 in the library
+    """Direct backend: leading Newton-Schulz iterations with fp16 operands
+    (later ones bf16); 64 or more: every iteration."""
+    _check(load().dmuon_set_fp16_iterations(h, int(iters)), "dmuon_set_fp16_iterations")
 
 
 def dmuon_set_fused_phases(h, mode=2):  # default 2 (automatic) in the library

@@ -142,6 +142,11 @@ struct GemmArgs {
   int n_iters;
   int* counters;           // per matrix, zero at launch
   float coef[64][3];
+  // Operand precision: iteration k multiplies fp16 operands when k <
+  // f16_iters, else bf16 (same scales).  Per-phase launches give their
+  // iteration in `iter`; X0 is always fp16 (f16_iters >= 1).
+  int iter;
+  int f16_iters;
 };
 
 // Items of one persistent processor (a CTA, or a CTA pair): its own run

@@ -152,6 +152,7 @@ struct dmuon_ctx {
   // a side stream, two alternating chunk workspaces and fork/join events.
   bool overlap = false;                     // requested (off: measured neutral at the power cap)
   bool balanced = true;                     // requested: work items dealt longest-first to the least loaded
+  int f16_iters = 3;                        // direct backend: leading iterations with fp16 operands
   int fused = 2;                            // direct backend, one launch per chunk for all products:
                                             // 0 never, 1 always, 2 for chunks of few work items
   bool plan_balanced = true;                // in the current plan
@@ -678,6 +679,7 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
       for (int q = 0; q < 3; ++q) a.coef[k][q] = row[q];
     }
     a.counters = ch.d_counters;
+    a.f16_iters = h->f16_iters;
     a.fold = 1;
     a.final_mode = ns_only ? kWriteO : kUpdateW;
     a.lr = lr;
@@ -712,6 +714,8 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
       a.src = k & 1;
       a.ca = row[0]; a.cb = row[1]; a.cc = row[2];
       a.first = k == 0;
+      a.iter = k;
+      a.f16_iters = h->f16_iters;
       a.fold = 1;
       a.final_mode = (k == ns_steps - 1) ? (ns_only ? kWriteO : kUpdateW) : kWriteX;
       a.lr = lr;
@@ -787,6 +791,7 @@ int run_chunk_gram(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr
     a.n_items = (int)L.items[kPhaseApply].size();
     a.src = src;
     a.ca = 0.f;          // X' = Q X
+    a.f16_iters = 1 << 30;  // the Gram backend is fp16 throughout
     a.fold = 1;          // no a*X term to add: skip reading X in the epilogue
     a.first = first;     // the first window's X is X0 = p U: times s/p
     a.final_mode = mode;
@@ -1467,6 +1472,12 @@ int dmuon_set_overlap(dmuon_handle_t h, int on) {
 int dmuon_set_balanced_dealing(dmuon_handle_t h, int on) {
   if (!h) return DMUON_ERR_ARG;
   h->balanced = on != 0;
+  return DMUON_OK;
+}
+
+int dmuon_set_fp16_iterations(dmuon_handle_t h, int iters) {
+  if (!h || iters < 1) return DMUON_ERR_ARG;
+  h->f16_iters = iters;
   return DMUON_OK;
 }
 

@@ -296,6 +296,8 @@ extern "C" int dmuon_newton_schulz_noalloc(const float* input, float* output, in
       a.cb = row[1];
       a.cc = row[2];
       a.first = k == 0;
+      a.iter = k;
+      a.f16_iters = 1 << 30;  // fp16 operands in every iteration
       a.final_mode = (k == ns_steps - 1) ? kWriteO : kWriteX;
       a.lr = 0.f;
       a.decay = 1.f;

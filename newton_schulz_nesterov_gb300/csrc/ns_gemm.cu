@@ -81,15 +81,24 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   return wait_slow(bar, parity, abort_flag, err, true, limit_ns);
 }
 
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  const __half2 v = __floats2half2_rn(lo, hi);
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
+  if (f16) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// 32 consecutive fp16 of one row -> fp32, zero outside [0, ncols) or when
-// the row is invalid.
+__device__ __forceinline__ float2 unpack2(uint32_t w, bool f16) {
+  if (f16) return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// 32 consecutive 16-bit values (fp16, or bf16 when !f16) of one row -> fp32,
+// zero outside [0, ncols) or when the row is invalid.
 __device__ __forceinline__ void load_row32(const __half* rowp, int64_t c, int64_t ncols,
-                                           bool row_ok, float (&f)[32]) {
+                                           bool row_ok, float (&f)[32], bool f16) {
   if (row_ok && c + 32 <= ncols) {
     const uint4* p = reinterpret_cast<const uint4*>(rowp + c);
 #pragma unroll
@@ -98,15 +107,16 @@ __device__ __forceinline__ void load_row32(const __half* rowp, int64_t c, int64_
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        const float2 t = unpack2(w[k], f16);
         f[q * 8 + 2 * k] = t.x;
         f[q * 8 + 2 * k + 1] = t.y;
       }
     }
   } else {
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(rowp);
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      f[j] = (row_ok && c + j < ncols) ? __half2float(rowp[c + j]) : 0.f;
+      f[j] = (row_ok && c + j < ncols) ? unpack2((uint32_t)h[c + j], f16).x : 0.f;
   }
 }
 
@@ -204,13 +214,15 @@ struct ItemCursor {
 struct StageParams {
   int src, first;
   float ca, cb, cc;
+  bool f16_in, f16_out;  // this iteration's operand format; the Apply output's (the next iteration's)
 };
 template <int PHASE>
 __device__ __forceinline__ StageParams stage_params(const GemmArgs& a, int it) {
   if constexpr (PHASE == kPhaseFused)
-    return StageParams{it & 1, it == 0 ? 1 : 0, a.coef[it][0], a.coef[it][1], a.coef[it][2]};
+    return StageParams{it & 1, it == 0 ? 1 : 0, a.coef[it][0], a.coef[it][1], a.coef[it][2], it < a.f16_iters,
+                       it + 1 < a.f16_iters};
   else
-    return StageParams{a.src, a.first, a.ca, a.cb, a.cc};
+    return StageParams{a.src, a.first, a.ca, a.cb, a.cc, a.iter < a.f16_iters, a.iter + 1 < a.f16_iters};
 }
 
 // Fused launches: a tile of stage s = 3k + p waits until its matrix's counter
@@ -312,7 +324,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const StagePara
         for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]) * alpha;
       } else {
         float av[32];
-        load_row32(d.A + r * ld, c, m, row_ok, av);
+        load_row32(d.A + r * ld, c, m, row_ok, av, sp.f16_in);
 #pragma unroll
         for (int j = 0; j < 32; ++j) f[j] = fmaf(gcc, __uint_as_float(v[j]), gcb * av[j]);
         if (a.fold) {
@@ -323,7 +335,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const StagePara
       }
       uint32_t w[16];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) w[k] = pack2(f[2 * k], f[2 * k + 1]);
+      for (int k = 0; k < 16; ++k) w[k] = pack2(f[2 * k], f[2 * k + 1], sp.f16_in);
       store_row32(dst + r * ld, c, m, row_ok, w);
       if (mirror) mirror_store32(dst, ld, c, rbase, m, lane, w, scratch);
     }
@@ -347,14 +359,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const StagePara
         for (int j = 0; j < 32; ++j) o[j] = alpha * __uint_as_float(v[j]);
       } else {
         float xv[32];
-        load_row32(xsrc + r * ldx, c, n, row_ok, xv);
+        load_row32(xsrc + r * ldx, c, n, row_ok, xv, sp.f16_in);
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = alpha * fmaf(sp.ca, xv[j], __uint_as_float(v[j]));
       }
       if constexpr (MODE == kWriteX) {
         uint32_t w[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) w[k] = pack2(o[2 * k], o[2 * k + 1]);
+        for (int k = 0; k < 16; ++k) w[k] = pack2(o[2 * k], o[2 * k + 1], sp.f16_out);
         store_row32(xd + r * ldx, c, n, row_ok, w);
       } else if (row_ok) {
         // All loads of W for this chunk are issued before any store, so the
@@ -534,6 +546,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_sym = ptx::idesc_f16(kBM, kBN, 0), idesc_app = ptx::idesc_f16(kBM, kBN, 1);
+      constexpr uint32_t bdesc_sym = ptx::idesc_bf16(kBM, kBN, 0), bdesc_app = ptx::idesc_bf16(kBM, kBN, 1);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
@@ -546,7 +559,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         ptx::tc_fence_after();
         const uint32_t dt = tmem_base + acc * kBN;
         const bool mn = inf.ph == kPhaseApply;  // X as the MN-major B operand
-        const uint32_t idesc = mn ? idesc_app : idesc_sym;
+        const bool f16 = (PHASE == kPhaseFused ? inf.it : a.iter) < a.f16_iters;
+        const uint32_t idesc = f16 ? (mn ? idesc_app : idesc_sym) : (mn ? bdesc_app : bdesc_sym);
         for (int kb = 0; kb < inf.kbn; ++kb, ++it) {
           const uint32_t s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
@@ -740,6 +754,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_sym = ptx::idesc_f16(256, kBN, 0), idesc_app = ptx::idesc_f16(256, kBN, 1);
+      constexpr uint32_t bdesc_sym = ptx::idesc_bf16(256, kBN, 0), bdesc_app = ptx::idesc_bf16(256, kBN, 1);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
@@ -752,7 +767,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
         ptx::tc_fence_after();
         const uint32_t dt = tmem_base + acc * kBN;
         const bool mn = inf.ph == kPhaseApply;  // X as the MN-major B operand
-        const uint32_t idesc = mn ? idesc_app : idesc_sym;
+        const bool f16 = (PHASE == kPhaseFused ? inf.it : a.iter) < a.f16_iters;
+        const uint32_t idesc = f16 ? (mn ? idesc_app : idesc_sym) : (mn ? bdesc_app : bdesc_sym);
         for (int kb = 0; kb < inf.kbn; ++kb, ++it) {
           const uint32_t s = it % kPairStages;
           const uint32_t ph = (it / kPairStages) & 1u;

@@ -252,12 +252,14 @@ def test_step_scaled_inputs_and_prescale_redo(handle):
             assert e <= NS_TOL, (scale, i, e)
 
 
+@pytest.mark.parametrize("f16_iters", [3, 64])
 @pytest.mark.parametrize("ratio", [1e2, 1e3, 1e4])
 @pytest.mark.parametrize("table", ["you", "polar_express"])
-def test_ill_conditioned_inputs(handle, ratio, table):
+def test_ill_conditioned_inputs(handle, ratio, table, f16_iters):
     """Inputs whose singular values spread log-uniformly over [1/ratio, 1]
     (wide, tall and square; ratio up to 1e4), with the printed table and the
-    Polar Express table: the fp16 iterate keeps the output within the bar."""
+    Polar Express table, fp16 operands in the first three iterations (the
+    default) or in all: the output stays within the bar."""
     from _parity import spectrum_matrix
     from oracle import polar_express as pe
     coeffs = None if table == "you" else dm.dmuon_polar_express_coefficients(5)
@@ -265,12 +267,44 @@ def test_ill_conditioned_inputs(handle, ratio, table):
     shapes = [(300, 700), (700, 300), (500, 500), (128, 4096)]
     ins = [torch.from_numpy(spectrum_matrix(r, c, ratio, 31 + k)) for k, (r, c) in enumerate(shapes)]
     outs = [torch.empty(s, device="cuda") for s in shapes]
-    handle.newton_schulz([x.cuda() for x in ins], outs, coeffs=coeffs)
+    dm.dmuon_set_fp16_iterations(handle.h, f16_iters)
+    try:
+        handle.newton_schulz([x.cuda() for x in ins], outs, coeffs=coeffs)
+    finally:
+        dm.dmuon_set_fp16_iterations(handle.h, 3)
     assert handle.status()[0] == 0
     for x, o, s in zip(ins, outs, shapes):
         ref = oracle.newton_schulz(x.numpy().astype(np.float64), 5, coeffs=ref_coeffs)
         e = rel_fro(o.cpu().numpy(), ref)
         assert e <= NS_TOL, (s, ratio, table, e)
+
+
+def test_fp16_iterations_knob(handle):
+    """Each iteration's operand format follows the knob: on a Gaussian
+    input, fp16 everywhere is the most accurate and fp16 in the first
+    iteration only the least, all within the bar; fused and per-phase
+    launches agree bitwise at every setting; 0 is refused."""
+    x = torch.randn((512, 1536), generator=torch.Generator().manual_seed(71))
+    ref = oracle.newton_schulz(x.numpy().astype(np.float64))
+    errs = {}
+    for iters in (1, 3, 64):
+        outs = []
+        for fused in (1, 0):
+            o = torch.empty((512, 1536), device="cuda")
+            dm.dmuon_set_fp16_iterations(handle.h, iters)
+            dm.dmuon_set_fused_phases(handle.h, fused)
+            try:
+                handle.newton_schulz([x.cuda()], [o])
+            finally:
+                dm.dmuon_set_fp16_iterations(handle.h, 3)
+                dm.dmuon_set_fused_phases(handle.h, 2)
+            assert handle.status()[0] == 0
+            outs.append(o.cpu())
+        assert torch.equal(outs[0], outs[1])
+        errs[iters] = rel_fro(outs[0].numpy(), ref)
+    assert errs[64] < errs[3] < errs[1] <= NS_TOL, errs
+    with pytest.raises(dm.DmuonError):
+        dm.dmuon_set_fp16_iterations(handle.h, 0)
 
 
 def test_coefficient_table_outside_fp16_range_is_refused(handle):
