@@ -166,6 +166,10 @@ __device__ __forceinline__ WorkRange work_range(const int* starts, int proc, int
 // flags the matrix; the redo pass (redo = 1) then rewrites X[0] and the tile
 // sums of the flagged matrices from G and the updated M (the same U, bit for
 // bit) and a second finalisation completes them.
+// Resident CTAs per SM of the momentum kernel (its launch bound); a launch
+// needs no more than num_sms * kMomCtasPerSm CTAs (they stride over tiles).
+constexpr int kMomCtasPerSm = 4;
+
 struct MomArgs {
   const MatDesc* mats;
   const MatPtrs* ptrs;

@@ -620,7 +620,7 @@ int run_chunk_norm(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float mu
   const Layout& L = ch.L;
   const int n = ch.n;
   const int64_t nt = L.tile_prefix[n];
-  const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * 8);
+  const int grid = (int)std::min<int64_t>(nt, (int64_t)h->num_sms * kMomCtasPerSm);
   cudaError_t e;
   for (int pass = 0; pass < 2; ++pass) {
     {

@@ -37,11 +37,14 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 // Momentum pass (redo_pass = 0):
 //   M <- mu*M + G ;  U = G + mu*M (nesterov) or M ;  X0 <- fp16(p U or p U^T)
 //   partials[tile] = sum((p U)^2), tmax[tile] = max |U|, fixed reduction order.
-// Redo pass (redo_pass = 1): only tiles of matrices flagged by the
-// finalisation; U is recomputed from G and the already updated M (the same
-// fmaf sequence, so the same U) and X0 and partials are rewritten with the
-// matrix's new p.  A CTA that finds no flagged matrix returns at once.
-__global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
+// Redo pass (REDO): only tiles of matrices flagged by the finalisation; U is
+// recomputed from G and the already updated M (the same fmaf sequence, so the
+// same U) and X0 and partials are rewritten with the matrix's new p.  A CTA
+// that finds no flagged matrix returns at once.
+// Up to 64 registers a thread (kMomCtasPerSm CTAs per SM), so that the eight
+// 16-byte loads of a tile's four rows are all in flight before its stores.
+template <bool REDO>
+__global__ void __launch_bounds__(256, kMomCtasPerSm) mom_norm_kernel(const MomArgs a) {
   __shared__ uint32_t stage[kMomTile * 33];  // 64 x 66 fp16, odd word stride
   __shared__ float red[8];
   __shared__ float redm[8];
@@ -50,7 +53,7 @@ __global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
   const int tid = threadIdx.x;
   const int cl = (tid & 15) * 4;
   const int rl0 = tid >> 4;
-  const bool redo_pass = a.redo_pass != 0;
+  constexpr bool redo_pass = REDO;
 
   if (redo_pass) {
     if (tid == 0) any = 0;
@@ -79,6 +82,17 @@ __global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
     const int64_t ldx = d.ldx;
     float ss = 0.f, mx = 0.f;
 
+    // Every load of the tile's four rows is issued before any store: the
+    // compiler may not move a load above a store to memory it might alias.
+    float4 gv[4], mv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t r = r0 + rl0 + 16 * i;
+      if (vec && r < rows && c < cols) {
+        gv[i] = ld_once(p.G + r * cols + c);
+        if (!a.ns_only) mv[i] = ld_once(p.M + r * cols + c);
+      }
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int rl = rl0 + 16 * i;
@@ -87,18 +101,18 @@ __global__ void __launch_bounds__(256) mom_norm_kernel(const MomArgs a) {
       if (r < rows && c < cols) {
         const int64_t off = r * cols + c;
         if (vec) {
-          const float4 g4 = ld_once(p.G + off);
+          const float4 g4 = gv[i];
           const float g[4] = {g4.x, g4.y, g4.z, g4.w};
           if (a.ns_only) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) u[j] = g[j];
           } else if (redo_pass) {
-            const float4 m4 = ld_once(p.M + off);  // already mu*M + G
+            const float4 m4 = mv[i];  // already mu*M + G
             const float mn[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) u[j] = a.nesterov ? fmaf(a.mu, mn[j], g[j]) : mn[j];
           } else {
-            const float4 m4 = ld_once(p.M + off);
+            const float4 m4 = mv[i];
             const float mo[4] = {m4.x, m4.y, m4.z, m4.w};
             float mn[4];
 #pragma unroll
@@ -309,7 +323,10 @@ __global__ void __launch_bounds__(256) update0_kernel(const Update0Args a) {
 }  // namespace
 
 cudaError_t launch_mom(const MomArgs& a, int grid, cudaStream_t s) {
-  mom_norm_kernel<<<grid, 256, 0, s>>>(a);
+  if (a.redo_pass)
+    mom_norm_kernel<true><<<grid, 256, 0, s>>>(a);
+  else
+    mom_norm_kernel<false><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

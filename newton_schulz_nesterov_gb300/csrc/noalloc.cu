@@ -266,8 +266,9 @@ extern "C" int dmuon_newton_schulz_noalloc(const float* input, float* output, in
   const CUtensorMap* maps = reinterpret_cast<const CUtensorMap*>(base + kOffMaps);
 
   const int grid_e = (int)std::min<int64_t>(n_tiles, (int64_t)ds->num_sms * 8);
+  const int grid_m = (int)std::min<int64_t>(n_tiles, (int64_t)ds->num_sms * kMomCtasPerSm);
   for (int pass = 0; pass < 2; ++pass) {  // momentum-free pass, then the redo pass if p missed
-    if (launch_mom(MomArgs{dd, dp, dprefix, 1, n_tiles, 0.f, 0, 1, partials, tmax, pscale, redo, pass}, grid_e,
+    if (launch_mom(MomArgs{dd, dp, dprefix, 1, n_tiles, 0.f, 0, 1, partials, tmax, pscale, redo, pass}, grid_m,
                    stream) != cudaSuccess)
       return DMUON_ERR_CUDA;
     if (launch_finalize(FinalizeArgs{dd, dprefix, partials, tmax, 1, eps, svec, bvec, pscale, redo, flags, pass},

@@ -124,7 +124,11 @@ __device__ __forceinline__ void load_row32(const __half* rowp, int64_t c, int64_
 __device__ __forceinline__ void store_row32(__half* rowp, int64_t c, int64_t ncols,
                                             bool row_ok, const uint32_t (&w)[16]) {
   if (!row_ok) return;
-  if (c + 32 <= ncols) {
+  if (c + 32 <= ncols && (reinterpret_cast<uintptr_t>(rowp + c) & 31u) == 0) {
+    // Two whole 32-byte sectors per lane, one 256-bit store each.
+#pragma unroll
+    for (int q = 0; q < 2; ++q) ptx::st_global_v8(rowp + c + 16 * q, w + 8 * q);
+  } else if (c + 32 <= ncols) {
     uint4* p = reinterpret_cast<uint4*>(rowp + c);
 #pragma unroll
     for (int q = 0; q < 4; ++q) p[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
