@@ -57,8 +57,9 @@ def parse_args():
                    help="direct backend: one launch per chunk for all products (auto: the library's rule)")
     p.add_argument("--no-split", action="store_true",
                    help="skip the per-phase breakdown (a few steps with one launch per phase)")
-    p.add_argument("--tile-mode", type=int, default=0, choices=[0, 1, 2],
-                   help="direct backend tiles: 0 automatic, 1 single CTAs (128x256), 2 CTA pairs (256x256)")
+    p.add_argument("--tile-mode", type=int, default=0, choices=[0, 1, 2, 3],
+                   help="direct backend tiles: 0 automatic, 1 single CTAs (128x256), 2 CTA pairs (256x256), "
+                        "3 single CTAs (128x128)")
     p.add_argument("--dealing", default="balanced", choices=["balanced", "strided"],
                    help="work items to persistent CTAs: longest first to the least loaded, or round-robin")
     return p.parse_args()
@@ -131,7 +132,8 @@ def fused_traffic(workload):
     return int(per.group(1))
 
 
-def apply_roofline(shapes, steps, apply_ms, apply_n, peak, peak_src, pairs, step_traffic, ns_steps=5):
+def apply_roofline(shapes, steps, apply_ms, apply_n, peak, peak_src, pairs, step_traffic, ns_steps=5,
+                   single_tiles="128x256"):
     """Roofline object of the Apply kernel from its summed CUDA-event time
     (apply_ms over apply_n launches in `steps` timed steps): achieved
     algorithmic TFLOP/s against the tensor peak, and per launch the measured
@@ -144,7 +146,7 @@ def apply_roofline(shapes, steps, apply_ms, apply_n, peak, peak_src, pairs, step
     launches_per_step = apply_n / steps
     alg_bytes = sum(2 * (2 * min(r, c) * max(r, c) + min(r, c) ** 2) for r, c in big) * ns_steps / launches_per_step
     kname = ("ns_gemm_pair_kernel<Apply> (X' = Z*X, Z = aI + bA + cAA, 256x256 CTA-pair tiles)" if pairs else
-             "ns_gemm_kernel<Apply> (X' = Z*X, 128x256 tiles)")
+             "ns_gemm_kernel<Apply> (X' = Z*X, %s tiles)" % single_tiles)
     return {"kernel": kname, "bound": "tensor",
             "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "peak_source": peak_src,
@@ -154,7 +156,8 @@ def apply_roofline(shapes, steps, apply_ms, apply_n, peak, peak_src, pairs, step
             "avg_launch_ms": apply_ms / apply_n}
 
 
-def fused_roofline(shapes, steps, fused_ms, fused_n, peak, peak_src, pairs, launch_traffic, ns_steps=5):
+def fused_roofline(shapes, steps, fused_ms, fused_n, peak, peak_src, pairs, launch_traffic, ns_steps=5,
+                   single_tiles="128x256"):
     """Roofline object of the fused Newton-Schulz kernel (every Gram, Gram2
     and Apply product of a chunk in one launch) from its summed CUDA-event
     time (fused_ms over fused_n launches in `steps` timed steps): the chunked
@@ -169,7 +172,7 @@ def fused_roofline(shapes, steps, fused_ms, fused_n, peak, peak_src, pairs, laun
     launches_per_step = fused_n / steps
     per_iter = sum(2 * (3 * min(r, c) * max(r, c) + 4 * min(r, c) ** 2) for r, c in big)
     kname = ("ns_gemm_pair_kernel<Fused> (all Gram, Gram2 and Apply products of a chunk, 256x256 CTA-pair tiles)"
-             if pairs else "ns_gemm_kernel<Fused> (all products of a chunk, 128x256 tiles)")
+             if pairs else "ns_gemm_kernel<Fused> (all products of a chunk, %s tiles)" % single_tiles)
     return {"kernel": kname, "bound": "tensor",
             "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "peak_source": peak_src,
@@ -458,13 +461,15 @@ def run_ours(args, rank, world, local_rank):
     # the phase's algorithmic work over the timed steps by its summed time.
     apply_ms, apply_n = prof["apply"]
     fused_ms, fused_n = prof["ns_fused"]
-    pairs = "pairs" in dm.dmuon_plan_summary(h.h)
+    summary = dm.dmuon_plan_summary(h.h)
+    pairs = "pairs" in summary
+    single_tiles = "128x128" if "128x128 single" in summary else "128x256"
     if fused_n:
         roofline = fused_roofline(shapes, args.steps, fused_ms, fused_n, peak, peak_src, pairs,
-                                  fused_traffic(args.workload))
+                                  fused_traffic(args.workload), single_tiles=single_tiles)
     elif apply_n:
         roofline = apply_roofline(shapes, args.steps, apply_ms, apply_n, peak, peak_src, pairs,
-                                  apply_traffic(args.workload))
+                                  apply_traffic(args.workload), single_tiles=single_tiles)
     else:
         roofline = None
     phase = {k: {"ms_per_launch": (v[0] / v[1]) if v[1] else None, "launches": v[1],

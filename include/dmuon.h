@@ -317,11 +317,14 @@ int dmuon_set_wait_timeout(dmuon_handle_t h, uint64_t ns);
 /* Tensor-core tiling of later plans: 0 = automatic (the default: CTA pairs when
  * the device can co-schedule 2-CTA clusters, some chunked matrix has a short
  * side above 128 and the chunked matrices give at least one 256x256 Gram
- * super-tile per pair; single CTAs otherwise), 1 = single CTAs computing
- * 128x256 tiles, 2 = CTA pairs computing 256x256 tiles (cta_group::2).  The
- * result is the same maths with the same roundings; the choice only changes
- * speed.  It applies to the direct backend; the Gram backend always uses CTA
- * pairs.  DMUON_ERR_UNSUPPORTED if pairs are requested but unavailable. */
+ * super-tile per pair; single CTAs otherwise, with 128x128 tiles when the
+ * 128x256 Gram tiles would number fewer than the SMs), 1 = single CTAs
+ * computing 128x256 tiles, 2 = CTA pairs computing 256x256 tiles
+ * (cta_group::2), 3 = single CTAs computing 128x128 tiles.  The result is the
+ * same maths up to the order of the fp32 sums of a tile's products; the
+ * choice only changes speed.  It applies to the direct backend; the Gram
+ * backend always uses CTA pairs.  DMUON_ERR_UNSUPPORTED if pairs are
+ * requested but unavailable, DMUON_ERR_ARG for another mode. */
 int dmuon_set_tile_mode(dmuon_handle_t h, int mode);
 
 /* Chunking of later plans: the matrix list is cut into contiguous chunks of
@@ -470,7 +473,8 @@ int dmuon_gram_check_coefficients(int ns_steps, const float* coeffs,
 /*
  * Host-only preview of the plan a handle would build for this list, without
  * a device: the tile kind the automatic choice (tile_mode 0) or the forced
- * one (1 single CTAs, 2 CTA pairs) gives, the chunks, the work items per
+ * one (1 single CTAs 128x256, 2 CTA pairs, 3 single CTAs 128x128) gives,
+ * the chunks, the work items per
  * phase and how evenly they are dealt ("balance", as in
  * dmuon_plan_summary), for a device with `clusters` co-resident 2-CTA
  * clusters (0 = none) and `sms` SMs; balanced = 0 previews the strided

@@ -216,7 +216,8 @@ struct Update0Args {          // ns_steps == 0: O = (s/p) X[0] straight to W / o
 cudaError_t launch_mom(const MomArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 cudaError_t launch_update0(const Update0Args& a, int grid, cudaStream_t s);
-cudaError_t launch_gemm(int phase, const GemmArgs& a, int grid, cudaStream_t s);
+// Single-CTA launches; bn: tile width (256, or 128 for narrow plans).
+cudaError_t launch_gemm(int phase, const GemmArgs& a, int grid, cudaStream_t s, int bn = kBN);
 cudaError_t gemm_configure();
 // CTA-pair kernels: items are {matrix, 256-row tile, 256-col tile, K blocks};
 // `clusters` 2-CTA clusters are launched.

@@ -144,9 +144,10 @@ struct dmuon_ctx {
   std::string last_error;
   unsigned long long wait_timeout_ns = 0;  // 0: kernels' default (4 s)
   int max_clusters = 0;                     // resident 2-CTA clusters (0: pairs unavailable)
-  int tile_mode = 0;                        // requested: 0 auto, 1 single CTA, 2 CTA pairs
+  int tile_mode = 0;                        // requested: 0 auto, 1 single CTA, 2 CTA pairs, 3 single CTA 128x128
   int64_t chunk_elems = 0;                  // requested chunk size (0: default)
   bool plan_pair = false;                   // tile kind of the current plan
+  int plan_bn = kBN;                        // its single-CTA tile width (256, or 128)
   int64_t plan_chunk_elems = 0;             // chunk size of the current plan
   // Overlap of chunk c+1's momentum pass with chunk c's tensor-core phases:
   // a side stream, two alternating chunk workspaces and fork/join events.
@@ -245,7 +246,7 @@ inline std::pair<double, double> deal_balance(const Layout& L, int q) {
 bool choose_pairs(int max_clusters, int tile_mode, bool small_on, const dmuon_shape_t* s, int n, bool gram) {
   if (max_clusters <= 0) return false;
   if (gram) return true;  // the Gram-space kernels exist for CTA pairs only
-  if (tile_mode == 1) return false;
+  if (tile_mode == 1 || tile_mode == 3) return false;  // single CTAs, 128 x 256 or 128 x 128
   if (tile_mode == 2) return true;
   // Automatic: pairs once some chunked matrix's short side exceeds one
   // 128-row tile and the chunked matrices give at least one 256 x 256 Gram
@@ -267,10 +268,32 @@ bool use_pairs(const dmuon_ctx* h, const dmuon_shape_t* s, int n, bool gram = fa
   return choose_pairs(h->max_clusters, h->tile_mode, h->small_path && h->small_ok, s, n, gram);
 }
 
+// Single-CTA tile width.  Automatic: 128 x 128 blocks when the 128 x 256
+// Gram items of the chunked matrices would leave SMs idle -- such lists are
+// latency-bound (short K, exposed epilogues), and blocks of half the width
+// double the items and halve each one's epilogue (TinyMLP d=512: 72 items
+// of 128 x 256 for 152 SMs).
+int choose_bn(int sms, int tile_mode, bool small_on, const dmuon_shape_t* s, int n) {
+  if (tile_mode == 3) return kBM;
+  if (tile_mode == 1) return kBN;
+  int64_t items = 0;
+  for (int i = 0; i < n; ++i) {
+    if (small_on && is_small(s[i])) continue;
+    const int64_t m = std::min(s[i].rows, s[i].cols), T = cdiv(m, 256), halves = cdiv(m, kBM);
+    items += T * (T - 1) / 2 * 2 + halves;  // super-tiles above the diagonal: both halves; on it: those inside m
+  }
+  return items < sms ? kBM : kBN;
+}
+
+int use_bn(const dmuon_ctx* h, const dmuon_shape_t* s, int n, bool gram = false) {
+  return use_pairs(h, s, n, gram) ? kBN : choose_bn(h->num_sms, h->tile_mode, h->small_path && h->small_ok, s, n);
+}
+
 int64_t chunk_limit(const dmuon_ctx* h) { return h->chunk_elems > 0 ? h->chunk_elems : kDefaultChunkElems; }
 
 bool same_shapes(const dmuon_ctx* h, const dmuon_shape_t* s, int n, bool gram = false) {
   if ((int)h->shapes.size() != n || !h->small || h->plan_pair != use_pairs(h, s, n, gram) ||
+      h->plan_bn != use_bn(h, s, n, gram) ||
       h->plan_gram != gram ||
       h->plan_small != (h->small_path && h->small_ok) ||
       h->plan_chunk_elems != chunk_limit(h) || h->plan_balanced != h->balanced || h->plan_overlap != (h->overlap && h->chunks.size() > 1))
@@ -324,9 +347,9 @@ int plan_order(const dmuon_shape_t* shapes, int n, bool small_path, std::vector<
 }
 
 // Host-side plan sizes (no device work): workspace of the largest chunk and
-// all device arrays.
+// all device arrays, for CTA pairs or single CTAs of tile width bn.
 void plan_sizes(const dmuon_shape_t* shapes, int n, bool pair, int64_t limit, bool small_path, size_t* ws,
-                size_t* small, bool gram = false) {
+                size_t* small, bool gram = false, int bn = kBN) {
   std::vector<int> order;
   const int n_large = plan_order(shapes, n, small_path, order);
   std::vector<dmuon_shape_t> ps(n);
@@ -336,7 +359,7 @@ void plan_sizes(const dmuon_shape_t* shapes, int n, bool pair, int64_t limit, bo
            rup(sizeof(SmallDesc) * (n - n_large), 256);
   for (const auto& c : split_chunks(ps.data(), n_large, limit)) {
     Layout L;
-    make_layout(ps.data() + c.first, c.second, L, pair, 1, true, gram);  // sizes do not depend on procs
+    make_layout(ps.data() + c.first, c.second, L, pair, 1, true, gram, bn);  // sizes do not depend on procs
     *ws = std::max(*ws, L.ws_bytes);
     *small += chunk_small_bytes(L, c.second);
   }
@@ -350,6 +373,7 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
     return fail(h, DMUON_ERR_UNSUPPORTED, "Gram-space backend needs 2-CTA clusters, unavailable on this device");
   h->plan_gram = gram;
   h->plan_pair = use_pairs(h, shapes, n, gram);
+  h->plan_bn = use_bn(h, shapes, n, gram);
   h->plan_chunk_elems = chunk_limit(h);
   h->plan_balanced = h->balanced;
   h->plan_small = h->small_path && h->small_ok;
@@ -370,7 +394,7 @@ int build_plan(dmuon_ctx* h, const dmuon_shape_t* shapes, int n, bool gram) {
     ch.i0 = parts[c].first;
     ch.n = parts[c].second;
     make_layout(ps.data() + ch.i0, ch.n, ch.L, h->plan_pair, h->plan_pair ? h->max_clusters : h->num_sms,
-                h->plan_balanced, gram);
+                h->plan_balanced, gram, h->plan_bn);
     h->ws_bytes = std::max(h->ws_bytes, ch.L.ws_bytes);
     h->small_bytes += chunk_small_bytes(ch.L, ch.n);
   }
@@ -695,7 +719,7 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
     if (h->plan_pair) {
       if ((e = launch_gemm_pair(kPhaseFused, a, grid, stream)) != cudaSuccess)
         return fail(h, cuda_err(e), "ns_gemm_pair fused launch", e);
-    } else if ((e = launch_gemm(kPhaseFused, a, grid, stream)) != cudaSuccess) {
+    } else if ((e = launch_gemm(kPhaseFused, a, grid, stream, h->plan_bn)) != cudaSuccess) {
       return fail(h, cuda_err(e), "ns_gemm fused launch", e);
     }
     return DMUON_OK;
@@ -732,7 +756,8 @@ int run_chunk_ns(dmuon_ctx* h, const Chunk& ch, const MatPtrs* dptrs, float lr, 
           return fail(h, cuda_err(e), "ns_gemm_pair launch", e);
       } else {
         const int grid = L.procs[p];
-        if ((e = launch_gemm(p, a, grid, stream)) != cudaSuccess) return fail(h, cuda_err(e), "ns_gemm launch", e);
+        if ((e = launch_gemm(p, a, grid, stream, h->plan_bn)) != cudaSuccess)
+          return fail(h, cuda_err(e), "ns_gemm launch", e);
       }
     }
   }
@@ -1188,10 +1213,10 @@ int dmuon_workspace_bytes(const dmuon_shape_t* shapes, int n_mats, size_t* out_b
   // The largest plan over tile kinds, with and without the small-matrix
   // kernel (which needs no workspace).
   size_t most = 0;
-  for (int pair = 0; pair < 2; ++pair)
+  for (int kind = 0; kind < 3; ++kind)  // single CTAs 128 x 256, CTA pairs, single CTAs 128 x 128
     for (int sp = 0; sp < 2; ++sp) {
       size_t ws, sm;
-      plan_sizes(shapes, n_mats, pair != 0, kDefaultChunkElems, sp != 0, &ws, &sm);
+      plan_sizes(shapes, n_mats, kind == 1, kDefaultChunkElems, sp != 0, &ws, &sm, false, kind == 2 ? kBM : kBN);
       most = std::max(most, ws + sm);
     }
   *out_bytes = most;
@@ -1495,7 +1520,7 @@ int dmuon_set_small_path(dmuon_handle_t h, int on) {
 }
 
 int dmuon_set_tile_mode(dmuon_handle_t h, int mode) {
-  if (!h || mode < 0 || mode > 2) return DMUON_ERR_ARG;
+  if (!h || mode < 0 || mode > 3) return DMUON_ERR_ARG;
   if (mode == 2 && h->max_clusters <= 0) return DMUON_ERR_UNSUPPORTED;
   h->tile_mode = mode;
   return DMUON_OK;
@@ -1529,7 +1554,7 @@ int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len) {
   const int n = (int)h->shapes.size();
   std::snprintf(line, sizeof line, "device %d, %d SMs, %d 2-CTA clusters; matrices %d; backend %s; tiles %s; ",
                 h->device, h->num_sms, h->max_clusters, n, h->plan_gram ? "gram" : "direct",
-                h->plan_pair ? "256x256 CTA pairs" : "128x256 single CTAs");
+                h->plan_pair ? "256x256 CTA pairs" : (h->plan_bn == kBM ? "128x128 single CTAs" : "128x256 single CTAs"));
   s += line;
   if (h->small) {
     int64_t tiles = 0;
@@ -1568,7 +1593,7 @@ int dmuon_plan_summary(dmuon_handle_t h, char* buf, size_t len) {
 
 int dmuon_plan_preview(const dmuon_shape_t* shapes, int n_mats, int backend, int tile_mode, int clusters,
                        int sms, int balanced, char* buf, size_t len) {
-  if (n_mats < 0 || (n_mats > 0 && !shapes) || tile_mode < 0 || tile_mode > 2 || clusters < 0 || sms < 1 ||
+  if (n_mats < 0 || (n_mats > 0 && !shapes) || tile_mode < 0 || tile_mode > 3 || clusters < 0 || sms < 1 ||
       (backend != DMUON_BACKEND_DIRECT && backend != DMUON_BACKEND_GRAM) ||
       (backend == DMUON_BACKEND_GRAM && clusters < 1))
     return DMUON_ERR_ARG;
@@ -1580,12 +1605,13 @@ int dmuon_plan_preview(const dmuon_shape_t* shapes, int n_mats, int backend, int
   std::vector<dmuon_shape_t> ps(n_mats);
   for (int k = 0; k < n_mats; ++k) ps[k] = shapes[order[k]];
   const bool pair = choose_pairs(clusters, tile_mode, true, shapes, n_mats, gram);
+  const int bn = pair ? kBN : choose_bn(sms, tile_mode, true, shapes, n_mats);
   const int procs = pair ? clusters : sms;
   size_t items[3] = {0, 0, 0}, chunks = 0;
   double busiest[3] = {0, 0, 0}, mean[3] = {0, 0, 0};
   for (const auto& cc : split_chunks(ps.data(), n_large, kDefaultChunkElems)) {
     Layout L;
-    make_layout(ps.data() + cc.first, cc.second, L, pair, procs, balanced != 0, gram);
+    make_layout(ps.data() + cc.first, cc.second, L, pair, procs, balanced != 0, gram, bn);
     ++chunks;
     for (int q = 0; q < 3; ++q) {
       items[q] += L.items[q].size();
@@ -1598,7 +1624,8 @@ int dmuon_plan_preview(const dmuon_shape_t* shapes, int n_mats, int backend, int
   std::snprintf(line, sizeof line,
                 "matrices %d; backend %s; tiles %s; small-matrix kernel %d; chunks %zu; "
                 "items gram %zu gram2 %zu apply %zu; balance gram %.4f gram2 %.4f apply %.4f",
-                n_mats, gram ? "gram" : "direct", pair ? "256x256 CTA pairs" : "128x256 single CTAs",
+                n_mats, gram ? "gram" : "direct",
+                pair ? "256x256 CTA pairs" : (bn == kBM ? "128x128 single CTAs" : "128x256 single CTAs"),
                 n_mats - n_large, chunks, items[0], items[1], items[2],
                 mean[0] > 0 ? busiest[0] / mean[0] : 1.0, mean[1] > 0 ? busiest[1] / mean[1] : 1.0,
                 mean[2] > 0 ? busiest[2] / mean[2] : 1.0);

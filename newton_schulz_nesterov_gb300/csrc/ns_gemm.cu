@@ -39,23 +39,38 @@ namespace {
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // default: 4 s without progress
 constexpr uint64_t kDrainTimeoutNs = 4000000000ull;  // drains after an abort
 
+// Single-CTA kernel geometry for a tile of 128 rows x BN columns (BN = 256,
+// or 128 for lists too small to fill the SMs with 128 x 256 tiles): B is
+// BN x 64 per K block, so a stage is 48 or 32 KB and 4 or 6 stages fit.
+template <int BN>
+struct SingleCfg {
+  static constexpr int kStageB = kABytes + BN * kBK * 2;
+  static constexpr int kNStages = BN == kBN ? kStages : 6;
+  static constexpr int kSmem = 1024 /*align slack*/ + kNStages * kStageB + 4 * kEpiWords * 4 + 256;
+  static constexpr int kTmem = 2 * BN;  // two accumulators
+};
+static_assert(SingleCfg<kBN>::kSmem == kGemmSmem, "128 x 256 geometry");
+static_assert(SingleCfg<128>::kSmem <= 227 * 1024, "128 x 128 geometry");
+
 struct Smem {
-  uint8_t* stages;     // kStages x (A 16 KB | B 32 KB), 1024-aligned
+  uint8_t* stages;     // stages x (A 16 KB | B BN x 64 x 2), 1024-aligned
   uint32_t* scratch;   // 4 warps x 32 x 17 words
-  uint64_t* bars;      // full[kStages], empty[kStages], tfull[2], tempty[2], drain
+  uint64_t* bars;      // full[stages], empty[stages], tfull[2], tempty[2], drain
   uint32_t* tmem_slot;
   volatile int* abort_flag;
   uint32_t* tile_done;  // fused launches: epilogue warps done per accumulator slot
 };
 
+template <int BN>
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
+  using C = SingleCfg<BN>;
   Smem s;
   const uint32_t a = ptx::smem_addr(raw);
   uint8_t* base = raw + ((1024u - (a & 1023u)) & 1023u);
   s.stages = base;
-  s.scratch = reinterpret_cast<uint32_t*>(base + kStages * kStageBytes);
-  s.bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes + 4 * kEpiWords * 4);
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + 2 * kStages + 5);
+  s.scratch = reinterpret_cast<uint32_t*>(base + C::kNStages * C::kStageB);
+  s.bars = reinterpret_cast<uint64_t*>(base + C::kNStages * C::kStageB + 4 * kEpiWords * 4);
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.bars + 2 * C::kNStages + 5);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
   s.tile_done = s.tmem_slot + 2;
   return s;
@@ -291,13 +306,13 @@ struct CounterCache {
   int mat = -1, val = 0;
 };
 
-template <int PHASE, int MODE>
+template <int PHASE, int MODE, int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const StageParams& sp, const int4 item,
                                               uint32_t tacc, int quad, int lane, uint32_t* scratch) {
   const MatDesc& d = a.mats[item.x];
   const int64_t m = d.m, n = d.n;
   const int64_t row0 = (int64_t)item.y * kBM;
-  const int64_t col0 = (int64_t)item.z * kBN;
+  const int64_t col0 = (int64_t)item.z * BN;
   const int64_t rbase = row0 + quad * 32;
   const int64_t r = rbase + lane;
   const bool row_ok = r < m;
@@ -308,7 +323,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const StagePara
   const float bp = a.bvec[item.x];
   const float xs = sp.first ? a.svec[item.x] : 1.f / bp;
   if constexpr (PHASE == kPhaseGram || PHASE == kPhaseGram2) {
-    const bool mirror = (item.y >> 1) < item.z;
+    // A tile strictly above the diagonal also writes its transpose (diagonal
+    // tiles are computed whole).
+    const bool mirror = (int64_t)item.y * kBM / BN < item.z;
     // Gram: A = kappa xs^2 X[src] X[src]^T.  Gram2 with A = kappa X X^T:
     // b A_true + c A_true^2 = (b/kappa) A + (c/kappa^2) A A.
     const float ik = 1.f / d.kappa;
@@ -317,7 +334,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const StagePara
     __half* dst = (PHASE == kPhaseGram) ? d.A : d.B;
     const int64_t ld = d.lda;
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = 0; ch < BN / 32; ++ch) {
       const int64_t c = col0 + ch * 32;
       if (c >= m) break;  // warp-uniform
       uint32_t v[32];
@@ -352,7 +369,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const StagePara
     const MatPtrs& p = a.ptrs[item.x];
     const float coef = a.lr * d.scale;
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = 0; ch < BN / 32; ++ch) {
       const int64_t c = col0 + ch * 32;
       if (c >= n) break;  // warp-uniform
       uint32_t v[32];
@@ -425,47 +442,49 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const StagePara
 // The epilogue of one item: the launch's own phase, or (fused launches) the
 // item's phase and iteration, the last iteration's Apply in the launch's
 // final mode.
-template <int PHASE, int MODE>
+template <int PHASE, int MODE, int BN>
 __device__ __forceinline__ void epilogue_item(const GemmArgs& a, const ItemInfo& inf, const int4 item, uint32_t tacc,
                                               int quad, int lane, uint32_t* scratch) {
   const StageParams sp = stage_params<PHASE>(a, inf.it);
   if constexpr (PHASE != kPhaseFused) {
-    epilogue_tile<PHASE, MODE>(a, sp, item, tacc, quad, lane, scratch);
+    epilogue_tile<PHASE, MODE, BN>(a, sp, item, tacc, quad, lane, scratch);
   } else {
     if (inf.ph == kPhaseGram) {
-      epilogue_tile<kPhaseGram, kWriteX>(a, sp, item, tacc, quad, lane, scratch);
+      epilogue_tile<kPhaseGram, kWriteX, BN>(a, sp, item, tacc, quad, lane, scratch);
     } else if (inf.ph == kPhaseGram2) {
       // This epilogue reads A tiles that other CTAs stored: an acquire of the
       // matrix's counter (already past this stage's need, which the producer
       // waited for) orders those stores before this thread's loads.
       (void)ld_acquire(a.counters + item.x);
-      epilogue_tile<kPhaseGram2, kWriteX>(a, sp, item, tacc, quad, lane, scratch);
+      epilogue_tile<kPhaseGram2, kWriteX, BN>(a, sp, item, tacc, quad, lane, scratch);
     }
     else if (inf.it < a.n_iters - 1)
-      epilogue_tile<kPhaseApply, kWriteX>(a, sp, item, tacc, quad, lane, scratch);
+      epilogue_tile<kPhaseApply, kWriteX, BN>(a, sp, item, tacc, quad, lane, scratch);
     else if (a.final_mode == kUpdateW)
-      epilogue_tile<kPhaseApply, kUpdateW>(a, sp, item, tacc, quad, lane, scratch);
+      epilogue_tile<kPhaseApply, kUpdateW, BN>(a, sp, item, tacc, quad, lane, scratch);
     else
-      epilogue_tile<kPhaseApply, kWriteO>(a, sp, item, tacc, quad, lane, scratch);
+      epilogue_tile<kPhaseApply, kWriteO, BN>(a, sp, item, tacc, quad, lane, scratch);
   }
 }
 
-template <int PHASE, int MODE>
+template <int PHASE, int MODE, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs a) {
+  using C = SingleCfg<BN>;
+  constexpr int kS = C::kNStages;
   extern __shared__ uint8_t smem_raw[];
-  const Smem sm = carve(smem_raw);
+  const Smem sm = carve<BN>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = a.timeout_ns ? a.timeout_ns : kTimeoutNs;
 
   uint64_t* full = sm.bars;
-  uint64_t* empty = sm.bars + kStages;
-  uint64_t* tfull = sm.bars + 2 * kStages;
-  uint64_t* tempty = sm.bars + 2 * kStages + 2;
-  uint64_t* drain = sm.bars + 2 * kStages + 4;
+  uint64_t* empty = sm.bars + kS;
+  uint64_t* tfull = sm.bars + 2 * kS;
+  uint64_t* tempty = sm.bars + 2 * kS + 2;
+  uint64_t* drain = sm.bars + 2 * kS + 4;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kS; ++s) {
       ptx::mbar_init(ptx::smem_addr(full + s), 1);
       ptx::mbar_init(ptx::smem_addr(empty + s), 1);
     }
@@ -479,7 +498,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(sm.tmem_slot), kTmemCols);
+    ptx::tmem_alloc(ptx::smem_addr(sm.tmem_slot), C::kTmem);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -516,20 +535,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           mapA = maps + 3; mapB = maps + src;
         }
         const int row0 = item.y * kBM;
-        const int col0 = item.z * kBN;
+        const int col0 = item.z * BN;
         for (int kb = 0; kb < inf.kbn; ++kb, ++it) {
-          const uint32_t s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
+          const uint32_t s = it % kS;
+          const uint32_t ph = (it / kS) & 1u;
           if (!wait_bar(ptx::smem_addr(empty + s), ph ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
           const uint32_t fb = ptx::smem_addr(full + s);
-          ptx::mbar_expect_tx(fb, kStageBytes);
-          const uint32_t sa = ptx::smem_addr(sm.stages + s * kStageBytes);
+          ptx::mbar_expect_tx(fb, C::kStageB);
+          const uint32_t sa = ptx::smem_addr(sm.stages + s * C::kStageB);
           const uint32_t sb = sa + kABytes;
           const int k0 = kb * kBK;
           ptx::tma_load_2d(sa, mapA, k0, row0, fb);
           ptx::tma_load_2d(sa + kBoxBytes, mapA, k0, row0 + kBox, fb);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < BN / kBox; ++q) {
             if (inf.ph == kPhaseApply)
               ptx::tma_load_2d(sb + q * kBoxBytes, mapB, col0 + q * kBox, k0, fb);
             else
@@ -540,17 +559,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       if (!ok || *sm.abort_flag) {
         // Drain: wait (bounded, ignoring the abort flag) for the copies of
         // the last issued stages so none lands after the CTA exits.
-        const uint32_t n_out = it < (uint32_t)kStages ? it : (uint32_t)kStages;
+        const uint32_t n_out = it < (uint32_t)kS ? it : (uint32_t)kS;
         for (uint32_t i = it - n_out; i < it; ++i)
-          wait_slow(ptx::smem_addr(full + (i % kStages)), (i / kStages) & 1u, sm.abort_flag,
+          wait_slow(ptx::smem_addr(full + (i % kS)), (i / kS) & 1u, sm.abort_flag,
                     a.err, false, kDrainTimeoutNs);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc_sym = ptx::idesc_f16(kBM, kBN, 0), idesc_app = ptx::idesc_f16(kBM, kBN, 1);
-      constexpr uint32_t bdesc_sym = ptx::idesc_bf16(kBM, kBN, 0), bdesc_app = ptx::idesc_bf16(kBM, kBN, 1);
+      constexpr uint32_t idesc_sym = ptx::idesc_f16(kBM, BN, 0), idesc_app = ptx::idesc_f16(kBM, BN, 1);
+      constexpr uint32_t bdesc_sym = ptx::idesc_bf16(kBM, BN, 0), bdesc_app = ptx::idesc_bf16(kBM, BN, 1);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       bool issued = false;
@@ -561,16 +580,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         const uint32_t acc = tc & 1u;
         if (!wait_bar(ptx::smem_addr(tempty + acc), ((tc >> 1) & 1u) ^ 1u, sm.abort_flag, a.err, tmo)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint32_t dt = tmem_base + acc * kBN;
+        const uint32_t dt = tmem_base + acc * BN;
         const bool mn = inf.ph == kPhaseApply;  // X as the MN-major B operand
         const bool f16 = (PHASE == kPhaseFused ? inf.it : a.iter) < a.f16_iters;
         const uint32_t idesc = f16 ? (mn ? idesc_app : idesc_sym) : (mn ? bdesc_app : bdesc_sym);
         for (int kb = 0; kb < inf.kbn; ++kb, ++it) {
-          const uint32_t s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
+          const uint32_t s = it % kS;
+          const uint32_t ph = (it / kS) & 1u;
           if (!wait_bar(ptx::smem_addr(full + s), ph, sm.abort_flag, a.err, tmo)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_addr(sm.stages + s * kStageBytes);
+          const uint32_t sa = ptx::smem_addr(sm.stages + s * C::kStageB);
           const uint32_t sb = sa + kABytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -602,7 +621,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const uint32_t acc = tc & 1u;
       if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err, tmo)) break;
       ptx::tc_fence_after();
-      epilogue_item<PHASE, MODE>(a, inf, item, tmem_base + acc * kBN, quad, lane, scratch);
+      epilogue_item<PHASE, MODE, BN>(a, inf, item, tmem_base + acc * BN, quad, lane, scratch);
       if (PHASE == kPhaseFused) signal_tile(a.counters + item.x, ptx::smem_addr(sm.tile_done + acc), lane);
       ptx::tc_fence_before();
       __syncwarp();
@@ -614,7 +633,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    ptx::tmem_dealloc(tmem_base, C::kTmem);
   }
 }
 
@@ -811,7 +830,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
       if (!wait_bar(ptx::smem_addr(tfull + acc), (tc >> 1) & 1u, sm.abort_flag, a.err, tmo)) break;
       ptx::tc_fence_after();
       item.y = item.y * 2 + (int)rank;  // this rank's 128-row tile
-      epilogue_item<PHASE, MODE>(a, inf, item, tmem_base + acc * kBN, quad, lane, scratch);
+      epilogue_item<PHASE, MODE, kBN>(a, inf, item, tmem_base + acc * kBN, quad, lane, scratch);
       if (PHASE == kPhaseFused) signal_tile(a.counters + item.x, ptx::smem_addr(sm.tile_done + acc), lane);
       ptx::tc_fence_before();
       __syncwarp();
@@ -830,39 +849,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_pair_kernel(const __g
 
 }  // namespace
 
-template <int PHASE, int MODE>
-cudaError_t configure_one() {
-  return cudaFuncSetAttribute(ns_gemm_kernel<PHASE, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kGemmSmem);
+template <int BN>
+cudaError_t configure_bn() {
+  constexpr int sm = SingleCfg<BN>::kSmem;
+  const cudaFuncAttribute att = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(ns_gemm_kernel<kPhaseGram, kWriteX, BN>, att, sm)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(ns_gemm_kernel<kPhaseGram2, kWriteX, BN>, att, sm)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(ns_gemm_kernel<kPhaseApply, kWriteX, BN>, att, sm)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(ns_gemm_kernel<kPhaseApply, kUpdateW, BN>, att, sm)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(ns_gemm_kernel<kPhaseFused, kWriteX, BN>, att, sm)) != cudaSuccess) return e;
+  return cudaFuncSetAttribute(ns_gemm_kernel<kPhaseApply, kWriteO, BN>, att, sm);
 }
 
 cudaError_t gemm_configure() {
-  cudaError_t e;
-  if ((e = configure_one<kPhaseGram, kWriteX>()) != cudaSuccess) return e;
-  if ((e = configure_one<kPhaseGram2, kWriteX>()) != cudaSuccess) return e;
-  if ((e = configure_one<kPhaseApply, kWriteX>()) != cudaSuccess) return e;
-  if ((e = configure_one<kPhaseApply, kUpdateW>()) != cudaSuccess) return e;
-  if ((e = configure_one<kPhaseFused, kWriteX>()) != cudaSuccess) return e;
-  return configure_one<kPhaseApply, kWriteO>();
+  const cudaError_t e = configure_bn<kBN>();
+  return e != cudaSuccess ? e : configure_bn<128>();
 }
 
 // Apply launches pick the kernel variant of their final mode, so each
 // variant carries only the epilogue it runs.
-cudaError_t launch_gemm(int phase, const GemmArgs& a, int grid, cudaStream_t s) {
+template <int BN>
+cudaError_t launch_bn(int phase, const GemmArgs& a, int grid, cudaStream_t s) {
+  constexpr int sm = SingleCfg<BN>::kSmem;
   if (phase == kPhaseFused) {
-    ns_gemm_kernel<kPhaseFused, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+    ns_gemm_kernel<kPhaseFused, kWriteX, BN><<<grid, kGemmThreads, sm, s>>>(a);
   } else if (phase == kPhaseGram) {
-    ns_gemm_kernel<kPhaseGram, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+    ns_gemm_kernel<kPhaseGram, kWriteX, BN><<<grid, kGemmThreads, sm, s>>>(a);
   } else if (phase == kPhaseGram2) {
-    ns_gemm_kernel<kPhaseGram2, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+    ns_gemm_kernel<kPhaseGram2, kWriteX, BN><<<grid, kGemmThreads, sm, s>>>(a);
   } else if (a.final_mode == kUpdateW) {
-    ns_gemm_kernel<kPhaseApply, kUpdateW><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+    ns_gemm_kernel<kPhaseApply, kUpdateW, BN><<<grid, kGemmThreads, sm, s>>>(a);
   } else if (a.final_mode == kWriteO) {
-    ns_gemm_kernel<kPhaseApply, kWriteO><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+    ns_gemm_kernel<kPhaseApply, kWriteO, BN><<<grid, kGemmThreads, sm, s>>>(a);
   } else {
-    ns_gemm_kernel<kPhaseApply, kWriteX><<<grid, kGemmThreads, kGemmSmem, s>>>(a);
+    ns_gemm_kernel<kPhaseApply, kWriteX, BN><<<grid, kGemmThreads, sm, s>>>(a);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(int phase, const GemmArgs& a, int grid, cudaStream_t s, int bn) {
+  return bn == 128 ? launch_bn<128>(phase, a, grid, s) : launch_bn<kBN>(phase, a, grid, s);
 }
 
 template <int PHASE, int MODE>

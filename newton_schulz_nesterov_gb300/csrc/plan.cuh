@@ -77,8 +77,9 @@ inline void deal_items(std::vector<int4>& items, int procs, bool balanced, std::
 // (m x m fp16) per matrix.  Gram plans: X[0], X[1] and the kGramBufs m x m
 // fp16 buffers of the Gram-space window (R[2], Z[2], W, Q[2], the window's
 // last Q).
+// bn (single CTAs only): 256 for 128 x 256 tiles, 128 for 128 x 128 tiles.
 inline void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair, int procs, bool balanced,
-                 bool gram = false) {
+                 bool gram = false, int bn = kBN) {
   L.mats.assign(n, MatDesc{});
   L.xoff.resize(n); L.aoff.resize(n); L.boff.resize(n);
   L.goff.assign(gram ? (size_t)n * kGramBufs : 0, -1);
@@ -111,7 +112,7 @@ inline void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair
   L.ws_bytes = off;
   // Work lists.  Symmetric phases: 256x256 super-tiles (I <= J); Apply: the
   // m x n output.  CTA pairs take a whole 256x256 tile per item; single CTAs
-  // take one 128-row half of it.
+  // take one 128-row half of it, or with 128-column tiles a 128 x 128 block.
   for (int p = 0; p < 3; ++p) L.items[p].clear();
   for (int i = 0; i < n; ++i) {
     MatDesc& d = L.mats[i];
@@ -131,17 +132,28 @@ inline void make_layout(const dmuon_shape_t* shapes, int n, Layout& L, bool pair
       d.apply_items = (int32_t)(L.items[kPhaseApply].size() - app0);
       continue;
     }
-    for (int64_t I = 0; I < T; ++I)
-      for (int64_t J = I; J < T; ++J)
-        for (int h = 0; h < 2; ++h) {
-          const int64_t ti = 2 * I + h;
-          if (ti * kBM >= d.m) continue;
-          L.items[kPhaseGram].push_back(make_int4(i, (int)ti, (int)J, kg));
-          L.items[kPhaseGram2].push_back(make_int4(i, (int)ti, (int)J, km));
+    if (bn == kBM) {
+      // 128 x 128 tiles: blocks (I, J) with I <= J; those above the diagonal
+      // also store their transpose.
+      const int64_t T1 = cdiv(d.m, kBM);
+      for (int64_t I = 0; I < T1; ++I)
+        for (int64_t J = I; J < T1; ++J) {
+          L.items[kPhaseGram].push_back(make_int4(i, (int)I, (int)J, kg));
+          L.items[kPhaseGram2].push_back(make_int4(i, (int)I, (int)J, km));
         }
-    // Column-panel-major: CTAs running together share 256-column panels of
-    // X (each read from DRAM once) while B (m x m) stays resident in L2.
-    for (int64_t tj = 0; tj < cdiv(d.n, kBN); ++tj)
+    } else {
+      for (int64_t I = 0; I < T; ++I)
+        for (int64_t J = I; J < T; ++J)
+          for (int h = 0; h < 2; ++h) {
+            const int64_t ti = 2 * I + h;
+            if (ti * kBM >= d.m) continue;
+            L.items[kPhaseGram].push_back(make_int4(i, (int)ti, (int)J, kg));
+            L.items[kPhaseGram2].push_back(make_int4(i, (int)ti, (int)J, km));
+          }
+    }
+    // Column-panel-major: CTAs running together share column panels of X
+    // (each read from DRAM once) while B (m x m) stays resident in L2.
+    for (int64_t tj = 0; tj < cdiv(d.n, bn); ++tj)
       for (int64_t ti = 0; ti < cdiv(d.m, kBM); ++ti)
         L.items[kPhaseApply].push_back(make_int4(i, (int)ti, (int)tj, km));
     d.sym_items = (int32_t)(L.items[kPhaseGram].size() - sym0);

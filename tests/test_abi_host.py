@@ -309,17 +309,41 @@ def test_plan_preview_items_dealing_and_chunks(lib):
     assert gb["chunks"] == 14 and gb["items"] == _pair_items(full)
 
 
+def _narrow_items(shapes):
+    """Work items of a 128 x 128 single-CTA plan from their definition: blocks
+    (I, J), I <= J, of the m x m products; all 128 x 128 output tiles of the
+    m x n iterate for the apply phase."""
+    cd = lambda a, b: -(-a // b)  # noqa: E731
+    g = a = 0
+    for r, c in shapes:
+        m, n = min(r, c), max(r, c)
+        T = cd(m, 128)
+        g += T * (T + 1) // 2
+        a += T * cd(n, 128)
+    return {"gram": g, "gram2": g, "apply": a}
+
+
 def test_plan_preview_tile_choice(lib):
     """Automatic tiles: CTA pairs only when some chunked matrix's short side
     exceeds 128 and there is at least one Gram super-tile per pair; small
-    matrices go to the small-matrix kernel and do not count."""
+    matrices go to the small-matrix kernel and do not count.  Single CTAs
+    take 128 x 128 tiles when the 128 x 256 Gram items would not cover the
+    SMs, else 128 x 256."""
     d512 = workloads.get("tinymlp_d512").shapes            # 12 x 3 = 36 super-tiles
-    assert "single CTAs" in _preview(d512)[0]               # 36 < 76 pairs
+    out, p = _preview(d512)                                 # 36 < 76 pairs; 72 halves < 152 SMs
+    assert p["tiles"] == "128x128 single CTAs" and p["items"] == _narrow_items(d512)
+    assert p["items"] == {"gram": 120, "gram2": 120, "apply": 768}
     assert "CTA pairs" in _preview(d512, clusters=36)[0]
-    assert "single CTAs" in _preview(d512, clusters=37)[0]
+    assert "128x128 single CTAs" in _preview(d512, clusters=37)[0]
+    assert "128x256 single CTAs" in _preview(d512, tile_mode=1)[0]
+    assert "128x128 single CTAs" in _preview(d512, tile_mode=3)[0]
+    assert "128x256 single CTAs" in _preview(d512, sms=72)[0]           # 72 halves cover 72 SMs
+    assert "128x128 single CTAs" in _preview(d512, sms=73)[0]
     assert "CTA pairs" in _preview(d512, tile_mode=2)[0]
-    assert "single CTAs" in _preview(workloads.get("llama3_8b_1layer").shapes, tile_mode=1)[0]
+    assert "128x256 single CTAs" in _preview(workloads.get("llama3_8b_1layer").shapes, tile_mode=1)[0]
+    assert "128x128 single CTAs" in _preview(workloads.get("llama3_8b_1layer").shapes, tile_mode=3)[0]
     assert "single CTAs" in _preview(d512, clusters=0, tile_mode=0)[0]
+    assert "128x256 single CTAs" in _preview(list(d512) * 4, clusters=0)[0]   # 288 halves >= 152
     _, s = _preview(workloads.get("tinymlp_d128").shapes)
     assert s["small"] == 12 and s["chunks"] == 0
     _, t = _preview(workloads.get("tp_70b_mixed").shapes)
@@ -333,7 +357,7 @@ def test_plan_preview_argument_errors(lib):
     f = lib.dmuon_plan_preview
     assert f(sh, 1, 1, 0, 0, 152, 1, None, 0) == -1      # Gram backend without clusters
     assert f(sh, 1, 7, 0, 76, 152, 1, None, 0) == -1     # unknown backend
-    assert f(sh, 1, 0, 3, 76, 152, 1, None, 0) == -1     # unknown tile mode
+    assert f(sh, 1, 0, 4, 76, 152, 1, None, 0) == -1     # unknown tile mode
     assert f(sh, 1, 0, 0, 76, 0, 1, None, 0) == -1       # no SMs
     assert f(None, 1, 0, 0, 76, 152, 1, None, 0) == -1
     sh[0].rows = 0

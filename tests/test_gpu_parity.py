@@ -123,11 +123,12 @@ def test_newton_schulz_ragged_shapes(handle):
         assert e <= NS_TOL, (s, e)
 
 
-@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("mode", [1, 2, 3])
 def test_tile_modes_match_oracle(handle, mode):
-    """Single-CTA 128x256 tiles (mode 1) and CTA-pair 256x256 tiles (mode 2)
-    both meet the bar on ragged shapes and a full step (the small-matrix
-    kernel off, so that the small shapes run through these tiles too)."""
+    """Single-CTA 128x256 tiles (mode 1), CTA-pair 256x256 tiles (mode 2) and
+    single-CTA 128x128 tiles (mode 3) all meet the bar on ragged shapes and a
+    full step (the small-matrix kernel off, so that the small shapes run
+    through these tiles too)."""
     gen = torch.Generator().manual_seed(23)
     ins = [torch.randn(s, generator=gen) for s in RAGGED]
     outs = [torch.empty(s, device="cuda") for s in RAGGED]
@@ -137,6 +138,7 @@ def test_tile_modes_match_oracle(handle, mode):
         h2.newton_schulz(_to_dev(ins), outs)
         assert h2.status()[0] == 0
         assert (("pairs" in dm.dmuon_plan_summary(h2.h)) == (mode == 2))
+        assert (("128x128" in dm.dmuon_plan_summary(h2.h)) == (mode == 3))
         for x, o, s in zip(ins, outs, RAGGED):
             e = rel_fro(o.cpu().numpy(), oracle.newton_schulz(x.numpy()))
             assert e <= NS_TOL, (mode, s, e)
@@ -156,12 +158,13 @@ SINGLE_TERM_ROWS = [(1.0, 0.0, 0.0), (1.0 / 64, 1.0, 0.0), (1.0 / 64, 0.0, 1.0),
 TERM_SHAPES = {
     "pair": [(1, 300), (300, 1), (64, 64), (130, 700), (700, 130), (257, 257), (520, 520)],
     "single": [(1, 300), (64, 64), (130, 700), (700, 130), (257, 257)],
+    "narrow": [(1, 300), (64, 64), (130, 700), (700, 130), (257, 257), (300, 520)],
     "small": [(1, 300), (300, 1), (64, 64), (100, 500), (500, 100), (128, 128)],
     "gram": [(1, 300), (64, 64), (130, 700), (700, 130), (257, 257), (520, 1100)],
 }
 
 
-@pytest.mark.parametrize("path", ["pair", "single", "small", "gram"])
+@pytest.mark.parametrize("path", ["pair", "single", "narrow", "small", "gram"])
 @pytest.mark.parametrize("row", SINGLE_TERM_ROWS)
 def test_each_term_of_the_step(path, row):
     """One Newton-Schulz step with one term of X' = aX + b(XX^T)X + c(XX^T)^2 X
@@ -184,6 +187,8 @@ def test_each_term_of_the_step(path, row):
             dm.dmuon_set_tile_mode(h2.h, 2)
         if path == "single":
             dm.dmuon_set_tile_mode(h2.h, 1)
+        if path == "narrow":
+            dm.dmuon_set_tile_mode(h2.h, 3)
         if path != "small":
             dm.dmuon_set_small_path(h2.h, False)
         if path == "gram":
@@ -420,7 +425,7 @@ def test_items_dealt_evenly_for_one_llama_layer():
     assert rel_fro(Ws[1].cpu().numpy() - W1.numpy(), ref["W"] - W1.numpy()) <= NS_TOL
 
 
-@pytest.mark.parametrize("backend,tiles", [("direct", 2), ("direct", 1), ("gram", 2)])
+@pytest.mark.parametrize("backend,tiles", [("direct", 2), ("direct", 1), ("direct", 3), ("gram", 2)])
 def test_dealing_is_bitwise_neutral(backend, tiles):
     """Balanced and strided dealing of the same plan give bitwise equal
     weights and momenta (mixed K: tall, wide, square and ragged matrices in
@@ -603,7 +608,7 @@ def test_launch_count_and_profile(handle, fused):
     assert handle.status()[0] == 0
 
 
-@pytest.mark.parametrize("tiles", [1, 2])
+@pytest.mark.parametrize("tiles", [1, 2, 3])
 def test_fused_phases_bitwise_equal_per_phase_launches(tiles):
     """One fused launch per chunk runs the same tiles with the same
     arithmetic as one launch per phase and iteration: weights and momenta
