@@ -65,8 +65,14 @@ __global__ void __launch_bounds__(256, kMomCtasPerSm) mom_norm_kernel(const MomA
     if (!any) return;
   }
 
+  int mi = 0;
+  int64_t mt0 = 0, mt1 = 0;  // tiles of matrix mi: the search is skipped while t stays inside
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
-    const int mi = find_mat(a.tile_prefix, a.n_mats, t);
+    if (t < mt0 || t >= mt1) {
+      mi = find_mat(a.tile_prefix, a.n_mats, t);
+      mt0 = __ldg(a.tile_prefix + mi);
+      mt1 = __ldg(a.tile_prefix + mi + 1);
+    }
     if (redo_pass && !a.redo[mi]) continue;  // uniform over the CTA
     const MatDesc& d = a.mats[mi];
     const MatPtrs& p = a.ptrs[mi];
