@@ -87,7 +87,7 @@ constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
-constexpr int kBox = 64;                        // TMA box is 64 x 64 bf16
+constexpr int kBox = 64;                        // TMA box is 64 x 64 16-bit values
 constexpr int kBoxBytes = kBox * kBox * 2;      // 8 KB
 constexpr int kGemmThreads = 192;               // TMA, MMA, 4 epilogue warps
 constexpr int kTmemCols = 512;                  // two 128x256 fp32 accumulators

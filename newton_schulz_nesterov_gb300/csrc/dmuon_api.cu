@@ -172,7 +172,7 @@ struct dmuon_ctx {
 
 namespace {
 
-// Default chunk: up to 2^29 matrix elements (1 GiB per bf16 iterate buffer).
+// Default chunk: up to 2^29 matrix elements (1 GiB per 16-bit iterate buffer).
 // Running the 2 + 3*ns_steps launches over a few layers' worth of matrices at
 // a time, instead of the whole list, measured ~6 % faster on the Llama-3-8B
 // set and bounds the workspace by the largest chunk.

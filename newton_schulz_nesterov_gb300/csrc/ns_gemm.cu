@@ -14,15 +14,18 @@
 // CTA layout (192 threads, one CTA per SM, persistent over a static run of
 // work items dealt by the host, longest first to the least-loaded CTA):
 //   warp 0   TMA producer: 64-wide K blocks of both operands into a
-//            4-stage shared-memory ring (128-byte swizzle, 64x64 boxes)
+//            shared-memory ring (128-byte swizzle, 64x64 boxes)
 //   warp 1   TMEM allocator and single-thread tcgen05.mma issuer
-//            (M=128, N=256, K=16 per instruction, fp32 accumulate)
+//            (M=128, N=256 or 128, K=16 per instruction, fp32 accumulate)
 //   warps 2-5 epilogue: TMEM -> registers, fused scaling / a*X / b*A terms,
-//            fp16 stores (direct and mirrored) or the fp32 weight update
-// Operands are fp16 (kind::f16 with fp16 A and B, fp32 accumulate); every
-// stored buffer carries a power-of-two scale (MatDesc) that keeps its
-// entries in fp16's normal range, undone in the epilogues.
-// Two 256-column accumulators in TMEM let the epilogue of one tile overlap
+//            16-bit stores (direct and mirrored) or the fp32 weight update
+// Single CTAs take 128 x 256 tiles (4 stages of 48 KB) or, for lists too
+// small to fill the SMs, 128 x 128 tiles (6 stages of 32 KB); CTA pairs
+// (cta_group::2, below) take 256 x 256 tiles.
+// Operands are fp16 in the first iterations and bf16 after (kind::f16,
+// fp32 accumulate); every stored buffer carries a power-of-two scale
+// (MatDesc) that keeps its entries in fp16's normal range, undone in the
+// epilogues.  Two accumulators in TMEM let the epilogue of one tile overlap
 // the main loop of the next.
 //
 // Every mbarrier wait is bounded (GemmArgs::timeout_ns, default 4 s without

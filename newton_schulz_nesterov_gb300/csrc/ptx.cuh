@@ -51,7 +51,7 @@ __device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
 
 // ---------------------------------------------------------------- TMA
 // 2-D tile load of one box into shared memory, completing bytes on `bar`.
-// x (inner coordinate, elements) must be a multiple of 8 for bf16.
+// x (inner coordinate, elements) must be a multiple of 8 for 16-bit types.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
   asm volatile(
