@@ -149,6 +149,33 @@ def test_tile_modes_match_oracle(handle, mode):
         _step_and_check(h2, Ws, Gs, Ms)
 
 
+@pytest.mark.parametrize("mode", [1, 3])
+@pytest.mark.parametrize("seed", [61, 62])
+def test_single_cta_tiles_random_lists(mode, seed):
+    """Seeded random lists (short sides 1-700 on both sides of every 128 and
+    256 boundary, long sides up to 1500, both orientations) with 1-7 steps
+    and the fused and per-phase launches, on 128x256 (mode 1) and 128x128
+    (mode 3) single-CTA tiles, against the fp64 oracle."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for _ in range(9):
+        m = int(rng.choice([int(rng.integers(1, 700)), 128, 129, 255, 256, 257, 383, 384, 385]))
+        n = int(rng.integers(m, 1500))
+        shapes.append((m, n) if rng.random() < 0.5 else (n, m))
+    gen = torch.Generator().manual_seed(seed)
+    Ws = [torch.rand(sh, generator=gen) - 0.5 for sh in shapes]
+    Gs = [torch.randn(sh, generator=gen) for sh in shapes]
+    Ms = [torch.randn(sh, generator=gen) for sh in shapes]
+    ns = int(rng.integers(1, 8))
+    for fused in (True, False):
+        with dm.Handle(0) as h2:
+            dm.dmuon_set_tile_mode(h2.h, mode)
+            dm.dmuon_set_small_path(h2.h, False)
+            dm.dmuon_set_fused_phases(h2.h, fused)
+            _step_and_check(h2, Ws, Gs, Ms, ns_steps=ns)
+            assert ("128x128" in dm.dmuon_plan_summary(h2.h)) == (mode == 3)
+
+
 # Rows isolating each term.  Every row keeps a >= 1/64 (the library refuses rows without the
 # identity part, which the unscaled fp16 Z needs); with the inputs below -- rank two plus a little
 # noise, normalised singular values ~0.83 and ~0.55 -- the b and c terms of the second and third
