@@ -463,7 +463,8 @@ def dmuon_set_small_path(h, on=True):  # default on in the library
 
 
 def dmuon_set_tile_mode(h, mode):
-    """0 automatic (CTA pairs), 1 single-CTA 128x256 tiles, 2 CTA-pair 256x256 tiles."""
+    """0 automatic, 1 single-CTA 128x256 tiles, 2 CTA-pair 256x256 tiles,
+    3 single-CTA 128x128 tiles."""
     _check(load().dmuon_set_tile_mode(h, int(mode)), "dmuon_set_tile_mode")
 
 
