@@ -77,41 +77,42 @@ __global__ void __launch_bounds__(256) adamw_kernel(const AdamWArgs a) {
 }
 
 // Per-tile sum of squares in a fixed order: each thread runs over a fixed
-// subset, then a shuffle tree and the warps in order.
-__global__ void __launch_bounds__(256) sumsq_kernel(const ClipArgs a) {
+// subset (elements threadIdx.x, +256, +512, ... of the tile, in that order),
+// then a shuffle tree and the warps in order.  Four CTAs per SM with up to 64
+// registers a thread, so that a whole tile's loads (eight 16-byte reads per
+// thread) are in flight before any is summed.
+constexpr int kSumsqCtasPerSm = 4;
+__global__ void __launch_bounds__(256, kSumsqCtasPerSm) sumsq_kernel(const ClipArgs a) {
   __shared__ float red[8];
+  int ti = 0;
+  int64_t t0 = 0, t1 = 0;  // tiles of tensor ti: the search is skipped while t stays inside
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
-    const int ti = find_tensor(a.tile_prefix, a.n, t);
+    if (t < t0 || t >= t1) {
+      ti = find_tensor(a.tile_prefix, a.n, t);
+      t0 = __ldg(a.tile_prefix + ti);
+      t1 = __ldg(a.tile_prefix + ti + 1);
+    }
     const FlatDesc& d = a.descs[ti];
-    const int64_t base = (t - a.tile_prefix[ti]) * kFlatTile;
+    const int64_t base = (t - t0) * kFlatTile;
     const int64_t len = min((int64_t)kFlatTile, d.numel - base);
     float ss = 0.f;
     if (d.vec4) {
-      // Four float4 per thread per round (a full tile is 2048 float4 over 256
-      // threads = 2 rounds), all loaded before any is summed so that four
-      // 16-byte reads per thread are in flight.
+      // A full tile is 2048 float4 over 256 threads: 8 per thread.
+      constexpr int kPer = kFlatTile / 4 / 256;
       const float4* g4 = reinterpret_cast<const float4*>(d.g + base);
       const int64_t nv = len / 4;
-      const int64_t bd = blockDim.x;
-      int64_t i = threadIdx.x;
-      for (; i + 3 * bd < nv; i += 4 * bd) {
-        float4 q[4];
+      float4 q[kPer];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) q[k] = __ldcs(g4 + i + k * bd);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          ss = fmaf(q[k].x, q[k].x, ss);
-          ss = fmaf(q[k].y, q[k].y, ss);
-          ss = fmaf(q[k].z, q[k].z, ss);
-          ss = fmaf(q[k].w, q[k].w, ss);
-        }
+      for (int k = 0; k < kPer; ++k) {
+        const int64_t i = threadIdx.x + (int64_t)k * 256;
+        q[k] = i < nv ? __ldcs(g4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      for (; i < nv; i += bd) {
-        const float4 a = __ldcs(g4 + i);
-        ss = fmaf(a.x, a.x, ss);
-        ss = fmaf(a.y, a.y, ss);
-        ss = fmaf(a.z, a.z, ss);
-        ss = fmaf(a.w, a.w, ss);
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        ss = fmaf(q[k].x, q[k].x, ss);
+        ss = fmaf(q[k].y, q[k].y, ss);
+        ss = fmaf(q[k].z, q[k].z, ss);
+        ss = fmaf(q[k].w, q[k].w, ss);
       }
     } else {
       for (int64_t i = threadIdx.x; i < len; i += blockDim.x) {
@@ -158,12 +159,18 @@ __global__ void __launch_bounds__(256) clip_finalize_kernel(const ClipArgs a) {
 }
 
 __global__ void __launch_bounds__(256) clip_scale_kernel(const ClipArgs a) {
+  int ti = 0;
+  int64_t t0 = 0, t1 = 0;
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
-    const int ti = find_tensor(a.tile_prefix, a.n, t);
+    if (t < t0 || t >= t1) {
+      ti = find_tensor(a.tile_prefix, a.n, t);
+      t0 = __ldg(a.tile_prefix + ti);
+      t1 = __ldg(a.tile_prefix + ti + 1);
+    }
     const FlatDesc& d = a.descs[ti];
     const float c = a.coefs[d.bucket];
     if (!(c >= 0.f && c < 1.f)) continue;  // no clipping for this bucket (NaN too)
-    const int64_t base = (t - a.tile_prefix[ti]) * kFlatTile;
+    const int64_t base = (t - t0) * kFlatTile;
     const int64_t len = min((int64_t)kFlatTile, d.numel - base);
     float* g = const_cast<float*>(d.g) + base;
     if (d.vec4) {
@@ -187,7 +194,9 @@ cudaError_t launch_adamw(const AdamWArgs& a, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_clip(const ClipArgs& a, int grid, cudaStream_t s) {
-  sumsq_kernel<<<grid, 256, 0, s>>>(a);
+  // grid: up to eight CTAs per SM; the sum of squares keeps half of them
+  // resident (its launch bound) and strides over the tiles.
+  sumsq_kernel<<<(grid + 1) / 2, 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   clip_finalize_kernel<<<a.n_buckets, 256, 0, s>>>(a);
